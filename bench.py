@@ -1,0 +1,418 @@
+"""Benchmark of the rolling-KV step: stream-steps/s (all layers) and decode-attention HBM GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload qwen] [--impl ours|reference]
+
+One step = the whole hot path for every active stream and every layer: begin
+step (ring bookkeeping + RoPE angles), then per layer the exact re-base (exact
+scheme), RoPE + append, and split-K decode attention with its merge.  The
+timed steps replay CUDA graphs of `rkv_step` over inputs already resident in
+HBM; the window is full before timing starts (steady state).  Under torchrun
+every rank runs its own copy of the workload (streams are independent: no
+collective on the data path) and `value` sums all ranks' stream-steps over
+the slowest rank's time.
+
+The reference arm (`--impl reference`) times the fp64 CPU oracle on this
+host's cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "stream-steps/sec (all layers) and decode-attn HBM GB/s as % of B300 peak"
+UNIT = "stream-steps/s"
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--workload", default="qwen", choices=["tiny", "qwen", "voxtral", "encoder", "mixed"])
+    p.add_argument("--scheme", default=None, choices=[None, "offset", "exact"])
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--inputs", type=int, default=4, help="distinct resident input sets cycled by the steps")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def describe(wl, scheme_name):
+    w = sorted(set(wl.windows().tolist()))
+    return (f"{wl.name}: {wl.n_layers} layers, {wl.n_streams} streams, Hq={wl.n_q_heads} Hkv={wl.n_kv_heads} "
+            f"d={wl.head_dim}, Q={wl.q_per_step}, W={'/'.join(map(str, w))}, {scheme_name}, "
+            f"P0<{wl.p0_high or 1}, inputs N(0,1){' x 1/sqrt(d)' if wl.scale_inputs else ''} bf16")
+
+
+def algorithmic_attn_bytes(wl, lens):
+    """Bytes decode attention must move for one layer: K+V of the window, q in, out, lse."""
+    Q, hq, hkv, d = wl.q_per_step, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    kv = sum(2 * int(n) * hkv * d * 2 for n in lens)
+    return kv + len(lens) * (Q * hq * d * 2 * 2 + Q * hq * 4)
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id  # nvidia-smi --id: the device's UUID ("GPU-...")
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            self.proc.wait(timeout=5)
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                        rows.append(parts)
+        finally:
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(float(r[1]) for r in rows),
+                "sm_max_mhz": max(float(r[2]) for r in rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit()) if rows else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6400.0, "fallback"
+
+
+# ---------------------------------------------------------------- oracle legs
+
+def _oracle_chunk(args):
+    """Oracle evaluation of consecutive steps of one stream, all layers (runs in a worker process)."""
+    name, stream, n0, n_steps, layers = args
+    import synth
+    from oracle.attention import attention_step
+    wl = synth.workload(name)
+    Q, hq, hkv, d = wl.q_per_step, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    w = int(wl.windows()[stream])
+    p0 = int(wl.start_offsets()[stream])
+    sc = wl.input_scale
+    done = 0
+    for i in range(n_steps):
+        n_old = n0 + i * Q
+        toks = list(range(max(0, n_old + Q - w), n_old + Q))
+        for layer in layers:
+            qb = synth.token_tensor(wl.seed, synth.TAG_Q, stream, layer, range(n_old, n_old + Q), hq, d, sc)
+            kb = synth.token_tensor(wl.seed, synth.TAG_K, stream, layer, toks, hkv, d, sc)
+            vb = synth.token_tensor(wl.seed, synth.TAG_V, stream, layer, toks, hkv, d, sc)
+            attention_step(synth.bf16_bits_to_f64(qb), synth.bf16_bits_to_f64(kb), synth.bf16_bits_to_f64(vb),
+                           toks, n_old, p0, w, 1.0 / math.sqrt(d), wl.rope_theta)
+            done += 1
+    return done
+
+
+def oracle_timing(wl, budget_s, steps_per_chunk=4):
+    """Time the oracle on all host cores (spawned workers) on a bounded sample.
+
+    Each chunk is `steps_per_chunk` consecutive full-window steps of one
+    stream over a subset of layers; chunks are issued until the budget is
+    spent.  Returns stream-steps/s (all layers), extrapolated from
+    stream-layer-steps/s.
+    """
+    import multiprocessing as mp
+    cores = os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    w = int(wl.windows().max())
+    n0 = (w // wl.q_per_step + 3) * wl.q_per_step     # steady state: window full
+    layers = list(range(0, wl.n_layers, max(1, wl.n_layers // 4)))[:4]
+    with ctx.Pool(cores) as pool:
+        pool.map(_oracle_chunk, [(wl.name, 0, n0, 1, [0])] * cores)   # import + warm caches
+        t0 = time.perf_counter()
+        done = 0
+        jobs = 0
+        while time.perf_counter() - t0 < budget_s:
+            batch = [(wl.name, (jobs + i) % wl.n_streams, n0 + 64 * wl.q_per_step * ((jobs + i) // wl.n_streams),
+                      steps_per_chunk, layers) for i in range(cores)]
+            done += sum(pool.map(_oracle_chunk, batch))
+            jobs += cores
+        elapsed = time.perf_counter() - t0
+    rate_layer_steps = done / elapsed
+    return {"value": rate_layer_steps / wl.n_layers, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"{done} full-window stream-layer-steps ({len(layers)} of {wl.n_layers} layers, "
+                       f"{steps_per_chunk} consecutive steps per stream) in {elapsed:.1f} s on {cores} spawned "
+                       f"processes; value = stream-layer-steps/s / {wl.n_layers} layers (extrapolated)")}
+
+
+def run_reference(args):
+    import synth
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    wl = synth.workload(args.workload)
+    scheme = args.scheme or ("exact" if wl.scheme == 1 else "offset")
+    # each step is a bounded sample: the whole run stays within about two minutes
+    per_step = max(0.02, min(1.0, 110.0 / max(1, args.steps + args.warmup)))
+    base = oracle_timing(wl, per_step * args.steps)
+    line = {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * wl.n_streams / base["value"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": describe(wl, scheme), "parallelism": "replicas"},
+            "cpu_baseline": base,
+            "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU leg
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import rolling_kv_sliding_rkv_b300 as rkv
+    import synth
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = synth.workload(args.workload)
+    if args.scheme:
+        wl = synth.workload(args.workload, scheme=1 if args.scheme == "exact" else 0)
+    scheme_name = "exact re-base" if wl.scheme == 1 else "offset-only"
+    S, L, Q, hq, hkv, d = wl.n_streams, wl.n_layers, wl.q_per_step, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    windows = wl.windows()
+    h = rkv.RollingKV(windows.tolist(), wl.start_offsets().tolist(), device=dev, n_layers=L, n_streams=S,
+                      n_q_heads=hq, n_kv_heads=hkv, head_dim=d, q_per_step=Q, scheme=wl.scheme,
+                      rebase_interval=wl.rebase_interval, rope_theta=wl.rope_theta)
+    if wl.tick_ms:
+        raise SystemExit("the mixed-clock workload is a parity case; bench the others")
+    active = list(range(S))
+    A = len(active)
+    nq, nkv = L * A * Q * hq * d, L * A * Q * hkv * d
+    R = max(1, args.inputs)
+    qs = [torch.empty(nq, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    ks = [torch.empty(nkv, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    vs = [torch.empty(nkv, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    outs = [torch.empty(nq, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    lses = [torch.empty(nq // d, dtype=torch.float32, device=dev) for _ in range(R)]
+    for r in range(R):
+        for tag, buf in ((synth.TAG_Q, qs[r]), (synth.TAG_K, ks[r]), (synth.TAG_V, vs[r])):
+            rkv.rkv_gen_tokens(wl.seed + 1000 * rank, tag, r, 0, 0, 1, buf.numel(), wl.input_scale, buf)
+    torch.cuda.synchronize()
+
+    # one CUDA graph per resident input set, each one full step of all layers
+    stream = torch.cuda.Stream()
+    graphs = []
+    with torch.cuda.stream(stream):
+        for r in range(R):      # eager warm-up of the capture stream
+            h.step(active, qs[r], ks[r], vs[r], outs[r], lses[r])
+        stream.synchronize()
+        for r in range(R):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                h.step(active, qs[r], ks[r], vs[r], outs[r], lses[r])
+            graphs.append(g)
+    launches_per_step = 1 + L * ((1 if wl.scheme == 1 else 0) + 1 + 2)
+
+    # fill the window, then warm up: steady state before timing
+    fill = int(windows.max()) // Q + 2
+    for i in range(fill + args.warmup):
+        graphs[i % R].replay()
+    torch.cuda.synchronize()
+    h.sync_status()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    cur = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(uuid if uuid.startswith("GPU-") else f"GPU-{uuid}")
+    barrier()
+    with sampler:
+        ev0.record(cur)
+        for i in range(args.steps):
+            graphs[i % R].replay()
+        ev1.record(cur)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    barrier()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    h.sync_status()
+    clocks = sampler.summary()
+    value = world * A * args.steps / (ms / 1000.0)
+
+    # decode attention alone (the dominant kernel pair: split-K partials + merge),
+    # all layers of one open step, replayed as a graph; lengths = full windows
+    lens = [min(int(w), 10 ** 12) for w in windows]
+    h.begin_step(active)
+    for layer in range(L):
+        if wl.scheme == 1:
+            h.rebase(layer)
+        h.append_rope(layer, ks[0][layer * A * Q * hkv * d:], vs[0][layer * A * Q * hkv * d:])
+    torch.cuda.synchronize()
+    g_attn = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for layer in range(L):
+            h.decode_attn(layer, qs[0][layer * A * Q * hq * d:], outs[0][layer * A * Q * hq * d:],
+                          lses[0][layer * A * Q * hq:])
+        stream.synchronize()
+        with torch.cuda.graph(g_attn, stream=stream):
+            for layer in range(L):
+                h.decode_attn(layer, qs[0][layer * A * Q * hq * d:], outs[0][layer * A * Q * hq * d:],
+                              lses[0][layer * A * Q * hq:])
+    reps = max(3, min(200, args.steps // 4))
+    for _ in range(3):
+        g_attn.replay()
+    torch.cuda.synchronize()
+    ev0.record(cur)
+    for _ in range(reps):
+        g_attn.replay()
+    ev1.record(cur)
+    torch.cuda.synchronize()
+    attn_ms = ev0.elapsed_time(ev1) / (reps * L)
+    attn_bytes = algorithmic_attn_bytes(wl, lens)
+    peak, peak_kind = measured_peak()
+    achieved = attn_bytes / (attn_ms / 1000.0) / 1e9
+    # close the open step so the handle's call order stays valid
+    h.sync_status()
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(h, wl, active, args, dev, stream)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = oracle_timing(wl, args.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": describe(wl, scheme_name), "streams_per_gpu": A, "layers": L,
+                           "l2": f"per-step working set {(h.pool_bytes) / 1e9:.2f} GB of KV pages > 126 MB L2; "
+                                 "no flush between steps",
+                           "graph": f"{R} CUDA graphs of one full step each, replayed round-robin",
+                           "parallelism": "replicas" if world == 1 else f"replicas x{world}"},
+                "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                             "frac": achieved / peak, "traffic": None,
+                             "kernel": "decode attention (split-K partials + merge), per layer launch",
+                             "algorithmic_bytes_per_launch": attn_bytes, "avg_launch_us": attn_ms * 1000.0,
+                             "peak_kind": f"{peak_kind} (hbm_gbs, STREAM-style copy)"},
+                "decode_attn_gbs": achieved,
+                "gpu_launches": launches_per_step * args.steps,
+                "clocks": clocks}
+        if e2e is not None:
+            line["e2e"] = e2e
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    h.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def measure_e2e(h, wl, active, args, dev, stream):
+    """Same metric through the public call with host buffers: H2D inputs, step, D2H outputs, every step."""
+    import torch
+    S, L, Q, hq, hkv, d = wl.n_streams, wl.n_layers, wl.q_per_step, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    A = len(active)
+    nq, nkv = L * A * Q * hq * d, L * A * Q * hkv * d
+    q_h = torch.randn(nq, dtype=torch.float32).mul_(wl.input_scale).to(torch.bfloat16).pin_memory()
+    k_h = torch.randn(nkv, dtype=torch.float32).mul_(wl.input_scale).to(torch.bfloat16).pin_memory()
+    v_h = torch.randn(nkv, dtype=torch.float32).mul_(wl.input_scale).to(torch.bfloat16).pin_memory()
+    out_h = torch.empty(nq, dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty(nq // d, dtype=torch.float32).pin_memory()
+    q_d = torch.empty(nq, dtype=torch.bfloat16, device=dev)
+    k_d = torch.empty(nkv, dtype=torch.bfloat16, device=dev)
+    v_d = torch.empty(nkv, dtype=torch.bfloat16, device=dev)
+    out_d = torch.empty(nq, dtype=torch.bfloat16, device=dev)
+    lse_d = torch.empty(nq // d, dtype=torch.float32, device=dev)
+    steps = max(5, min(args.steps, 300))
+
+    def one():
+        q_d.copy_(q_h, non_blocking=True)
+        k_d.copy_(k_h, non_blocking=True)
+        v_d.copy_(v_h, non_blocking=True)
+        h.step(active, q_d, k_d, v_d, out_d, lse_d)
+        out_h.copy_(out_d, non_blocking=True)
+        lse_h.copy_(lse_d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            one()
+        e1.record(stream)
+        stream.synchronize()
+    ms = e0.elapsed_time(e1)
+    bi = (q_h.numel() + k_h.numel() + v_h.numel()) * 2
+    bo = out_h.numel() * 2 + lse_h.numel() * 4
+    return {"value": A * steps / (ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "steps": steps, "call": "rkv_step (eager) with pinned-host copies in and out every step"}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,245 @@
+/*
+ * rkv.h — C ABI of librkv.so: the rolling KV-cache step for unbounded
+ * streaming attention, on one NVIDIA B300 (sm_103a).
+ *
+ * What one step does, for every active audio stream and every layer
+ * (Audio8 ASR Infinite 无限长转写原理, "Rolling KV Cache 三步拆解"):
+ *   1. the window is fixed; once full, the oldest tokens leave it
+ *      (第 1 步; voxtral.c rolling-KV article §二 keeps the last
+ *      VOX_DEC_WINDOW positions);
+ *   2. the new K/V are written with RoPE at their position: either the
+ *      logical position physical + kv_pos_offset, never re-encoded
+ *      (voxtral.c article §二 "RoPE 逻辑位置修正", the offset-only scheme),
+ *      or a window-relative position, every retained key being rotated by
+ *      R(-delta) when delta positions leave the window (第 2 步, the exact
+ *      re-base scheme);
+ *   3. attention of the step's queries over the fixed window, so the cost
+ *      per step is constant (第 3 步); one query per stream for the decoder
+ *      (one text token per clock step, Edge0/Audio8-ASR-Infinite model card
+ *      "亮点"), frame_len = 4 queries with a causal mask inside the step for
+ *      the audio encoder's incremental step (voxtral.c article §三).
+ *
+ * Conventions for every function below.
+ *   - Return value: RKV_OK (0) or a negative rkv_status.  Host-side
+ *     validation failures return before anything is enqueued.  The message
+ *     of the last failure is rkv_last_error(handle) (or rkv_last_error(NULL)
+ *     for calls without a handle; per thread).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call that takes one is asynchronous on it unless
+ *     stated, and may be captured into a CUDA graph.
+ *   - Device buffers are owned by the caller; the library never allocates
+ *     or frees device memory.  Pointers marked "device" must be device (or
+ *     managed) memory of the current device; "host" pointers are read
+ *     during the call only.
+ *   - bf16 tensors are uint16 bit patterns of bfloat16, row-major, densely
+ *     packed, 16-byte aligned.
+ *   - Errors found by kernels (an index outside its table, a wait that timed
+ *     out) are recorded in a device status word and reported by
+ *     rkv_sync_status(); the kernel skips the offending access and returns.
+ *
+ * Per-step order.  rkv_begin_step opens a step; then, for every layer,
+ * rkv_rebase (exact scheme only) and rkv_append_rope in either order, then
+ * rkv_decode_attn (any number of times).  Calling rkv_append_rope or
+ * rkv_rebase twice for a layer in one step, rkv_decode_attn before them,
+ * rkv_rebase in the offset-only scheme, or opening the next step while a
+ * layer lacks them returns RKV_ERR_STATE.
+ *
+ * Memory in HBM (pool_dev).  Three regions of [L][pages][Hkv][page_size][d]
+ * 16-bit elements: rotated keys (fp16), values (bf16), and in the exact
+ * scheme pre-RoPE keys (bf16).  Stream s owns ceil(W_s / page_size) pages;
+ * token j lives in ring slot j mod W_s, so eviction moves no data.
+ */
+#ifndef RKV_H_
+#define RKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define RKV_API __attribute__((visibility("default")))
+#else
+#define RKV_API
+#endif
+
+typedef uint16_t rkv_bf16; /* bfloat16 bits */
+
+typedef enum {
+  RKV_OK = 0,
+  RKV_ERR_INVALID_ARG = -1,  /* null pointer, id out of range, duplicate id, misaligned buffer */
+  RKV_ERR_CONFIG = -2,       /* configuration or clock not supported / inconsistent */
+  RKV_ERR_CUDA = -3,         /* a CUDA runtime call failed (message has the CUDA error) */
+  RKV_ERR_CAPACITY = -4,     /* a caller buffer is smaller than rkv_required_bytes says */
+  RKV_ERR_TIMEOUT = -5,      /* a bounded device-side wait gave up */
+  RKV_ERR_STATE = -6,        /* call out of order (see "Per-step order" above) */
+  RKV_ERR_DEVICE_BOUNDS = -7, /* a kernel found an index outside its table */
+  RKV_ERR_DEVICE_RANGE = -8   /* a rotated key did not fit fp16 (|k| >= 65520) */
+} rkv_status;
+
+typedef enum {
+  RKV_SCHEME_OFFSET_ONLY = 0,  /* K rotated once at P0 + j; kv_pos_offset bookkeeping only */
+  RKV_SCHEME_EXACT_REBASE = 1  /* K kept at window-relative positions, re-based on every roll */
+} rkv_scheme;
+
+/* Shape and policy of one handle.  All layers share it. */
+typedef struct {
+  int32_t n_layers;        /* L >= 1 */
+  int32_t n_streams;       /* S, 1 .. RKV_MAX_STREAMS */
+  int32_t n_q_heads;       /* Hq, multiple of n_kv_heads; Hq/Hkv * q_per_step <= 16 */
+  int32_t n_kv_heads;      /* Hkv >= 1; q head h reads kv head h / (Hq/Hkv) */
+  int32_t head_dim;        /* d: 64 or 128; RoPE pairs (x_i, x_{i+d/2}) */
+  int32_t q_per_step;      /* Q: 1 (decoder) .. 8; Q > 1 is causal inside the step */
+  int32_t page_size;       /* ring slots per page: 16, 32, 64 or 128 */
+  int32_t scheme;          /* rkv_scheme */
+  int32_t rebase_interval; /* exact scheme: re-base once this many tokens left (>= 1) */
+  int32_t reserved;        /* must be 0 */
+  double rope_theta;       /* RoPE base theta > 1 (1e6 for the Qwen2.5 decoder) */
+  double softmax_scale;    /* score scale; 0 selects 1/sqrt(head_dim) */
+} rkv_config;
+
+#define RKV_MAX_STREAMS 1024
+#define RKV_MAX_WINDOW (1 << 20)
+#define RKV_STATE_FIELDS 8
+
+/* Clock arithmetic of the audio front end (Edge0/Audio8-ASR-Infinite README,
+ * "Optimized operation points"; explainer "三档音频时钟", "可配置转写延迟"). */
+typedef struct {
+  int32_t clock_ms;          /* 20 ms tower frame x frame_len */
+  int32_t window;            /* clock steps in the 30 s native context, rounded up */
+  int32_t num_delay_tokens;  /* target_delay_ms / clock_ms */
+  int32_t left_pad_tokens;   /* streaming_n_left_pad_tokens: 18 / 12 / 9 */
+  int32_t samples_per_token; /* 16 kHz samples per clock step */
+  int32_t post_trained;      /* 1 if (clock, delay) is in the post-trained table */
+  double decisions_per_s;    /* 1000 / clock_ms */
+} rkv_clock;
+
+typedef struct rkv_handle rkv_handle;
+
+/* Validate frame_len (4, 6 or 8) and target_delay_ms (a positive multiple of
+ * the clock) and fill *out.  Host only.  RKV_ERR_CONFIG if invalid,
+ * RKV_ERR_INVALID_ARG if out is NULL. */
+RKV_API int rkv_clock_resolve(int32_t frame_len, int32_t target_delay_ms, rkv_clock* out);
+
+/* Bytes of the two caller-owned device buffers a handle needs.  `window` is a
+ * host array [n_streams] of per-stream windows W_s (q_per_step <= W_s <=
+ * RKV_MAX_WINDOW).  The sizes depend only on the config and the windows, not
+ * on how long the streams run: memory is constant (explainer 第 1 步).
+ * Host only. */
+RKV_API int rkv_required_bytes(const rkv_config* cfg, const int32_t* window,
+                       size_t* pool_bytes, size_t* state_bytes);
+
+/* Create a handle.
+ *   window       host [S] int32: window W_s of each stream
+ *   start_offset host [S] int64: logical position P0_s of each stream's first
+ *                token, 0 <= P0_s < 2^52
+ *   pool_dev     device buffer >= pool_bytes, 256-byte aligned: the K/V pages
+ *   state_dev    device buffer >= state_bytes, 256-byte aligned: stream state,
+ *                page tables, RoPE tables, split-K partials, status word
+ * Initialises state_dev on `stream` and waits for it (synchronous).  Streams
+ * start empty (n = 0).  The handle keeps the two pointers; the caller keeps
+ * the buffers alive until rkv_destroy. */
+RKV_API int rkv_create(const rkv_config* cfg, const int32_t* window, const int64_t* start_offset,
+               void* pool_dev, size_t pool_bytes, void* state_dev, size_t state_bytes,
+               void* stream, rkv_handle** out);
+
+/* Open a step for the streams in active_ids (host [n_active], distinct ids in
+ * [0, S), 1 <= n_active <= S).  On the device, for each active stream:
+ * n += Q; len = min(n, W); evicted = n - len; kv_pos_offset = P0 + evicted;
+ * head_slot = evicted mod W; in the exact scheme, if evicted - rope_base >=
+ * rebase_interval, the step re-bases by delta = evicted - rope_base and
+ * rope_base = evicted.  Then cos/sin of the new tokens' RoPE positions are
+ * computed once for all layers (fp64 with error-free range reduction).
+ * The id list travels in the kernel's parameters, so a captured graph
+ * replays the same active set. */
+RKV_API int rkv_begin_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active, void* stream);
+
+/* RoPE + append for one layer (explainer 第 2 步; voxtral.c article §二:
+ * RoPE is baked into K at write time).
+ *   k  device [A][Q][Hkv][d] bf16, pre-RoPE keys of the new tokens (A =
+ *      n_active, rows in active_ids order)
+ *   v  device [A][Q][Hkv][d] bf16
+ * Writes the key rotated to its position (logical P0 + j, or j - rope_base
+ * in the exact scheme) into ring slot (token mod W) of each stream, stored
+ * as fp16 (round to nearest even; eleven significant bits, so a stored key
+ * adds ~2e-4 to a unit-scale score, where bf16 would add ~1.6e-3), and v as
+ * given (bf16), plus the pre-RoPE k in the exact scheme.  A rotated key of
+ * magnitude >= 65520 is reported as RKV_ERR_DEVICE_RANGE by rkv_sync_status.
+ * Once per layer per step. */
+RKV_API int rkv_append_rope(rkv_handle* h, int32_t layer, const rkv_bf16* k, const rkv_bf16* v,
+                            void* stream);
+
+/* Exact re-base for one layer (explainer 第 2 步): every retained key of a
+ * stream whose step re-bases is rotated by R(-delta), which brings the
+ * stored positions back to j - rope_base inside the window.  The rotation is
+ * applied to the key's pre-RoPE copy with the composite angle, so a stored
+ * key carries one bf16 rounding however many times it was re-based.  Exact
+ * scheme only (RKV_ERR_STATE otherwise); must be called once per layer per
+ * step, before rkv_decode_attn of that layer (a no-op on the device for
+ * streams that do not re-base this step). */
+RKV_API int rkv_rebase(rkv_handle* h, int32_t layer, void* stream);
+
+/* Windowed GQA attention for one layer (explainer 第 3 步), split-K over the
+ * window with a log-sum-exp merge.
+ *   q     device [A][Q][Hq][d] bf16, pre-RoPE queries of the new tokens;
+ *         rotated inside the kernel in fp32 at the same positions as the
+ *         step's keys (never rounded back to 16 bits), not modified
+ *   out   device [A][Q][Hq][d] bf16: softmax(q k^T * scale) v over the window
+ *   lse   device [A][Q][Hq] fp32: natural log of sum exp(scaled scores); may
+ *         be NULL
+ * Query token n_old + i of a stream attends its tokens j with
+ * max(0, n_new - W) <= j <= n_old + i. */
+RKV_API int rkv_decode_attn(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv_bf16* out,
+                            float* lse, void* stream);
+
+/* The whole step for all layers: rkv_begin_step, then per layer
+ * rkv_rebase (exact scheme), rkv_append_rope, rkv_decode_attn.
+ *   q     device [L][A][Q][Hq][d], k, v [L][A][Q][Hkv][d], all pre-RoPE bf16
+ *   out   device [L][A][Q][Hq][d], lse [L][A][Q][Hq] (may be NULL) */
+RKV_API int rkv_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active, const rkv_bf16* q,
+             const rkv_bf16* k, const rkv_bf16* v, rkv_bf16* out, float* lse, void* stream);
+
+/* Copy one stream's device state to host `out` (RKV_STATE_FIELDS int64):
+ * n, len, evicted, kv_pos_offset, rope_base, head_slot, W, P0.  Waits for
+ * `stream`. */
+RKV_API int rkv_get_stream_state(rkv_handle* h, int32_t stream_id, int64_t* out, void* stream);
+
+/* Wait for `stream`, read and clear the device status word: RKV_OK,
+ * RKV_ERR_DEVICE_BOUNDS, RKV_ERR_DEVICE_RANGE or RKV_ERR_TIMEOUT. */
+RKV_API int rkv_sync_status(rkv_handle* h, void* stream);
+
+/* Message of the last failure on this handle (NULL: of the calling thread's
+ * last failure without a handle).  Valid until the next call. */
+RKV_API const char* rkv_last_error(const rkv_handle* h);
+
+/* Free the host-side handle.  Device buffers stay with the caller. */
+RKV_API int rkv_destroy(rkv_handle* h);
+
+/* ---- building blocks, exposed for tests and benchmarks ---------------- */
+
+/* cos/sin of RoPE angles: cs_dev[n][d/2][2] fp32 = (cos, sin)(pos[i] * omega_j)
+ * with omega_j = theta^(-2j/d) rounded to fp64 on the host, the product
+ * split exactly (FMA) and reduced modulo 2*pi with a three-part 2*pi.
+ *   pos_dev device [n] int64, |pos| < 2^52. */
+RKV_API int rkv_rope_cossin(const int64_t* pos_dev, int32_t n, int32_t head_dim, double theta,
+                    float* cs_dev, void* stream);
+
+/* Counter-based N(0,1)-like bf16 inputs (SplitMix64, Steele, Lea and Flood
+ * 2014; twelve 12-bit fields summed, Irwin-Hall), times an fp32 scale,
+ * rounded to nearest even.  out_dev[t][e] for token token0 + t, element e <
+ * width of one token's [heads][head_dim] tensor. */
+RKV_API int rkv_gen_tokens(uint64_t seed, uint32_t tag, int32_t stream_id, int32_t layer, int64_t token0,
+                   int32_t n_tokens, int32_t width, float scale, rkv_bf16* out_dev, void* stream);
+
+/* The same draws for the open step's new tokens of one layer, in the layout
+ * rkv_append_rope takes: q [A][Q][Hq][d] (tag 1), k and v [A][Q][Hkv][d]
+ * (tags 2, 3); token index = the stream's own token count. */
+RKV_API int rkv_gen_step_inputs(rkv_handle* h, uint64_t seed, int32_t layer, float scale, rkv_bf16* q,
+                        rkv_bf16* k, rkv_bf16* v, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RKV_H_ */

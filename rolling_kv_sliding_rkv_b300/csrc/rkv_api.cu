@@ -1,0 +1,427 @@
+// Host side of the C ABI declared in include/rkv.h: validation, the layout of
+// the caller-owned device buffers, the per-step call order, error reporting.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "rkv_internal.cuh"
+
+struct rkv_handle {
+  rkv_config cfg;
+  rkv::DevView view;
+  size_t pool_bytes = 0, state_bytes = 0;
+  int32_t w_max = 0;
+  int device = 0;
+  int num_sms = 0;
+  bool step_open = false;
+  int32_t n_active = 0;
+  std::vector<uint8_t> appended, rebased;
+  std::string last_error;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(rkv_handle* h, int code, const std::string& msg) {
+  (h ? h->last_error : g_last_error) = msg;
+  return code;
+}
+
+int cuda_fail(rkv_handle* h, cudaError_t e, const char* what) {
+  return fail(h, RKV_ERR_CUDA, std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")");
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Layout {
+  size_t state, page_table, desc, cs_new, omega, rope_table, part_ml, part_o, status, total;
+  size_t pool_region_elems;  // elements of one pool region (all layers)
+  int32_t max_pages, n_pages, t_rows, w_max, regions;
+};
+
+bool validate_config(const rkv_config* c, std::string* why) {
+  char buf[256];
+  auto bad = [&](const char* m) { *why = m; return false; };
+  if (!c) return bad("config is NULL");
+  if (c->n_layers < 1 || c->n_layers > 4096) return bad("n_layers must be in [1, 4096]");
+  if (c->n_streams < 1 || c->n_streams > RKV_MAX_STREAMS) return bad("n_streams must be in [1, RKV_MAX_STREAMS]");
+  if (c->n_kv_heads < 1 || c->n_q_heads < 1 || c->n_q_heads % c->n_kv_heads != 0)
+    return bad("n_q_heads must be a positive multiple of n_kv_heads");
+  if (c->head_dim != 64 && c->head_dim != 128) return bad("head_dim must be 64 or 128");
+  if (c->q_per_step < 1 || c->q_per_step > 8) return bad("q_per_step must be in [1, 8]");
+  if (c->n_q_heads / c->n_kv_heads * c->q_per_step > 16) return bad("(n_q_heads / n_kv_heads) * q_per_step must be <= 16");
+  if (c->n_q_heads > 256 || c->n_kv_heads > 256) return bad("at most 256 heads");
+  if (c->page_size != 16 && c->page_size != 32 && c->page_size != 64 && c->page_size != 128)
+    return bad("page_size must be 16, 32, 64 or 128");
+  if (c->scheme != RKV_SCHEME_OFFSET_ONLY && c->scheme != RKV_SCHEME_EXACT_REBASE) return bad("unknown scheme");
+  if (c->rebase_interval < 1) return bad("rebase_interval must be >= 1");
+  if (c->reserved != 0) return bad("reserved must be 0");
+  if (!(c->rope_theta > 1.0) || !std::isfinite(c->rope_theta)) return bad("rope_theta must be finite and > 1");
+  if (!(c->softmax_scale >= 0.0) || !std::isfinite(c->softmax_scale)) return bad("softmax_scale must be finite and >= 0");
+  (void)buf;
+  return true;
+}
+
+bool compute_layout(const rkv_config* c, const int32_t* window, Layout* L, std::string* why) {
+  if (!validate_config(c, why)) return false;
+  if (!window) {
+    *why = "window is NULL";
+    return false;
+  }
+  const int S = c->n_streams;
+  int32_t w_max = 0;
+  int64_t n_pages = 0;
+  for (int s = 0; s < S; ++s) {
+    const int32_t w = window[s];
+    if (w < c->q_per_step || w > RKV_MAX_WINDOW) {
+      char buf[160];
+      snprintf(buf, sizeof buf, "window[%d] = %d outside [q_per_step, RKV_MAX_WINDOW]", s, w);
+      *why = buf;
+      return false;
+    }
+    w_max = w > w_max ? w : w_max;
+    n_pages += (w + c->page_size - 1) / c->page_size;
+  }
+  if (n_pages > (1 << 30)) {
+    *why = "too many pages";
+    return false;
+  }
+  L->w_max = w_max;
+  L->max_pages = (w_max + c->page_size - 1) / c->page_size;
+  L->n_pages = static_cast<int32_t>(n_pages);
+  const bool exact = c->scheme == RKV_SCHEME_EXACT_REBASE;
+  // window-relative positions of the exact scheme stay below W + interval - 1
+  const int64_t t_rows = exact ? static_cast<int64_t>(w_max) + c->rebase_interval - 1 : 0;
+  if (t_rows > (1 << 24)) {
+    *why = "window + rebase_interval too large";
+    return false;
+  }
+  L->t_rows = static_cast<int32_t>(t_rows);
+  L->regions = exact ? 3 : 2;
+  const int half = c->head_dim / 2;
+  const size_t rows = static_cast<size_t>(S) * c->q_per_step * c->n_q_heads;
+  const size_t splits_max = static_cast<size_t>(L->max_pages);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  L->state = take(static_cast<size_t>(S) * rkv::kStateFields * sizeof(int64_t));
+  L->page_table = take(static_cast<size_t>(S) * L->max_pages * sizeof(int32_t));
+  L->desc = take(static_cast<size_t>(S) * sizeof(rkv::StepDesc));
+  L->cs_new = take(static_cast<size_t>(S) * c->q_per_step * half * 2 * sizeof(float));
+  L->omega = take(static_cast<size_t>(half) * sizeof(double));
+  L->rope_table = take(static_cast<size_t>(t_rows) * half * 2 * sizeof(float));
+  L->part_ml = take(rows * splits_max * 2 * sizeof(float));
+  L->part_o = take(rows * splits_max * c->head_dim * sizeof(float));
+  L->status = take(4 * sizeof(int32_t));
+  L->total = off;
+  L->pool_region_elems = static_cast<size_t>(c->n_layers) * n_pages * c->n_kv_heads * c->page_size * c->head_dim;
+  return true;
+}
+
+bool check_layer(rkv_handle* h, int32_t layer) { return layer >= 0 && layer < h->cfg.n_layers; }
+
+}  // namespace
+
+extern "C" {
+
+int rkv_clock_resolve(int32_t frame_len, int32_t target_delay_ms, rkv_clock* out) {
+  if (!out) return fail(nullptr, RKV_ERR_INVALID_ARG, "out is NULL");
+  int left_pad;
+  switch (frame_len) {  // Edge0/Audio8-ASR-Infinite README, "Optimized operation points"
+    case 4: left_pad = 18; break;
+    case 6: left_pad = 12; break;
+    case 8: left_pad = 9; break;
+    default: return fail(nullptr, RKV_ERR_CONFIG, "frame_len must be 4, 6 or 8");
+  }
+  const int32_t clock = 20 * frame_len;  // 20 ms tower frame (explainer, "三档音频时钟")
+  if (target_delay_ms <= 0 || target_delay_ms % clock != 0)
+    return fail(nullptr, RKV_ERR_CONFIG, "target_delay_ms must be a positive multiple of the clock");
+  static const int32_t trained[3][4] = {{240, 320, 480, 560}, {240, 480, 0, 0}, {320, 480, 0, 0}};
+  const int row = frame_len == 4 ? 0 : frame_len == 6 ? 1 : 2;
+  int post = 0;
+  for (int i = 0; i < 4; ++i) post |= trained[row][i] == target_delay_ms;
+  out->clock_ms = clock;
+  out->window = (30000 + clock - 1) / clock;  // 30 s native context, rounded up
+  out->num_delay_tokens = target_delay_ms / clock;
+  out->left_pad_tokens = left_pad;
+  out->samples_per_token = 16000 * clock / 1000;
+  out->post_trained = post;
+  out->decisions_per_s = 1000.0 / clock;
+  return RKV_OK;
+}
+
+int rkv_required_bytes(const rkv_config* cfg, const int32_t* window, size_t* pool_bytes, size_t* state_bytes) {
+  if (!pool_bytes || !state_bytes) return fail(nullptr, RKV_ERR_INVALID_ARG, "size outputs are NULL");
+  Layout L;
+  std::string why;
+  if (!compute_layout(cfg, window, &L, &why)) return fail(nullptr, cfg && window ? RKV_ERR_CONFIG : RKV_ERR_INVALID_ARG, why);
+  *pool_bytes = L.pool_region_elems * L.regions * sizeof(uint16_t);
+  *state_bytes = L.total;
+  return RKV_OK;
+}
+
+int rkv_create(const rkv_config* cfg, const int32_t* window, const int64_t* start_offset, void* pool_dev,
+               size_t pool_bytes, void* state_dev, size_t state_bytes, void* stream, rkv_handle** out) {
+  if (!out) return fail(nullptr, RKV_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  Layout L;
+  std::string why;
+  if (!cfg || !window || !start_offset) return fail(nullptr, RKV_ERR_INVALID_ARG, "config, window or start_offset is NULL");
+  if (!compute_layout(cfg, window, &L, &why)) return fail(nullptr, RKV_ERR_CONFIG, why);
+  for (int s = 0; s < cfg->n_streams; ++s)
+    if (start_offset[s] < 0 || start_offset[s] >= (int64_t(1) << 52))
+      return fail(nullptr, RKV_ERR_CONFIG, "start_offset must be in [0, 2^52)");
+  if (!pool_dev || !state_dev) return fail(nullptr, RKV_ERR_INVALID_ARG, "pool_dev or state_dev is NULL");
+  if ((reinterpret_cast<uintptr_t>(pool_dev) | reinterpret_cast<uintptr_t>(state_dev)) & (kAlign - 1))
+    return fail(nullptr, RKV_ERR_INVALID_ARG, "device buffers must be 256-byte aligned");
+  const size_t need_pool = L.pool_region_elems * L.regions * sizeof(uint16_t);
+  if (pool_bytes < need_pool || state_bytes < L.total)
+    return fail(nullptr, RKV_ERR_CAPACITY, "pool or state buffer smaller than rkv_required_bytes");
+
+  rkv_handle* h = new rkv_handle();
+  h->cfg = *cfg;
+  h->pool_bytes = pool_bytes;
+  h->state_bytes = state_bytes;
+  h->w_max = L.w_max;
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(nullptr, e, "querying the device");
+  }
+
+  char* sb = static_cast<char*>(state_dev);
+  rkv::DevView& v = h->view;
+  v.state = reinterpret_cast<int64_t*>(sb + L.state);
+  v.page_table = reinterpret_cast<int32_t*>(sb + L.page_table);
+  v.desc = reinterpret_cast<rkv::StepDesc*>(sb + L.desc);
+  v.cs_new = reinterpret_cast<float*>(sb + L.cs_new);
+  v.omega = reinterpret_cast<double*>(sb + L.omega);
+  v.rope_table = L.t_rows ? reinterpret_cast<float*>(sb + L.rope_table) : nullptr;
+  v.part_ml = reinterpret_cast<float*>(sb + L.part_ml);
+  v.part_o = reinterpret_cast<float*>(sb + L.part_o);
+  v.status = reinterpret_cast<int32_t*>(sb + L.status);
+  uint16_t* pool = static_cast<uint16_t*>(pool_dev);
+  v.k_rot = pool;
+  v.v = pool + L.pool_region_elems;
+  v.k_raw = L.regions == 3 ? pool + 2 * L.pool_region_elems : nullptr;
+  v.layer_stride = static_cast<int64_t>(L.n_pages) * cfg->n_kv_heads * cfg->page_size * cfg->head_dim;
+  v.n_streams = cfg->n_streams;
+  v.n_layers = cfg->n_layers;
+  v.n_q_heads = cfg->n_q_heads;
+  v.n_kv_heads = cfg->n_kv_heads;
+  v.head_dim = cfg->head_dim;
+  v.q_per_step = cfg->q_per_step;
+  v.page_size = cfg->page_size;
+  v.n_pages = L.n_pages;
+  v.max_pages = L.max_pages;
+  v.t_rows = L.t_rows;
+  v.scheme = cfg->scheme;
+  v.rebase_interval = cfg->rebase_interval;
+  const double scale = cfg->softmax_scale > 0.0 ? cfg->softmax_scale : 1.0 / std::sqrt(static_cast<double>(cfg->head_dim));
+  v.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
+  // Split the window into enough pieces to give every SM several blocks.
+  const int64_t items = static_cast<int64_t>(cfg->n_streams) * cfg->n_kv_heads * L.max_pages;
+  int64_t pps = items / (8 * static_cast<int64_t>(h->num_sms));
+  pps = pps < 1 ? 1 : pps > L.max_pages ? L.max_pages : pps;
+  v.pages_per_split = static_cast<int32_t>(pps);
+  v.splits = static_cast<int32_t>((L.max_pages + pps - 1) / pps);
+
+  // host images of the stream state, page tables and RoPE frequencies
+  const int S = cfg->n_streams, half = cfg->head_dim / 2;
+  std::vector<int64_t> state(static_cast<size_t>(S) * rkv::kStateFields, 0);
+  std::vector<int32_t> table(static_cast<size_t>(S) * L.max_pages, -1);
+  int32_t next_page = 0;
+  for (int s = 0; s < S; ++s) {
+    int64_t* st = &state[static_cast<size_t>(s) * rkv::kStateFields];
+    st[rkv::F_KV_POS_OFFSET] = start_offset[s];
+    st[rkv::F_W] = window[s];
+    st[rkv::F_P0] = start_offset[s];
+    const int pages = (window[s] + cfg->page_size - 1) / cfg->page_size;
+    for (int p = 0; p < pages; ++p) table[static_cast<size_t>(s) * L.max_pages + p] = next_page++;
+  }
+  std::vector<double> omega(half);
+  for (int i = 0; i < half; ++i) omega[i] = std::pow(cfg->rope_theta, -2.0 * i / cfg->head_dim);
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  e = cudaMemcpyAsync(v.state, state.data(), state.size() * sizeof(int64_t), cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(v.page_table, table.data(), table.size() * sizeof(int32_t), cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(v.omega, omega.data(), half * sizeof(double), cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(v.status, 0, 4 * sizeof(int32_t), st);
+  if (e == cudaSuccess) e = rkv::launch_init_tables(v, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(nullptr, e, "initialising the device state");
+  }
+  h->appended.assign(cfg->n_layers, 0);
+  h->rebased.assign(cfg->n_layers, 0);
+  *out = h;
+  return RKV_OK;
+}
+
+int rkv_begin_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active, void* stream) {
+  if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
+  if (!active_ids || n_active < 1 || n_active > h->cfg.n_streams)
+    return fail(h, RKV_ERR_INVALID_ARG, "active_ids must list 1 .. n_streams streams");
+  if (h->step_open) {
+    const bool exact = h->cfg.scheme == RKV_SCHEME_EXACT_REBASE;
+    for (int l = 0; l < h->cfg.n_layers; ++l)
+      if (!h->appended[l] || (exact && !h->rebased[l]))
+        return fail(h, RKV_ERR_STATE, "previous step left a layer without rkv_append_rope (or rkv_rebase)");
+  }
+  rkv::ActiveIds ids;
+  ids.n = n_active;
+  std::vector<uint8_t> seen(h->cfg.n_streams, 0);
+  for (int i = 0; i < n_active; ++i) {
+    const int32_t s = active_ids[i];
+    if (s < 0 || s >= h->cfg.n_streams) return fail(h, RKV_ERR_INVALID_ARG, "stream id out of range");
+    if (seen[s]) return fail(h, RKV_ERR_INVALID_ARG, "stream id listed twice");
+    seen[s] = 1;
+    ids.id[i] = s;
+  }
+  cudaError_t e = rkv::launch_begin_step(h->view, ids, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "begin_step launch");
+  h->step_open = true;
+  h->n_active = n_active;
+  std::fill(h->appended.begin(), h->appended.end(), 0);
+  std::fill(h->rebased.begin(), h->rebased.end(), 0);
+  return RKV_OK;
+}
+
+int rkv_append_rope(rkv_handle* h, int32_t layer, const rkv_bf16* k, const rkv_bf16* v, void* stream) {
+  if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
+  if (!h->step_open) return fail(h, RKV_ERR_STATE, "no open step (call rkv_begin_step)");
+  if (!check_layer(h, layer)) return fail(h, RKV_ERR_INVALID_ARG, "layer out of range");
+  if (!k || !v || !aligned16(k) || !aligned16(v))
+    return fail(h, RKV_ERR_INVALID_ARG, "k and v must be non-NULL and 16-byte aligned");
+  if (h->appended[layer]) return fail(h, RKV_ERR_STATE, "rkv_append_rope called twice for this layer in this step");
+  cudaError_t e = rkv::launch_append_rope(h->view, h->n_active, layer, k, v, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "append_rope launch");
+  h->appended[layer] = 1;
+  return RKV_OK;
+}
+
+int rkv_rebase(rkv_handle* h, int32_t layer, void* stream) {
+  if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
+  if (h->cfg.scheme != RKV_SCHEME_EXACT_REBASE) return fail(h, RKV_ERR_STATE, "rkv_rebase needs the exact re-base scheme");
+  if (!h->step_open) return fail(h, RKV_ERR_STATE, "no open step (call rkv_begin_step)");
+  if (!check_layer(h, layer)) return fail(h, RKV_ERR_INVALID_ARG, "layer out of range");
+  if (h->rebased[layer]) return fail(h, RKV_ERR_STATE, "rkv_rebase called twice for this layer in this step");
+  cudaError_t e = rkv::launch_rebase(h->view, h->n_active, layer, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "rebase launch");
+  h->rebased[layer] = 1;
+  return RKV_OK;
+}
+
+int rkv_decode_attn(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv_bf16* out, float* lse, void* stream) {
+  if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
+  if (!h->step_open) return fail(h, RKV_ERR_STATE, "no open step (call rkv_begin_step)");
+  if (!check_layer(h, layer)) return fail(h, RKV_ERR_INVALID_ARG, "layer out of range");
+  if (!q || !out || !aligned16(q) || !aligned16(out) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return fail(h, RKV_ERR_INVALID_ARG, "q and out must be non-NULL and 16-byte aligned");
+  if (!h->appended[layer]) return fail(h, RKV_ERR_STATE, "rkv_decode_attn before rkv_append_rope for this layer");
+  if (h->cfg.scheme == RKV_SCHEME_EXACT_REBASE && !h->rebased[layer])
+    return fail(h, RKV_ERR_STATE, "rkv_decode_attn before rkv_rebase for this layer");
+  cudaError_t e = rkv::launch_decode_attn(h->view, h->n_active, layer, q, out, lse, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "decode_attn launch");
+  return RKV_OK;
+}
+
+int rkv_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active, const rkv_bf16* q, const rkv_bf16* k,
+             const rkv_bf16* v, rkv_bf16* out, float* lse, void* stream) {
+  int rc = rkv_begin_step(h, active_ids, n_active, stream);
+  if (rc != RKV_OK) return rc;
+  const rkv_config& c = h->cfg;
+  const size_t rows = static_cast<size_t>(n_active) * c.q_per_step;
+  const size_t q_stride = rows * c.n_q_heads * c.head_dim, kv_stride = rows * c.n_kv_heads * c.head_dim;
+  const size_t lse_stride = rows * c.n_q_heads;
+  for (int l = 0; l < c.n_layers; ++l) {
+    if (c.scheme == RKV_SCHEME_EXACT_REBASE && (rc = rkv_rebase(h, l, stream)) != RKV_OK) return rc;
+    if ((rc = rkv_append_rope(h, l, k + l * kv_stride, v + l * kv_stride, stream)) != RKV_OK) return rc;
+    if ((rc = rkv_decode_attn(h, l, q + l * q_stride, out + l * q_stride, lse ? lse + l * lse_stride : nullptr,
+                              stream)) != RKV_OK)
+      return rc;
+  }
+  return RKV_OK;
+}
+
+int rkv_get_stream_state(rkv_handle* h, int32_t stream_id, int64_t* out, void* stream) {
+  if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
+  if (!out || stream_id < 0 || stream_id >= h->cfg.n_streams) return fail(h, RKV_ERR_INVALID_ARG, "bad stream id or out");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(out, h->view.state + static_cast<int64_t>(stream_id) * rkv::kStateFields,
+                                  rkv::kStateFields * sizeof(int64_t), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return e == cudaSuccess ? RKV_OK : cuda_fail(h, e, "reading stream state");
+}
+
+int rkv_sync_status(rkv_handle* h, void* stream) {
+  if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t status[4];
+  cudaError_t e = cudaMemcpyAsync(status, h->view.status, sizeof status, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "reading the status word");
+  if (status[0] == rkv::DEV_OK) return RKV_OK;
+  e = cudaMemsetAsync(h->view.status, 0, sizeof status, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "clearing the status word");
+  char buf[160];
+  const char* what = status[0] == rkv::DEV_TIMEOUT ? "a timed-out wait"
+                     : status[0] == rkv::DEV_RANGE ? "a rotated key outside the fp16 range"
+                                                   : "an index out of bounds";
+  snprintf(buf, sizeof buf, "device reported %s (site %d, value %d)", what, status[1], status[2]);
+  const int code = status[0] == rkv::DEV_TIMEOUT ? RKV_ERR_TIMEOUT
+                   : status[0] == rkv::DEV_RANGE ? RKV_ERR_DEVICE_RANGE
+                                                 : RKV_ERR_DEVICE_BOUNDS;
+  return fail(h, code, buf);
+}
+
+const char* rkv_last_error(const rkv_handle* h) { return h ? h->last_error.c_str() : g_last_error.c_str(); }
+
+int rkv_destroy(rkv_handle* h) {
+  delete h;
+  return RKV_OK;
+}
+
+int rkv_rope_cossin(const int64_t* pos_dev, int32_t n, int32_t head_dim, double theta, float* cs_dev, void* stream) {
+  if (n < 0 || (n > 0 && (!pos_dev || !cs_dev))) return fail(nullptr, RKV_ERR_INVALID_ARG, "bad pointers or n");
+  if (head_dim < 2 || head_dim > 128 || head_dim % 2) return fail(nullptr, RKV_ERR_CONFIG, "head_dim must be even, <= 128");
+  if (!(theta > 1.0) || !std::isfinite(theta)) return fail(nullptr, RKV_ERR_CONFIG, "theta must be finite and > 1");
+  rkv::Omegas w;
+  for (int i = 0; i < head_dim / 2; ++i) w.w[i] = std::pow(theta, -2.0 * i / head_dim);
+  cudaError_t e = rkv::launch_rope_cossin(pos_dev, n, head_dim, w, cs_dev, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RKV_OK : cuda_fail(nullptr, e, "rope_cossin launch");
+}
+
+int rkv_gen_tokens(uint64_t seed, uint32_t tag, int32_t stream_id, int32_t layer, int64_t token0, int32_t n_tokens,
+                   int32_t width, float scale, rkv_bf16* out_dev, void* stream) {
+  if (n_tokens < 0 || n_tokens > 65535 || width < 0 || (n_tokens && width && !out_dev))
+    return fail(nullptr, RKV_ERR_INVALID_ARG, "bad sizes or out pointer");
+  cudaError_t e = rkv::launch_gen_tokens(seed, tag, stream_id, layer, token0, n_tokens, width, scale, out_dev,
+                                         static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RKV_OK : cuda_fail(nullptr, e, "gen_tokens launch");
+}
+
+int rkv_gen_step_inputs(rkv_handle* h, uint64_t seed, int32_t layer, float scale, rkv_bf16* q, rkv_bf16* k,
+                        rkv_bf16* v, void* stream) {
+  if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
+  if (!h->step_open) return fail(h, RKV_ERR_STATE, "no open step (call rkv_begin_step)");
+  if (!q || !k || !v) return fail(h, RKV_ERR_INVALID_ARG, "q, k, v must be non-NULL");
+  cudaError_t e = rkv::launch_gen_step_inputs(h->view, h->n_active, seed, layer, scale, q, k, v,
+                                              static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RKV_OK : cuda_fail(h, e, "gen_step_inputs launch");
+}
+
+}  // extern "C"

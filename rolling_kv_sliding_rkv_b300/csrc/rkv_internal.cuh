@@ -1,0 +1,136 @@
+// Internal declarations shared by the librkv.so translation units.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rkv.h"
+#include "twopi_split.h"
+
+namespace rkv {
+
+constexpr int kStateFields = RKV_STATE_FIELDS;
+// state field indices (order reported by rkv_get_stream_state)
+enum { F_N = 0, F_LEN, F_EVICTED, F_KV_POS_OFFSET, F_ROPE_BASE, F_HEAD_SLOT, F_W, F_P0 };
+
+// status word codes written by kernels (first error wins)
+enum { DEV_OK = 0, DEV_BOUNDS = 1, DEV_TIMEOUT = 2, DEV_RANGE = 3 };
+
+// Per active stream of the open step, written by the begin-step kernel.
+struct StepDesc {
+  int64_t n_old;      // tokens before this step
+  int64_t evicted;    // tokens out of the window after this step
+  int64_t rope_base;  // exact scheme: origin of stored key positions after this step
+  int64_t delta;      // exact scheme: re-base amount this step (0: none)
+  int32_t stream;     // stream id
+  int32_t len;        // window length after this step
+  int32_t window;     // W
+  int32_t pad;
+};
+
+// Device addresses and shape, passed by value to every kernel.
+struct DevView {
+  int64_t* state;        // [S][8]
+  int32_t* page_table;   // [S][max_pages] -> physical page
+  StepDesc* desc;        // [S] by active index
+  float* cs_new;         // [S][Q][d/2][2] cos/sin of the new tokens' positions
+  float* rope_table;     // [t_rows][d/2][2] cos/sin of r * omega, r < t_rows (exact scheme)
+  double* omega;         // [d/2]
+  float* part_ml;        // [S][Q*Hq][splits][2] (running max in log2 units, sum)
+  float* part_o;         // [S][Q*Hq][splits][d] normalised partial outputs
+  int32_t* status;       // [4]: code, detail, detail2, unused
+  uint16_t* k_rot;       // pool: [L][n_pages][Hkv][ps][d] rotated keys, fp16 bits
+  uint16_t* v;           // pool: values (bf16 bits), same layout
+  uint16_t* k_raw;       // pool: pre-RoPE keys (bf16 bits, exact scheme), same layout
+  int64_t layer_stride;  // elements of one layer in one pool region
+  int32_t n_streams, n_layers, n_q_heads, n_kv_heads, head_dim, q_per_step;
+  int32_t page_size, n_pages, max_pages, splits, pages_per_split, t_rows;
+  int32_t scheme, rebase_interval;
+  float scale_log2;      // softmax scale * log2(e)
+};
+
+struct Omegas {
+  double w[64];  // omega_i = theta^(-2i/d), i < d/2, rounded to fp64 on the host
+};
+
+struct ActiveIds {
+  int32_t n;
+  int32_t id[RKV_MAX_STREAMS];
+};
+
+__device__ __forceinline__ void record_error(int32_t* status, int code, int detail, int detail2) {
+  if (atomicCAS(status, DEV_OK, code) == DEV_OK) {
+    status[1] = detail;
+    status[2] = detail2;
+  }
+}
+
+// cos/sin of p * omega in fp32 from an fp64 computation whose only error is
+// the final rounding steps.  p * omega = hi + lo exactly (FMA; |p| < 2^53).
+// k = nearest integer to hi / (2 pi).  With 2 pi = C1 + C2 + C3,
+// hi - k*C1 is exact under FMA (the result is a multiple of ulp(C1) below 8
+// in magnitude), then k*C2, k*C3 and lo are folded in with one rounding each.
+__device__ __forceinline__ void rope_cos_sin(int64_t p, double omega, float* c, float* s) {
+  const double pd = static_cast<double>(p);
+  const double hi = pd * omega;
+  const double lo = fma(pd, omega, -hi);
+  const double k = rint(hi * RKV_INV_TWO_PI);
+  double r = fma(-k, RKV_TWO_PI_C1, hi);
+  r = fma(-k, RKV_TWO_PI_C2, r);
+  r = fma(-k, RKV_TWO_PI_C3, r);
+  r += lo;
+  double sd, cd;
+  sincos(r, &sd, &cd);
+  *c = static_cast<float>(cd);
+  *s = static_cast<float>(sd);
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// round to nearest, ties to even (finite inputs)
+__device__ __forceinline__ uint16_t f32_to_bf16(float x) {
+  uint32_t u = __float_as_uint(x);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+// fp32 -> fp16 bits, round to nearest even
+__device__ __forceinline__ uint16_t f32_to_f16(float x) { return __half_as_ushort(__float2half_rn(x)); }
+
+__device__ __forceinline__ float f16_to_f32(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+
+// largest finite fp16 value after rounding: |x| >= 65520 rounds to infinity
+__device__ __forceinline__ bool fits_f16(float x) { return fabsf(x) < 65520.0f; }
+
+// token held by ring slot `slot` once `evicted` tokens have left a window of W
+__device__ __forceinline__ int64_t token_in_slot(int64_t slot, int64_t evicted, int32_t window) {
+  int64_t d = (slot - evicted % window) % window;
+  if (d < 0) d += window;
+  return evicted + d;
+}
+
+// element offset of (layer, physical page, kv head, offset in page) in a pool region
+__device__ __forceinline__ int64_t pool_offset(const DevView& v, int layer, int page, int kvh, int off) {
+  return static_cast<int64_t>(layer) * v.layer_stride +
+         ((static_cast<int64_t>(page) * v.n_kv_heads + kvh) * v.page_size + off) * v.head_dim;
+}
+
+// ---- launchers (host functions, one translation unit each) ----
+cudaError_t launch_init_tables(const DevView& v, cudaStream_t st);
+cudaError_t launch_begin_step(const DevView& v, const ActiveIds& ids, cudaStream_t st);
+cudaError_t launch_append_rope(const DevView& v, int n_active, int layer, const uint16_t* k, const uint16_t* vv,
+                               cudaStream_t st);
+cudaError_t launch_rebase(const DevView& v, int n_active, int layer, cudaStream_t st);
+cudaError_t launch_decode_attn(const DevView& v, int n_active, int layer, const uint16_t* q, uint16_t* out,
+                               float* lse, cudaStream_t st);
+cudaError_t launch_rope_cossin(const int64_t* pos, int n, int head_dim, const Omegas& w, float* cs,
+                               cudaStream_t st);
+cudaError_t launch_gen_tokens(uint64_t seed, uint32_t tag, int32_t stream_id, int32_t layer, int64_t token0,
+                              int32_t n_tokens, int32_t width, float scale, uint16_t* out, cudaStream_t st);
+cudaError_t launch_gen_step_inputs(const DevView& v, int n_active, uint64_t seed, int32_t layer, float scale,
+                                   uint16_t* q, uint16_t* k, uint16_t* vv, cudaStream_t st);
+
+}  // namespace rkv

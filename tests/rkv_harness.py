@@ -1,0 +1,121 @@
+"""Drive the CUDA path through the C ABI and compare sampled outputs with the oracle.
+
+The GPU run draws its inputs on the device (rkv_gen_step_inputs); the oracle
+regenerates the same tokens on the host (synth.token_tensor), so nothing the
+GPU computes ever feeds the oracle.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+import synth
+from oracle.attention import attention_step
+from oracle.ring import StreamRing
+
+OUT_TOL = 2e-2
+LSE_TOL = 1e-3
+
+
+@dataclass
+class Run:
+    """Outputs copied back from the GPU at sampled (stream step index, stream, layer)."""
+    samples: dict = field(default_factory=dict)   # (stream, layer, n_old) -> (out [Q][Hq][d], lse [Q][Hq])
+    states: dict = field(default_factory=dict)    # stream -> final device state
+    ring: dict = field(default_factory=dict)      # stream -> oracle StreamRing after the run
+
+
+def run_gpu(wl: synth.Workload, n_ticks: int, want: set, streams_of_interest=None, graph=False):
+    """Run `n_ticks` steps (ticks for the mixed-clock workload) and copy sampled outputs.
+
+    want: set of (stream, layer, n_old) to record, n_old = the stream's token
+    count before the step.  A mixed-clock workload first brings every stream
+    to its initial fill with extra steps of the lagging streams.
+    """
+    import torch
+
+    import rolling_kv_sliding_rkv_b300 as rkv
+
+    dev = torch.device("cuda")
+    windows = wl.windows()
+    p0 = wl.start_offsets()
+    h = rkv.RollingKV(windows.tolist(), p0.tolist(), device=dev, n_layers=wl.n_layers, n_streams=wl.n_streams,
+                      n_q_heads=wl.n_q_heads, n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim,
+                      q_per_step=wl.q_per_step, scheme=wl.scheme, rebase_interval=wl.rebase_interval,
+                      rope_theta=wl.rope_theta)
+    S, L, Q, hq, hkv, d = wl.n_streams, wl.n_layers, wl.q_per_step, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    q = torch.empty(S * Q * hq * d, dtype=torch.bfloat16, device=dev)
+    k = torch.empty(S * Q * hkv * d, dtype=torch.bfloat16, device=dev)
+    v = torch.empty_like(k)
+    out = torch.empty_like(q)
+    lse = torch.empty(S * Q * hq, dtype=torch.float32, device=dev)
+    rings = {s: StreamRing(int(windows[s]), int(p0[s]), Q, wl.scheme, wl.rebase_interval) for s in range(S)}
+    exact = wl.scheme == rkv.RKV_SCHEME_EXACT_REBASE
+    run = Run()
+    want_streams = {s for s, _, _ in want}
+
+    def one_step(active):
+        a = len(active)
+        h.begin_step(active)
+        n_old = {s: rings[s].n for s in active}
+        for s in active:
+            rings[s].step()
+        for layer in range(L):
+            h.gen_step_inputs(wl.seed, layer, wl.input_scale, q, k, v)
+            if exact:
+                h.rebase(layer)
+            h.append_rope(layer, k, v)
+            h.decode_attn(layer, q, out, lse)
+            for idx, s in enumerate(active):
+                if s in want_streams and (s, layer, n_old[s]) in want:
+                    o = out[: a * Q * hq * d].view(a, Q, hq, d)[idx].float().cpu().numpy()
+                    lv = lse[: a * Q * hq].view(a, Q, hq)[idx].cpu().numpy()
+                    run.samples[(s, layer, n_old[s])] = (o, lv)
+
+    # initial fill (ragged), one extra step at a time for the streams still short of it
+    fill = wl.initial_fill()
+    for r in range(int(fill.max()) if len(fill) else 0):
+        active = [s for s in range(S) if fill[s] > r]
+        if active:
+            one_step(active)
+    for tick in range(n_ticks):
+        active = wl.active_at_tick(tick).tolist()
+        if active:
+            one_step(active)
+    h.sync_status()
+    for s in (streams_of_interest if streams_of_interest is not None else range(S)):
+        run.states[s] = h.stream_state(s)
+        run.ring[s] = rings[s]
+    h.close()
+    return run
+
+
+def oracle_step(wl: synth.Workload, stream: int, layer: int, n_old: int):
+    """Oracle outputs of one stream-layer-step, from regenerated inputs."""
+    Q, hq, hkv, d = wl.q_per_step, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    w = int(wl.windows()[stream])
+    p0 = int(wl.start_offsets()[stream])
+    n_new = n_old + Q
+    toks = np.arange(max(0, n_new - w), n_new)
+    sc = wl.input_scale
+    qb = synth.token_tensor(wl.seed, synth.TAG_Q, stream, layer, np.arange(n_old, n_new), hq, d, sc)
+    kb = synth.token_tensor(wl.seed, synth.TAG_K, stream, layer, toks, hkv, d, sc)
+    vb = synth.token_tensor(wl.seed, synth.TAG_V, stream, layer, toks, hkv, d, sc)
+    return attention_step(synth.bf16_bits_to_f64(qb), synth.bf16_bits_to_f64(kb), synth.bf16_bits_to_f64(vb),
+                          toks, n_old, p0, w, 1.0 / math.sqrt(d), wl.rope_theta)
+
+
+def compare(run: Run, wl: synth.Workload):
+    """Max errors over all samples; asserts the tolerances."""
+    worst_o = worst_l = 0.0
+    for (s, layer, n_old), (o, lv) in sorted(run.samples.items()):
+        o_ref, l_ref = oracle_step(wl, s, layer, n_old)
+        e_o = float(np.abs(o - o_ref).max())
+        e_l = float((np.abs(lv - l_ref) / np.maximum(1.0, np.abs(l_ref))).max())
+        assert np.all(np.isfinite(o)) and np.all(np.isfinite(lv))
+        assert e_o <= OUT_TOL, f"out error {e_o:.3g} at stream {s} layer {layer} n_old {n_old}"
+        assert e_l <= LSE_TOL, f"lse error {e_l:.3g} at stream {s} layer {layer} n_old {n_old}"
+        worst_o, worst_l = max(worst_o, e_o), max(worst_l, e_l)
+    return worst_o, worst_l

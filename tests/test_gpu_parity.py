@@ -1,0 +1,75 @@
+"""CUDA path against the fp64 oracle (max |out error| <= 2e-2, |lse error| <= 1e-3 max(1, |lse|)).
+
+Small cases compare every output of every step; full-size workloads run in the
+shape the benchmark times and compare sampled stream-layer-steps.
+"""
+import numpy as np
+import pytest
+
+import synth
+from rkv_harness import compare, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    # several pages of 64 slots with a ragged tail (150 = 2 * 64 + 22), window rolls
+    "tiny_exact": ("tiny", dict(n_layers=2, n_streams=3, extra={"window": 150}), 190),
+    "tiny_exact_interval5": ("tiny", dict(n_layers=1, n_streams=2, extra={"window": 150}, rebase_interval=5), 190),
+    "tiny_offset_large_p0": ("tiny", dict(n_layers=1, n_streams=3, extra={"window": 150}, scheme=0,
+                                          p0_high=2 ** 41), 190),
+    "voxtral_shape": ("voxtral", dict(n_layers=1, n_streams=2, extra={"window": 130}), 150),
+    "encoder_q4": ("encoder", dict(n_layers=1, n_streams=3, extra={"window": 70}), 30),
+    "encoder_q4_exact": ("encoder", dict(n_layers=1, n_streams=2, extra={"window": 70}, scheme=1), 30),
+    "qwen_scaled": ("qwen", dict(n_layers=2, n_streams=3, extra={"window": 100}), 120),
+    "mixed_small": ("mixed", dict(n_layers=1, n_streams=9, extra={}), 60),
+}
+
+
+@pytest.mark.parametrize("case", sorted(SMALL))
+def test_small_every_output(case):
+    name, over, ticks = SMALL[case]
+    wl = synth.workload(name, **over)
+    want = set()
+    w = wl.windows()
+    fill = wl.initial_fill()
+    counts = fill.copy()
+    for t in range(ticks):
+        counts[wl.active_at_tick(t)] += 1
+    for s in range(wl.n_streams):
+        for layer in range(wl.n_layers):
+            for n_old in range(int(fill[s]) * wl.q_per_step, int(counts[s]) * wl.q_per_step, wl.q_per_step):
+                want.add((s, layer, n_old))
+    run = run_gpu(wl, ticks, want)
+    assert len(run.samples) == len(want)
+    e_o, e_l = compare(run, wl)
+    print(case, "max out err", e_o, "max lse err", e_l)
+
+
+FULL = {
+    "tiny": ("tiny", dict(), 1000, [0, 1, 374, 375, 376, 998, 999], [0]),
+    "qwen": ("qwen", dict(), 1000, [0, 1, 374, 375, 376, 999], [0, 17, 40, 63]),
+    "encoder": ("encoder", dict(), 200, [0, 4, 744, 748, 752, 796], [0, 31]),
+    "mixed": ("mixed", dict(), 400, None, [0, 1, 2, 3]),
+    "voxtral": ("voxtral", dict(), 8200, [0, 8191, 8192, 8193, 8199], [0, 15]),
+}
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("case", sorted(FULL))
+def test_full_size_sampled(case):
+    name, over, ticks, steps, streams = FULL[case]
+    wl = synth.workload(name, **over)
+    layers = sorted({0, wl.n_layers // 2, wl.n_layers - 1})
+    want = set()
+    if steps is None:   # mixed clocks: sample every 37th token of the chosen streams
+        steps = list(range(0, 500, 37))
+    for s in streams:
+        for layer in layers:
+            for n_old in steps:
+                want.add((s, layer, n_old))
+    run = run_gpu(wl, ticks, want, streams_of_interest=streams)
+    assert len(run.samples) >= len(want) // 2
+    e_o, e_l = compare(run, wl)
+    for s in streams:
+        assert list(run.states[s].values()) == run.ring[s].state()
+    print(case, len(run.samples), "samples; max out err", e_o, "max lse err", e_l)
