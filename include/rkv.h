@@ -201,6 +201,30 @@ RKV_API int rkv_decode_attn(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv
 RKV_API int rkv_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active, const rkv_bf16* q,
              const rkv_bf16* k, const rkv_bf16* v, rkv_bf16* out, float* lse, void* stream);
 
+/* Decode attention that allocates nothing and needs no scratch from the
+ * caller.  No page describes this call: it exists for callers that may not
+ * allocate device memory where they run attention, such as a real-time audio
+ * callback that cannot risk an allocator call synchronising the device
+ * inside its 80 ms clock step, or a plug-in inside a serving engine whose
+ * caching allocator already holds the free HBM.
+ *
+ * Same arguments, call-order rules and results as rkv_decode_attn, but the
+ * split-K partial results go to a fixed array compiled into the library
+ * (8 MiB per device, held by every GPU that loads the library until the
+ * process exits) instead of the handle's state buffer.  A call that needs
+ * more than 8 MiB of partials ((2 + head_dim) floats per active stream,
+ * query row and split) returns RKV_ERR_CAPACITY with the sizes in the
+ * message.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current, so make that first call
+ * before any stream capture.  Every call on a device shares the one array,
+ * and the array keeps the last call's contents; nothing in it needs to start
+ * at zero, because every partial the merge reads is written earlier in the
+ * same call.  Calls that overlap on the GPU (other streams, other handles,
+ * other threads) race on the array: the caller must serialise them.  No
+ * cudaMalloc, cudaFree or allocating library routine is called. */
+RKV_API int rkv_decode_attn_static(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv_bf16* out,
+                                   float* lse, void* stream);
+
 /* Copy one stream's device state to host `out` (RKV_STATE_FIELDS int64):
  * n, len, evicted, kv_pos_offset, rope_base, head_slot, W, P0.  Waits for
  * `stream`. */

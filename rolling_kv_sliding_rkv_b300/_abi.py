@@ -63,6 +63,7 @@ _SIGS = {
     "rkv_append_rope": [_vp, _i32, _vp, _vp, _vp],
     "rkv_rebase": [_vp, _i32, _vp],
     "rkv_decode_attn": [_vp, _i32, _vp, _vp, _vp, _vp],
+    "rkv_decode_attn_static": [_vp, _i32, _vp, _vp, _vp, _vp],
     "rkv_step": [_vp, C.POINTER(_i32), _i32, _vp, _vp, _vp, _vp, _vp, _vp],
     "rkv_get_stream_state": [_vp, _i32, C.POINTER(_i64), _vp],
     "rkv_sync_status": [_vp, _vp],
@@ -169,6 +170,10 @@ def rkv_rebase(h: int, layer: int, stream=None) -> None:
 
 def rkv_decode_attn(h: int, layer: int, q, out, lse=None, stream=None) -> None:
     _check(_lib.rkv_decode_attn(h, layer, _ptr(q), _ptr(out), _ptr(lse), _stream(stream)), h)
+
+
+def rkv_decode_attn_static(h: int, layer: int, q, out, lse=None, stream=None) -> None:
+    _check(_lib.rkv_decode_attn_static(h, layer, _ptr(q), _ptr(out), _ptr(lse), _stream(stream)), h)
 
 
 def rkv_step(h: int, active_ids, q, k, v, out, lse=None, stream=None) -> None:

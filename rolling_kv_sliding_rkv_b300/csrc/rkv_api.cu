@@ -424,4 +424,28 @@ int rkv_gen_step_inputs(rkv_handle* h, uint64_t seed, int32_t layer, float scale
   return e == cudaSuccess ? RKV_OK : cuda_fail(h, e, "gen_step_inputs launch");
 }
 
+int rkv_decode_attn_static(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv_bf16* out, float* lse,
+                           void* stream) {
+  if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
+  if (!h->step_open) return fail(h, RKV_ERR_STATE, "no open step (call rkv_begin_step)");
+  if (!check_layer(h, layer)) return fail(h, RKV_ERR_INVALID_ARG, "layer out of range");
+  if (!q || !out || !aligned16(q) || !aligned16(out) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return fail(h, RKV_ERR_INVALID_ARG, "q and out must be non-NULL and 16-byte aligned");
+  if (!h->appended[layer]) return fail(h, RKV_ERR_STATE, "rkv_decode_attn_static before rkv_append_rope for this layer");
+  if (h->cfg.scheme == RKV_SCHEME_EXACT_REBASE && !h->rebased[layer])
+    return fail(h, RKV_ERR_STATE, "rkv_decode_attn_static before rkv_rebase for this layer");
+  const size_t need = rkv::static_scratch_need(h->view, h->n_active);
+  if (need > rkv::static_scratch_floats()) {
+    char buf[200];
+    snprintf(buf, sizeof buf,
+             "rkv_decode_attn_static needs %zu bytes of scratch for %d active streams; the fixed array holds %zu",
+             need * sizeof(float), h->n_active, rkv::static_scratch_floats() * sizeof(float));
+    return fail(h, RKV_ERR_CAPACITY, buf);
+  }
+  cudaError_t e =
+      rkv::launch_decode_attn_static(h->view, h->n_active, layer, q, out, lse, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "decode_attn_static launch");
+  return RKV_OK;
+}
+
 }  // extern "C"

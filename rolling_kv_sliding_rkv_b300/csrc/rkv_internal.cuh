@@ -126,6 +126,11 @@ cudaError_t launch_append_rope(const DevView& v, int n_active, int layer, const 
 cudaError_t launch_rebase(const DevView& v, int n_active, int layer, cudaStream_t st);
 cudaError_t launch_decode_attn(const DevView& v, int n_active, int layer, const uint16_t* q, uint16_t* out,
                                float* lse, cudaStream_t st);
+// decode attention with its split-K scratch in the library's fixed array (rkv_noalloc.cu)
+size_t static_scratch_floats();
+size_t static_scratch_need(const DevView& v, int n_active);
+cudaError_t launch_decode_attn_static(const DevView& v, int n_active, int layer, const uint16_t* q, uint16_t* out,
+                                      float* lse, cudaStream_t st);
 cudaError_t launch_rope_cossin(const int64_t* pos, int n, int head_dim, const Omegas& w, float* cs,
                                cudaStream_t st);
 cudaError_t launch_gen_tokens(uint64_t seed, uint32_t tag, int32_t stream_id, int32_t layer, int64_t token0,
