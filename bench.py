@@ -46,6 +46,7 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--inputs", type=int, default=4, help="distinct resident input sets cycled by the steps")
+    p.add_argument("--layers", type=int, default=None, help="override the workload's layer count (profiling cases)")
     return p.parse_args()
 
 
@@ -220,9 +221,12 @@ def run_ours(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl = synth.workload(args.workload)
+    over = {}
     if args.scheme:
-        wl = synth.workload(args.workload, scheme=1 if args.scheme == "exact" else 0)
+        over["scheme"] = 1 if args.scheme == "exact" else 0
+    if args.layers:
+        over["n_layers"] = args.layers
+    wl = synth.workload(args.workload, **over)
     scheme_name = "exact re-base" if wl.scheme == 1 else "offset-only"
     S, L, Q, hq, hkv, d = wl.n_streams, wl.n_layers, wl.q_per_step, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
     windows = wl.windows()
