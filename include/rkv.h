@@ -44,10 +44,14 @@
  * rkv_rebase in the offset-only scheme, or opening the next step while a
  * layer lacks them returns RKV_ERR_STATE.
  *
- * Memory in HBM (pool_dev).  Three regions of [L][pages][Hkv][page_size][d]
- * 16-bit elements: rotated keys (fp16), values (bf16), and in the exact
- * scheme pre-RoPE keys (bf16).  Stream s owns ceil(W_s / page_size) pages;
- * token j lives in ring slot j mod W_s, so eviction moves no data.
+ * Memory in HBM (pool_dev).  Regions of [L][pages][Hkv][page_size][d]
+ * 16-bit elements: rotated keys (fp16; not in RKV_SCHEME_EXACT_ON_READ),
+ * values (bf16), and in the exact schemes pre-RoPE keys (bf16).  Stream s
+ * owns ceil(W_s / page_size) pages; token j lives in ring slot j mod W_s, so
+ * eviction moves no data.  Within a row of d elements the 16-byte chunk c
+ * sits at chunk position c ^ (row offset in the page & 7), which makes a
+ * page copied verbatim into shared memory bank-conflict-free for 8x8 matrix
+ * loads.  rkv_create zeroes the pool.
  */
 #ifndef RKV_H_
 #define RKV_H_
@@ -81,7 +85,10 @@ typedef enum {
 
 typedef enum {
   RKV_SCHEME_OFFSET_ONLY = 0,  /* K rotated once at P0 + j; kv_pos_offset bookkeeping only */
-  RKV_SCHEME_EXACT_REBASE = 1  /* K kept at window-relative positions, re-based on every roll */
+  RKV_SCHEME_EXACT_REBASE = 1, /* K kept at window-relative positions, re-based on every roll */
+  RKV_SCHEME_EXACT_ON_READ = 2 /* the same window-relative positions and re-base bookkeeping, but the
+                                * rotation R(j - rope_base) is applied to the pre-RoPE key as attention
+                                * reads it, so no re-based key is ever stored (re-base moves no bytes) */
 } rkv_scheme;
 
 /* Shape and policy of one handle.  All layers share it. */
@@ -175,14 +182,17 @@ RKV_API int rkv_append_rope(rkv_handle* h, int32_t layer, const rkv_bf16* k, con
  * stream whose step re-bases is rotated by R(-delta), which brings the
  * stored positions back to j - rope_base inside the window.  The rotation is
  * applied to the key's pre-RoPE copy with the composite angle, so a stored
- * key carries one bf16 rounding however many times it was re-based.  Exact
- * scheme only (RKV_ERR_STATE otherwise); must be called once per layer per
+ * key carries one fp16 rounding however many times it was re-based.  Exact
+ * schemes only (RKV_ERR_STATE otherwise); must be called once per layer per
  * step, before rkv_decode_attn of that layer (a no-op on the device for
- * streams that do not re-base this step). */
+ * streams that do not re-base this step).  In RKV_SCHEME_EXACT_ON_READ it
+ * enqueues nothing: rkv_decode_attn applies the same rotation to every key
+ * it reads. */
 RKV_API int rkv_rebase(rkv_handle* h, int32_t layer, void* stream);
 
 /* Windowed GQA attention for one layer (explainer 第 3 步), split-K over the
- * window with a log-sum-exp merge.
+ * window with a log-sum-exp merge of the splits in distributed shared memory
+ * (no scratch memory).
  *   q     device [A][Q][Hq][d] bf16, pre-RoPE queries of the new tokens;
  *         rotated inside the kernel in fp32 at the same positions as the
  *         step's keys (never rounded back to 16 bits), not modified
@@ -194,8 +204,18 @@ RKV_API int rkv_rebase(rkv_handle* h, int32_t layer, void* stream);
 RKV_API int rkv_decode_attn(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv_bf16* out,
                             float* lse, void* stream);
 
-/* The whole step for all layers: rkv_begin_step, then per layer
- * rkv_rebase (exact scheme), rkv_append_rope, rkv_decode_attn.
+/* rkv_decode_attn for layers layer0 .. layer0 + n_layers - 1 of the open
+ * step in one launch (the layers' queries must all be known, as in
+ * rkv_step).  q and out are [n_layers][A][Q][Hq][d], lse [n_layers][A][Q][Hq]
+ * (may be NULL); every layer in the range must have had rkv_append_rope (and
+ * rkv_rebase in the exact schemes) in this step, else RKV_ERR_STATE. */
+RKV_API int rkv_decode_attn_layers(rkv_handle* h, int32_t layer0, int32_t n_layers, const rkv_bf16* q,
+                                   rkv_bf16* out, float* lse, void* stream);
+
+/* The whole step for all layers: rkv_begin_step, then rkv_rebase (exact
+ * scheme), rkv_append_rope and rkv_decode_attn for every layer, each as one
+ * launch over all layers (the layers' inputs are all given, so their work is
+ * independent).  Same results as the per-layer calls.
  *   q     device [L][A][Q][Hq][d], k, v [L][A][Q][Hkv][d], all pre-RoPE bf16
  *   out   device [L][A][Q][Hq][d], lse [L][A][Q][Hq] (may be NULL) */
 RKV_API int rkv_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active, const rkv_bf16* q,

@@ -24,6 +24,7 @@ RKV_ERR_DEVICE_BOUNDS = -7
 RKV_ERR_DEVICE_RANGE = -8
 RKV_SCHEME_OFFSET_ONLY = 0
 RKV_SCHEME_EXACT_REBASE = 1
+RKV_SCHEME_EXACT_ON_READ = 2
 RKV_MAX_STREAMS = 1024
 RKV_STATE_FIELDS = 8
 STATE_FIELDS = ("n", "len", "evicted", "kv_pos_offset", "rope_base", "head_slot", "W", "P0")
@@ -64,6 +65,7 @@ _SIGS = {
     "rkv_rebase": [_vp, _i32, _vp],
     "rkv_decode_attn": [_vp, _i32, _vp, _vp, _vp, _vp],
     "rkv_decode_attn_static": [_vp, _i32, _vp, _vp, _vp, _vp],
+    "rkv_decode_attn_layers": [_vp, _i32, _i32, _vp, _vp, _vp, _vp],
     "rkv_step": [_vp, C.POINTER(_i32), _i32, _vp, _vp, _vp, _vp, _vp, _vp],
     "rkv_get_stream_state": [_vp, _i32, C.POINTER(_i64), _vp],
     "rkv_sync_status": [_vp, _vp],
@@ -174,6 +176,10 @@ def rkv_decode_attn(h: int, layer: int, q, out, lse=None, stream=None) -> None:
 
 def rkv_decode_attn_static(h: int, layer: int, q, out, lse=None, stream=None) -> None:
     _check(_lib.rkv_decode_attn_static(h, layer, _ptr(q), _ptr(out), _ptr(lse), _stream(stream)), h)
+
+
+def rkv_decode_attn_layers(h: int, layer0: int, n_layers: int, q, out, lse=None, stream=None) -> None:
+    _check(_lib.rkv_decode_attn_layers(h, layer0, n_layers, _ptr(q), _ptr(out), _ptr(lse), _stream(stream)), h)
 
 
 def rkv_step(h: int, active_ids, q, k, v, out, lse=None, stream=None) -> None:

@@ -40,7 +40,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Layout {
-  size_t state, page_table, desc, cs_new, omega, rope_table, part_ml, part_o, status, total;
+  size_t state, page_table, desc, cs_new, omega, rope_table, status, total;
   size_t pool_region_elems;  // elements of one pool region (all layers)
   int32_t max_pages, n_pages, t_rows, w_max, regions;
 };
@@ -59,7 +59,7 @@ bool validate_config(const rkv_config* c, std::string* why) {
   if (c->n_q_heads > 256 || c->n_kv_heads > 256) return bad("at most 256 heads");
   if (c->page_size != 16 && c->page_size != 32 && c->page_size != 64 && c->page_size != 128)
     return bad("page_size must be 16, 32, 64 or 128");
-  if (c->scheme != RKV_SCHEME_OFFSET_ONLY && c->scheme != RKV_SCHEME_EXACT_REBASE) return bad("unknown scheme");
+  if (c->scheme != RKV_SCHEME_OFFSET_ONLY && !rkv::exact_scheme(c->scheme)) return bad("unknown scheme");
   if (c->rebase_interval < 1) return bad("rebase_interval must be >= 1");
   if (c->reserved != 0) return bad("reserved must be 0");
   if (!(c->rope_theta > 1.0) || !std::isfinite(c->rope_theta)) return bad("rope_theta must be finite and > 1");
@@ -95,7 +95,7 @@ bool compute_layout(const rkv_config* c, const int32_t* window, Layout* L, std::
   L->w_max = w_max;
   L->max_pages = (w_max + c->page_size - 1) / c->page_size;
   L->n_pages = static_cast<int32_t>(n_pages);
-  const bool exact = c->scheme == RKV_SCHEME_EXACT_REBASE;
+  const bool exact = rkv::exact_scheme(c->scheme);
   // window-relative positions of the exact scheme stay below W + interval - 1
   const int64_t t_rows = exact ? static_cast<int64_t>(w_max) + c->rebase_interval - 1 : 0;
   if (t_rows > (1 << 24)) {
@@ -103,10 +103,9 @@ bool compute_layout(const rkv_config* c, const int32_t* window, Layout* L, std::
     return false;
   }
   L->t_rows = static_cast<int32_t>(t_rows);
-  L->regions = exact ? 3 : 2;
+  // rotated keys, values, pre-RoPE keys (exact re-base); rotate-on-read keeps no rotated copy
+  L->regions = c->scheme == RKV_SCHEME_EXACT_REBASE ? 3 : 2;
   const int half = c->head_dim / 2;
-  const size_t rows = static_cast<size_t>(S) * c->q_per_step * c->n_q_heads;
-  const size_t splits_max = static_cast<size_t>(L->max_pages);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -119,8 +118,6 @@ bool compute_layout(const rkv_config* c, const int32_t* window, Layout* L, std::
   L->cs_new = take(static_cast<size_t>(S) * c->q_per_step * half * 2 * sizeof(float));
   L->omega = take(static_cast<size_t>(half) * sizeof(double));
   L->rope_table = take(static_cast<size_t>(t_rows) * half * 2 * sizeof(float));
-  L->part_ml = take(rows * splits_max * 2 * sizeof(float));
-  L->part_o = take(rows * splits_max * c->head_dim * sizeof(float));
   L->status = take(4 * sizeof(int32_t));
   L->total = off;
   L->pool_region_elems = static_cast<size_t>(c->n_layers) * n_pages * c->n_kv_heads * c->page_size * c->head_dim;
@@ -207,13 +204,19 @@ int rkv_create(const rkv_config* cfg, const int32_t* window, const int64_t* star
   v.cs_new = reinterpret_cast<float*>(sb + L.cs_new);
   v.omega = reinterpret_cast<double*>(sb + L.omega);
   v.rope_table = L.t_rows ? reinterpret_cast<float*>(sb + L.rope_table) : nullptr;
-  v.part_ml = reinterpret_cast<float*>(sb + L.part_ml);
-  v.part_o = reinterpret_cast<float*>(sb + L.part_o);
+  v.part_ml = nullptr;  // split-K partials: only the scratch form of decode attention has them
+  v.part_o = nullptr;
   v.status = reinterpret_cast<int32_t*>(sb + L.status);
   uint16_t* pool = static_cast<uint16_t*>(pool_dev);
-  v.k_rot = pool;
-  v.v = pool + L.pool_region_elems;
-  v.k_raw = L.regions == 3 ? pool + 2 * L.pool_region_elems : nullptr;
+  if (cfg->scheme == RKV_SCHEME_EXACT_ON_READ) {
+    v.k_rot = nullptr;
+    v.k_raw = pool;
+    v.v = pool + L.pool_region_elems;
+  } else {
+    v.k_rot = pool;
+    v.v = pool + L.pool_region_elems;
+    v.k_raw = L.regions == 3 ? pool + 2 * L.pool_region_elems : nullptr;
+  }
   v.layer_stride = static_cast<int64_t>(L.n_pages) * cfg->n_kv_heads * cfg->page_size * cfg->head_dim;
   v.n_streams = cfg->n_streams;
   v.n_layers = cfg->n_layers;
@@ -229,12 +232,7 @@ int rkv_create(const rkv_config* cfg, const int32_t* window, const int64_t* star
   v.rebase_interval = cfg->rebase_interval;
   const double scale = cfg->softmax_scale > 0.0 ? cfg->softmax_scale : 1.0 / std::sqrt(static_cast<double>(cfg->head_dim));
   v.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
-  // Split the window into enough pieces to give every SM several blocks.
-  const int64_t items = static_cast<int64_t>(cfg->n_streams) * cfg->n_kv_heads * L.max_pages;
-  int64_t pps = items / (8 * static_cast<int64_t>(h->num_sms));
-  pps = pps < 1 ? 1 : pps > L.max_pages ? L.max_pages : pps;
-  v.pages_per_split = static_cast<int32_t>(pps);
-  v.splits = static_cast<int32_t>((L.max_pages + pps - 1) / pps);
+  v.num_sms = h->num_sms;
 
   // host images of the stream state, page tables and RoPE frequencies
   const int S = cfg->n_streams, half = cfg->head_dim / 2;
@@ -253,7 +251,11 @@ int rkv_create(const rkv_config* cfg, const int32_t* window, const int64_t* star
   for (int i = 0; i < half; ++i) omega[i] = std::pow(cfg->rope_theta, -2.0 * i / cfg->head_dim);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  e = cudaMemcpyAsync(v.state, state.data(), state.size() * sizeof(int64_t), cudaMemcpyHostToDevice, st);
+  // a zeroed pool keeps never-written slots finite (they are masked, but a masked
+  // score still multiplies its value row by zero)
+  e = cudaMemsetAsync(pool_dev, 0, need_pool, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(v.state, state.data(), state.size() * sizeof(int64_t), cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(v.page_table, table.data(), table.size() * sizeof(int32_t), cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(v.omega, omega.data(), half * sizeof(double), cudaMemcpyHostToDevice, st);
@@ -275,7 +277,7 @@ int rkv_begin_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active, v
   if (!active_ids || n_active < 1 || n_active > h->cfg.n_streams)
     return fail(h, RKV_ERR_INVALID_ARG, "active_ids must list 1 .. n_streams streams");
   if (h->step_open) {
-    const bool exact = h->cfg.scheme == RKV_SCHEME_EXACT_REBASE;
+    const bool exact = rkv::exact_scheme(h->cfg.scheme);
     for (int l = 0; l < h->cfg.n_layers; ++l)
       if (!h->appended[l] || (exact && !h->rebased[l]))
         return fail(h, RKV_ERR_STATE, "previous step left a layer without rkv_append_rope (or rkv_rebase)");
@@ -306,7 +308,7 @@ int rkv_append_rope(rkv_handle* h, int32_t layer, const rkv_bf16* k, const rkv_b
   if (!k || !v || !aligned16(k) || !aligned16(v))
     return fail(h, RKV_ERR_INVALID_ARG, "k and v must be non-NULL and 16-byte aligned");
   if (h->appended[layer]) return fail(h, RKV_ERR_STATE, "rkv_append_rope called twice for this layer in this step");
-  cudaError_t e = rkv::launch_append_rope(h->view, h->n_active, layer, k, v, static_cast<cudaStream_t>(stream));
+  cudaError_t e = rkv::launch_append_rope(h->view, h->n_active, layer, 1, k, v, 0, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(h, e, "append_rope launch");
   h->appended[layer] = 1;
   return RKV_OK;
@@ -314,11 +316,11 @@ int rkv_append_rope(rkv_handle* h, int32_t layer, const rkv_bf16* k, const rkv_b
 
 int rkv_rebase(rkv_handle* h, int32_t layer, void* stream) {
   if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
-  if (h->cfg.scheme != RKV_SCHEME_EXACT_REBASE) return fail(h, RKV_ERR_STATE, "rkv_rebase needs the exact re-base scheme");
+  if (!rkv::exact_scheme(h->cfg.scheme)) return fail(h, RKV_ERR_STATE, "rkv_rebase needs an exact re-base scheme");
   if (!h->step_open) return fail(h, RKV_ERR_STATE, "no open step (call rkv_begin_step)");
   if (!check_layer(h, layer)) return fail(h, RKV_ERR_INVALID_ARG, "layer out of range");
   if (h->rebased[layer]) return fail(h, RKV_ERR_STATE, "rkv_rebase called twice for this layer in this step");
-  cudaError_t e = rkv::launch_rebase(h->view, h->n_active, layer, static_cast<cudaStream_t>(stream));
+  cudaError_t e = rkv::launch_rebase(h->view, h->n_active, layer, 1, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(h, e, "rebase launch");
   h->rebased[layer] = 1;
   return RKV_OK;
@@ -331,28 +333,57 @@ int rkv_decode_attn(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv_bf16* o
   if (!q || !out || !aligned16(q) || !aligned16(out) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
     return fail(h, RKV_ERR_INVALID_ARG, "q and out must be non-NULL and 16-byte aligned");
   if (!h->appended[layer]) return fail(h, RKV_ERR_STATE, "rkv_decode_attn before rkv_append_rope for this layer");
-  if (h->cfg.scheme == RKV_SCHEME_EXACT_REBASE && !h->rebased[layer])
+  if (rkv::exact_scheme(h->cfg.scheme) && !h->rebased[layer])
     return fail(h, RKV_ERR_STATE, "rkv_decode_attn before rkv_rebase for this layer");
-  cudaError_t e = rkv::launch_decode_attn(h->view, h->n_active, layer, q, out, lse, static_cast<cudaStream_t>(stream));
+  cudaError_t e = rkv::launch_decode_attn(h->view, h->n_active, layer, 1, q, out, lse, 0, 0,
+                                          static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "decode_attn launch");
+  return RKV_OK;
+}
+
+int rkv_decode_attn_layers(rkv_handle* h, int32_t layer0, int32_t n_layers, const rkv_bf16* q, rkv_bf16* out,
+                           float* lse, void* stream) {
+  if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
+  if (!h->step_open) return fail(h, RKV_ERR_STATE, "no open step (call rkv_begin_step)");
+  if (n_layers < 1 || layer0 < 0 || layer0 + n_layers > h->cfg.n_layers)
+    return fail(h, RKV_ERR_INVALID_ARG, "layer range outside [0, n_layers)");
+  if (!q || !out || !aligned16(q) || !aligned16(out) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return fail(h, RKV_ERR_INVALID_ARG, "q and out must be non-NULL and 16-byte aligned");
+  const bool exact = rkv::exact_scheme(h->cfg.scheme);
+  for (int l = layer0; l < layer0 + n_layers; ++l)
+    if (!h->appended[l] || (exact && !h->rebased[l]))
+      return fail(h, RKV_ERR_STATE, "rkv_decode_attn_layers before rkv_append_rope (or rkv_rebase) of a layer");
+  const rkv_config& c = h->cfg;
+  const int64_t rows = static_cast<int64_t>(h->n_active) * c.q_per_step;
+  cudaError_t e = rkv::launch_decode_attn(h->view, h->n_active, layer0, n_layers, q, out, lse,
+                                          rows * c.n_q_heads * c.head_dim, rows * c.n_q_heads,
+                                          static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(h, e, "decode_attn launch");
   return RKV_OK;
 }
 
 int rkv_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active, const rkv_bf16* q, const rkv_bf16* k,
              const rkv_bf16* v, rkv_bf16* out, float* lse, void* stream) {
+  if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
+  if (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return fail(h, RKV_ERR_INVALID_ARG, "q, k, v and out must be non-NULL and 16-byte aligned");
   int rc = rkv_begin_step(h, active_ids, n_active, stream);
   if (rc != RKV_OK) return rc;
   const rkv_config& c = h->cfg;
-  const size_t rows = static_cast<size_t>(n_active) * c.q_per_step;
-  const size_t q_stride = rows * c.n_q_heads * c.head_dim, kv_stride = rows * c.n_kv_heads * c.head_dim;
-  const size_t lse_stride = rows * c.n_q_heads;
-  for (int l = 0; l < c.n_layers; ++l) {
-    if (c.scheme == RKV_SCHEME_EXACT_REBASE && (rc = rkv_rebase(h, l, stream)) != RKV_OK) return rc;
-    if ((rc = rkv_append_rope(h, l, k + l * kv_stride, v + l * kv_stride, stream)) != RKV_OK) return rc;
-    if ((rc = rkv_decode_attn(h, l, q + l * q_stride, out + l * q_stride, lse ? lse + l * lse_stride : nullptr,
-                              stream)) != RKV_OK)
-      return rc;
-  }
+  const int64_t rows = static_cast<int64_t>(n_active) * c.q_per_step;
+  const int64_t q_stride = rows * c.n_q_heads * c.head_dim, kv_stride = rows * c.n_kv_heads * c.head_dim;
+  const int64_t lse_stride = rows * c.n_q_heads;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (rkv::exact_scheme(c.scheme)) e = rkv::launch_rebase(h->view, n_active, 0, c.n_layers, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "rebase launch");
+  std::fill(h->rebased.begin(), h->rebased.end(), 1);
+  e = rkv::launch_append_rope(h->view, n_active, 0, c.n_layers, k, v, kv_stride, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "append_rope launch");
+  std::fill(h->appended.begin(), h->appended.end(), 1);
+  e = rkv::launch_decode_attn(h->view, n_active, 0, c.n_layers, q, out, lse, q_stride, lse_stride, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "decode_attn launch");
   return RKV_OK;
 }
 
@@ -432,7 +463,7 @@ int rkv_decode_attn_static(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv_
   if (!q || !out || !aligned16(q) || !aligned16(out) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
     return fail(h, RKV_ERR_INVALID_ARG, "q and out must be non-NULL and 16-byte aligned");
   if (!h->appended[layer]) return fail(h, RKV_ERR_STATE, "rkv_decode_attn_static before rkv_append_rope for this layer");
-  if (h->cfg.scheme == RKV_SCHEME_EXACT_REBASE && !h->rebased[layer])
+  if (rkv::exact_scheme(h->cfg.scheme) && !h->rebased[layer])
     return fail(h, RKV_ERR_STATE, "rkv_decode_attn_static before rkv_rebase for this layer");
   const size_t need = rkv::static_scratch_need(h->view, h->n_active);
   if (need > rkv::static_scratch_floats()) {

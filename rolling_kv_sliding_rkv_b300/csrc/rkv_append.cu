@@ -9,105 +9,163 @@
 // inputs, where bf16 storage would give ~1.6e-3 (the voxtral.c article, §七,
 // mentions an fp16 KV cache).  Values and pre-RoPE keys are stored as the
 // bf16 inputs, bit for bit.
+//
+// Both kernels move 16-byte chunks: a thread owns chunk c (elements 8c ..
+// 8c+7) and its rotation partner c + d/16 (elements + d/2) of one key row,
+// written at their swizzled chunk positions (rkv_internal.cuh).
 #include "rkv_internal.cuh"
 
 namespace rkv {
 namespace {
 
-constexpr int kWarps = 4;
+__device__ __forceinline__ void unpack8(const uint4 u, float (&x)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    x[2 * j] = __uint_as_float(w[j] << 16);
+    x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+}
 
-// One warp per (active stream, new token, kv head): rotate k with the
-// token's cos/sin, write it and v into the token's ring slot (and the
-// pre-RoPE k in the exact scheme).
-__global__ void __launch_bounds__(kWarps * 32) append_rope_kernel(DevView v, int layer, const uint16_t* __restrict__ k,
-                                                                  const uint16_t* __restrict__ val) {
-  const int row = blockIdx.x;  // a * Q + t
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kvh = blockIdx.y * kWarps + warp;
-  const int hkv = v.n_kv_heads, d = v.head_dim, half = d / 2;
-  if (kvh >= hkv) return;
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  return static_cast<uint32_t>(f32_to_f16(lo)) | (static_cast<uint32_t>(f32_to_f16(hi)) << 16);
+}
+
+// Rotate 8 pairs: xa[j] with xb[j] by (cos, sin) cs[2j], cs[2j+1]; fp16 out.
+__device__ __forceinline__ void rotate8(const float (&xa)[8], const float (&xb)[8], const float* cs, uint4* ya,
+                                        uint4* yb, bool* fits) {
+  float ra[8], rb[8];
+  bool ok = true;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float c = cs[2 * j], s = cs[2 * j + 1];
+    ra[j] = xa[j] * c - xb[j] * s;
+    rb[j] = xa[j] * s + xb[j] * c;
+    ok = ok && fits_f16(ra[j]) && fits_f16(rb[j]);
+  }
+  *ya = make_uint4(pack_h2(ra[0], ra[1]), pack_h2(ra[2], ra[3]), pack_h2(ra[4], ra[5]), pack_h2(ra[6], ra[7]));
+  *yb = make_uint4(pack_h2(rb[0], rb[1]), pack_h2(rb[2], rb[3]), pack_h2(rb[4], rb[5]), pack_h2(rb[6], rb[7]));
+  *fits = ok;
+}
+
+// One thread per (layer, active stream, new token, kv head, chunk pair).
+__global__ void __launch_bounds__(128) append_rope_kernel(DevView v, int layer0, int n_rows, const uint16_t* __restrict__ k,
+                                                          const uint16_t* __restrict__ val, int64_t kv_layer_stride) {
+  const int d = v.head_dim, half = d / 2, cpairs = d / 16, hkv = v.n_kv_heads;
+  const int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  const int64_t per_layer = static_cast<int64_t>(n_rows) * hkv * cpairs;
+  const int lz = blockIdx.y;
+  if (idx >= per_layer) return;
+  const int cp = static_cast<int>(idx % cpairs);
+  const int kvh = static_cast<int>((idx / cpairs) % hkv);
+  const int row = static_cast<int>(idx / (static_cast<int64_t>(cpairs) * hkv));  // a * Q + t
+  const int layer = layer0 + lz;
   const int a = row / v.q_per_step, t = row % v.q_per_step;
-  const float* cs = v.cs_new + static_cast<int64_t>(row) * half * 2;
   const StepDesc dsc = v.desc[a];
   const int64_t tok = dsc.n_old + t;
   const int slot = static_cast<int>(tok % dsc.window);
   const int ring_page = slot / v.page_size;
   if (ring_page >= v.max_pages) {
-    if (lane == 0) record_error(v.status, DEV_BOUNDS, 1, ring_page);
+    record_error(v.status, DEV_BOUNDS, 1, ring_page);
     return;
   }
   const int page = v.page_table[static_cast<int64_t>(dsc.stream) * v.max_pages + ring_page];
   if (page < 0 || page >= v.n_pages) {
-    if (lane == 0) record_error(v.status, DEV_BOUNDS, 2, page);
+    record_error(v.status, DEV_BOUNDS, 2, page);
     return;
   }
-  const int64_t dst = pool_offset(v, layer, page, kvh, slot % v.page_size);
-  const int64_t src = (static_cast<int64_t>(row) * hkv + kvh) * d;
-  for (int i = lane; i < half; i += 32) {
-    const float c = cs[2 * i], s = cs[2 * i + 1];
-    const uint16_t ra = k[src + i], rb = k[src + i + half];
-    const float xa = bf16_to_f32(ra), xb = bf16_to_f32(rb);
-    const float ya = xa * c - xb * s, yb = xa * s + xb * c;
-    if (!fits_f16(ya) || !fits_f16(yb)) record_error(v.status, DEV_RANGE, 1, i);
-    v.k_rot[dst + i] = f32_to_f16(ya);
-    v.k_rot[dst + i + half] = f32_to_f16(yb);
-    if (v.k_raw) {
-      v.k_raw[dst + i] = ra;
-      v.k_raw[dst + i + half] = rb;
-    }
-    v.v[dst + i] = val[src + i];
-    v.v[dst + i + half] = val[src + i + half];
+  const int off = slot % v.page_size;
+  const int64_t dst = pool_offset(v, layer, page, kvh, off);
+  const int pa = swizzle_chunk(cp, off) * 8, pb = swizzle_chunk(cp + cpairs, off) * 8;
+  const int64_t src = lz * kv_layer_stride + (static_cast<int64_t>(row) * hkv + kvh) * d;
+  const uint4 ka = *reinterpret_cast<const uint4*>(k + src + cp * 8);
+  const uint4 kb = *reinterpret_cast<const uint4*>(k + src + half + cp * 8);
+  *reinterpret_cast<uint4*>(v.v + dst + pa) = *reinterpret_cast<const uint4*>(val + src + cp * 8);
+  *reinterpret_cast<uint4*>(v.v + dst + pb) = *reinterpret_cast<const uint4*>(val + src + half + cp * 8);
+  if (v.k_raw) {
+    *reinterpret_cast<uint4*>(v.k_raw + dst + pa) = ka;
+    *reinterpret_cast<uint4*>(v.k_raw + dst + pb) = kb;
+  }
+  float xa[8], xb[8];
+  unpack8(ka, xa);
+  unpack8(kb, xb);
+  if (v.k_rot) {
+    const float* cs = v.cs_new + (static_cast<int64_t>(row) * half + cp * 8) * 2;
+    uint4 ya, yb;
+    bool fits;
+    rotate8(xa, xb, cs, &ya, &yb, &fits);
+    if (!fits) record_error(v.status, DEV_RANGE, 1, cp);
+    *reinterpret_cast<uint4*>(v.k_rot + dst + pa) = ya;
+    *reinterpret_cast<uint4*>(v.k_rot + dst + pb) = yb;
+  } else {
+    // rotate-on-read: the rotation happens in attention; |R x| <= sqrt(2) max(|a|, |b|) must fit fp16
+    bool ok = true;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ok = ok && fmaxf(fabsf(xa[j]), fabsf(xb[j])) < 46000.0f;
+    if (!ok) record_error(v.status, DEV_RANGE, 2, cp);
   }
 }
 
-// Grid (active stream, ring page, kv head).  For a stream that re-bases this
-// step, every retained key written before the step (tokens evicted ..
-// n_old - 1) becomes R(j - rope_base) applied to its pre-RoPE copy: the
-// exact result of rotating the previously stored key by R(-delta), with one
-// rounding however many re-bases the key has seen.
-__global__ void __launch_bounds__(128) rebase_kernel(DevView v, int layer) {
-  const int a = blockIdx.x, ring_page = blockIdx.y, kvh = blockIdx.z;
+// One thread per (layer, active stream, ring slot, kv head, chunk pair).  For
+// a stream that re-bases this step, every retained key written before the
+// step (tokens evicted .. n_old - 1) becomes R(j - rope_base) applied to its
+// pre-RoPE copy: the exact result of rotating the previously stored key by
+// R(-delta), with one rounding however many re-bases the key has seen.
+__global__ void __launch_bounds__(256) rebase_kernel(DevView v, int layer0) {
+  const int d = v.head_dim, half = d / 2, cpairs = d / 16;
+  const int a = blockIdx.y;
+  const int lz = blockIdx.z;
   const StepDesc dsc = v.desc[a];
   if (dsc.delta == 0) return;
-  const int ps = v.page_size, d = v.head_dim, half = d / 2;
-  const int slot0 = ring_page * ps;
-  if (slot0 >= dsc.window) return;
-  const int n_slots = min(ps, dsc.window - slot0);
-  const int page = v.page_table[static_cast<int64_t>(dsc.stream) * v.max_pages + ring_page];
-  if (page < 0 || page >= v.n_pages) {
-    if (threadIdx.x == 0) record_error(v.status, DEV_BOUNDS, 3, page);
+  const int per_slot = v.n_kv_heads * cpairs;
+  const int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  const int slot = static_cast<int>(idx / per_slot);
+  if (slot >= dsc.window) return;
+  const int kvh = static_cast<int>((idx / cpairs) % v.n_kv_heads);
+  const int cp = static_cast<int>(idx % cpairs);
+  const int64_t tok = token_in_slot(slot, dsc.evicted, dsc.window);
+  if (tok >= dsc.n_old) return;  // a slot of this step's new tokens, or never written
+  const int64_t rel = tok - dsc.rope_base;
+  if (rel < 0 || rel >= v.t_rows) {
+    record_error(v.status, DEV_BOUNDS, 4, static_cast<int>(rel));
     return;
   }
-  const int64_t base = pool_offset(v, layer, page, kvh, 0);
-  for (int e = threadIdx.x; e < n_slots * half; e += blockDim.x) {
-    const int off = e / half, i = e % half;
-    const int64_t tok = token_in_slot(slot0 + off, dsc.evicted, dsc.window);
-    if (tok >= dsc.n_old) continue;  // a slot of this step's new tokens, or never written
-    const int64_t rel = tok - dsc.rope_base;
-    if (rel < 0 || rel >= v.t_rows) {
-      record_error(v.status, DEV_BOUNDS, 4, static_cast<int>(rel));
-      continue;
-    }
-    const float c = v.rope_table[(rel * half + i) * 2], s = v.rope_table[(rel * half + i) * 2 + 1];
-    const int64_t o = base + static_cast<int64_t>(off) * d;
-    const float xa = bf16_to_f32(v.k_raw[o + i]), xb = bf16_to_f32(v.k_raw[o + i + half]);
-    v.k_rot[o + i] = f32_to_f16(xa * c - xb * s);
-    v.k_rot[o + i + half] = f32_to_f16(xa * s + xb * c);
+  const int ring_page = slot / v.page_size;
+  const int page = v.page_table[static_cast<int64_t>(dsc.stream) * v.max_pages + ring_page];
+  if (page < 0 || page >= v.n_pages) {
+    record_error(v.status, DEV_BOUNDS, 3, page);
+    return;
   }
+  const int off = slot % v.page_size;
+  const int64_t base = pool_offset(v, layer0 + lz, page, kvh, off);
+  const int pa = swizzle_chunk(cp, off) * 8, pb = swizzle_chunk(cp + cpairs, off) * 8;
+  float xa[8], xb[8];
+  unpack8(*reinterpret_cast<const uint4*>(v.k_raw + base + pa), xa);
+  unpack8(*reinterpret_cast<const uint4*>(v.k_raw + base + pb), xb);
+  const float* cs = v.rope_table + (rel * half + cp * 8) * 2;
+  uint4 ya, yb;
+  bool fits;
+  rotate8(xa, xb, cs, &ya, &yb, &fits);
+  *reinterpret_cast<uint4*>(v.k_rot + base + pa) = ya;
+  *reinterpret_cast<uint4*>(v.k_rot + base + pb) = yb;
 }
 
 }  // namespace
 
-cudaError_t launch_append_rope(const DevView& v, int n_active, int layer, const uint16_t* k, const uint16_t* vv,
-                               cudaStream_t st) {
-  dim3 grid(n_active * v.q_per_step, (v.n_kv_heads + kWarps - 1) / kWarps);
-  append_rope_kernel<<<grid, kWarps * 32, 0, st>>>(v, layer, k, vv);
+cudaError_t launch_append_rope(const DevView& v, int n_active, int layer0, int n_layers, const uint16_t* k,
+                               const uint16_t* vv, int64_t kv_layer_stride, cudaStream_t st) {
+  const int n_rows = n_active * v.q_per_step;
+  const int64_t per_layer = static_cast<int64_t>(n_rows) * v.n_kv_heads * (v.head_dim / 16);
+  dim3 grid(static_cast<unsigned>((per_layer + 127) / 128), n_layers);
+  append_rope_kernel<<<grid, 128, 0, st>>>(v, layer0, n_rows, k, vv, kv_layer_stride);
   return cudaGetLastError();
 }
 
-cudaError_t launch_rebase(const DevView& v, int n_active, int layer, cudaStream_t st) {
-  dim3 grid(n_active, v.max_pages, v.n_kv_heads);
-  rebase_kernel<<<grid, 128, 0, st>>>(v, layer);
+cudaError_t launch_rebase(const DevView& v, int n_active, int layer0, int n_layers, cudaStream_t st) {
+  if (v.k_rot == nullptr) return cudaSuccess;  // rotate-on-read: nothing is stored re-based
+  const int64_t per_stream = static_cast<int64_t>(v.max_pages) * v.page_size * v.n_kv_heads * (v.head_dim / 16);
+  dim3 grid(static_cast<unsigned>((per_stream + 255) / 256), n_active, n_layers);
+  rebase_kernel<<<grid, 256, 0, st>>>(v, layer0);
   return cudaGetLastError();
 }
 

@@ -1,154 +1,713 @@
-// Windowed GQA attention over the ring (Audio8 ASR Infinite 无限长转写原理,
-// "Rolling KV Cache 三步拆解", 第 3 步: attention scans only the fixed window,
-// so the cost of a step is constant), split over the window's pages, then a
-// log-sum-exp merge of the splits.
+// Windowed GQA decode attention over the ring (Audio8 ASR Infinite
+// 无限长转写原理, "Rolling KV Cache 三步拆解", 第 3 步: attention scans only
+// the fixed window, so the cost of a step is constant).
 //
-// Split (stream a, kv head, split c) covers ring slots
-// [c * pages_per_split * page_size, ...) of stream a.  Slot order is not
-// token order, which softmax does not care about; a slot whose token is not
-// in [evicted, n_new) is empty.  Query token n_old + t attends key token j iff
-// j <= n_old + t (causal inside a multi-query step; every stored token is in
-// the window by construction of the ring).
+// One CTA streams the K/V pages of one (layer, stream, kv head), or of a
+// contiguous share of them (split-K), through shared memory and keeps an
+// online softmax for the kv head's G = Hq/Hkv query heads times the step's Q
+// queries (R = G*Q rows, at most 16).
 //
-// The step's queries arrive pre-RoPE (bf16) and are rotated here, in fp32,
-// with the cos/sin of their positions computed once per step; they are never
-// rounded back to a 16-bit format.  Keys are read as the stored fp16 rotated
-// keys, values as bf16.
+// Data movement.  A stage is 64 consecutive ring slots: K and V page blocks
+// (64 x d 16-bit values each, contiguous in the pool) land in shared memory
+// through bulk asynchronous copies (cp.async.bulk) issued by one producer
+// warp and completed on an mbarrier; three stages are in flight per CTA.
+// The pool's chunk swizzle (rkv_internal.cuh) makes the verbatim copies
+// conflict-free for ldmatrix.
 //
-// Partial results per (a, query row, split): m = max scaled score in log2
-// units, l = sum 2^(s - m), o = sum 2^(s - m) v / l.
+// Arithmetic.  Per warp, 16 keys at a time on the tensor cores (mma.sync
+// m16n8k16, fp32 accumulate), with keys as the M dimension so the query rows
+// fill N = 8 without padding:
+//   S^T[16 keys][8 rows] = K[16][d] . Qs^T, Qs = q rotated in fp32, times the
+//       softmax scale * log2(e), split into fp16 hi + lo parts (two MMAs), so
+//       the query adds no rounding of its own;
+//   P^T = exp2(S^T - m) (rows' running max m), rounded to bf16 and turned
+//       into the B operand by an 8x8 transpose (movmatrix);
+//   O^T[d][8 rows] += V^T[d][16 keys] . P^T  (V read with ldmatrix.trans).
+// Stored keys are fp16 (offset-only and exact re-base schemes).  In the
+// rotate-on-read scheme the pool holds pre-RoPE bf16 keys and every key is
+// rotated here by R(j - rope_base) in fp32 (cos/sin from the window-relative
+// table), then rounded once to fp16: the exact re-base with no stored copy.
+//
+// Splits of one (layer, stream, kv head) form a thread-block cluster and
+// combine their (m, l, O) through distributed shared memory; the scratch
+// form writes per-split partials to global memory for a separate merge.
+#include <cuda_bf16.h>
 #include <math_constants.h>
+
+#include <mutex>
 
 #include "rkv_internal.cuh"
 
 namespace rkv {
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kCW = 4;                    // consumer warps
+constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
+constexpr int kKS = 64;                   // ring slots per stage
+constexpr int kStages = 3;                // stages in flight per CTA
+constexpr unsigned long long kWaitNs = 1000000000ull;  // give up on a barrier after 1 s
 
-template <int D, int R>
-__global__ void __launch_bounds__(kWarps * 32) attn_partial_kernel(DevView v, int layer,
-                                                                   const uint16_t* __restrict__ q) {
-  constexpr int E = D / 32;  // elements of a head vector per lane
-  const int splits = v.splits;
-  const int a = blockIdx.x / splits, c = blockIdx.x % splits, kvh = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hq = v.n_q_heads, group = hq / v.n_kv_heads, nq = v.q_per_step;
-  const int rows = group * nq;
-  const StepDesc dsc = v.desc[a];
+struct AttnArgs {
+  DevView v;
+  const uint16_t* q;   // [layer][A][Q][Hq][d]
+  uint16_t* out;       // [layer][A][Q][Hq][d]
+  float* lse;          // [layer][A][Q][Hq] or NULL
+  int64_t q_layer_stride, lse_layer_stride;
+  int layer0, n_layers, n_active;
+  int splits, stages_per_split;
+  int mode;            // 0: whole windows; 1: split, cluster merge; 2: split, partials to part_ml / part_o
+};
 
-  __shared__ float qs[R][D];
-  __shared__ float red_ml[kWarps][R][2];
-  __shared__ float red_o[kWarps][R][D];
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
 
-  constexpr int H = D / 2;
-  for (int e = threadIdx.x; e < R * H; e += blockDim.x) {
-    const int r = e / H, i = e % H;
-    float ya = 0.f, yb = 0.f;
-    if (r < rows) {
-      const int t = r / group, h = kvh * group + r % group;
-      const uint16_t* x = q + ((static_cast<int64_t>(a) * nq + t) * hq + h) * D;
-      const float* cs = v.cs_new + ((static_cast<int64_t>(a) * nq + t) * H + i) * 2;
-      const float xa = bf16_to_f32(x[i]), xb = bf16_to_f32(x[i + H]);
-      ya = xa * cs[0] - xb * cs[1];
-      yb = xa * cs[1] + xb * cs[0];
-    }
-    qs[r][i] = ya;
-    qs[r][i + H] = yb;
-  }
-  __syncthreads();
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
 
-  float qreg[R][E], acc[R][E], m[R], l[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    m[r] = -CUDART_INF_F;
-    l[r] = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      qreg[r][e] = qs[r][lane * E + e];
-      acc[r][e] = 0.f;
-    }
-  }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
 
-  const int64_t n_new = dsc.n_old + nq;
-  const int span = v.pages_per_split * v.page_size;
-  const int s0 = c * span;
-  const int s1 = min(s0 + span, dsc.window);
-  for (int slot = s0 + warp; slot < s1; slot += kWarps) {
-    const int64_t tok = token_in_slot(slot, dsc.evicted, dsc.window);
-    if (tok >= n_new) continue;
-    const int page = v.page_table[static_cast<int64_t>(dsc.stream) * v.max_pages + slot / v.page_size];
-    if (page < 0 || page >= v.n_pages) {
-      if (lane == 0) record_error(v.status, DEV_BOUNDS, 5, page);
-      continue;
-    }
-    const int64_t off = pool_offset(v, layer, page, kvh, slot % v.page_size) + lane * E;
-    float kf[E], vf[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      kf[e] = f16_to_f32(v.k_rot[off + e]);
-      vf[e] = bf16_to_f32(v.v[off + e]);
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      if (r >= rows) break;
-      float dot = 0.f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) dot = fmaf(qreg[r][e], kf[e], dot);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-      if (tok > dsc.n_old + r / group) continue;  // causal inside the step
-      const float s2 = dot * v.scale_log2;
-      const float m_new = fmaxf(m[r], s2);
-      const float alpha = exp2f(m[r] - m_new);
-      const float p = exp2f(s2 - m_new);
-      l[r] = l[r] * alpha + p;
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[r][e] = fmaf(acc[r][e], alpha, p * vf[e]);
-      m[r] = m_new;
-    }
-  }
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
 
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    if (lane == 0) {
-      red_ml[warp][r][0] = m[r];
-      red_ml[warp][r][1] = l[r];
-    }
-#pragma unroll
-    for (int e = 0; e < E; ++e) red_o[warp][r][lane * E + e] = acc[r][e];
-  }
-  __syncthreads();
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 
-  const int qhq = nq * hq;
-  for (int e = threadIdx.x; e < rows * D; e += blockDim.x) {
-    const int r = e / D, i = e % D;
-    float mx = -CUDART_INF_F;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, red_ml[w][r][0]);
-    float lsum = 0.f, osum = 0.f;
-    if (mx != -CUDART_INF_F) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float f = exp2f(red_ml[w][r][0] - mx);
-        lsum += red_ml[w][r][1] * f;
-        osum += red_o[w][r][i] * f;
-      }
-    }
-    const int t = r / group, h = kvh * group + r % group;
-    const int64_t prow = (static_cast<int64_t>(a) * qhq + t * hq + h) * splits + c;
-    v.part_o[prow * D + i] = lsum > 0.f ? osum / lsum : 0.f;
-    if (i == 0) {
-      v.part_ml[prow * 2] = mx;
-      v.part_ml[prow * 2 + 1] = lsum;
-    }
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase with the given parity to complete; false after kWaitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_test(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_test(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitNs) return false;
   }
 }
 
-// One block per (active stream, query row): combine the splits.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "memory"); }
+
+// consumer_sync that also returns whether any consumer thread passed `pred`
+__device__ __forceinline__ bool consumer_sync_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred a, o;\n\tsetp.ne.u32 a, %1, 0;\n\t"
+      "bar.red.or.pred o, 1, %2, a;\n\tselp.u32 %0, 1, 0, o;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "n"(kCW * 32)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ float ld_dsmem_f32(const void* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  float x;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(x) : "r"(remote) : "memory");
+  return x;
+}
+
+// Rotate the pairs held by a (first half) and b (second half) of one key's
+// bf16 A-fragment registers: x = (lo, hi) at frequencies (i, i + 1).
+// cs = (cos_i, sin_i, cos_{i+1}, sin_{i+1}).  Results in fp16.
+__device__ __forceinline__ void rotate_pair_regs(uint32_t& a, uint32_t& b, const float4 cs) {
+  const float xa0 = __uint_as_float(a << 16), xa1 = __uint_as_float(a & 0xFFFF0000u);
+  const float xb0 = __uint_as_float(b << 16), xb1 = __uint_as_float(b & 0xFFFF0000u);
+  const float ya0 = xa0 * cs.x - xb0 * cs.y, yb0 = xa0 * cs.y + xb0 * cs.x;
+  const float ya1 = xa1 * cs.z - xb1 * cs.w, yb1 = xa1 * cs.w + xb1 * cs.z;
+  a = pack_f16(ya0, ya1);
+  b = pack_f16(yb0, yb1);
+}
+
+template <int D, int NT>
+constexpr int smem_bytes() {
+  // stages (K | V), query tiles hi + lo, fp32 output accumulator
+  return kStages * 2 * kKS * D * 2 + 2 * (8 * NT) * (D + 8) * 2 + (8 * NT) * (D + 4) * 4;
+}
+
+__device__ __forceinline__ void red_add_shared(float* p, float x) {
+  asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(smem_u32(p)), "f"(x) : "memory");
+}
+
+__device__ __forceinline__ float4 ld_dsmem_f32x4(const void* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  float4 x;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+               : "r"(remote)
+               : "memory");
+  return x;
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float (&x)[8]) {
+  return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+}
+
+// The unit (layer offset, active stream, kv head) of flat index u.
+struct Unit {
+  int lz, a, kvh;
+};
+__device__ __forceinline__ Unit unit_of(int u, int n_active, int hkv) {
+  Unit r;
+  const int per_layer = n_active * hkv;
+  r.lz = u / per_layer;
+  const int rem = u - r.lz * per_layer;
+  r.a = rem / hkv;
+  r.kvh = rem - r.a * hkv;
+  return r;
+}
+
+// Ring slots holding tokens: all W once anything was evicted, else 0 .. len-1.
+__device__ __forceinline__ int slots_in_use(const StepDesc& d) { return d.evicted > 0 ? d.window : d.len; }
+
+// Query prefetch of one consumer thread: pair cp of row r (chunks cp and cp + D/16).
 template <int D>
-__global__ void __launch_bounds__(128) merge_kernel(DevView v, uint16_t* __restrict__ out, float* __restrict__ lse) {
-  const int splits = v.splits;
+struct QPrefetch {
+  uint4 xa, xb;
+  float4 cs[4];
+};
+
+template <int D>
+__device__ __forceinline__ void q_prefetch(const AttnArgs& args, const Unit& un, int tid, QPrefetch<D>& pf) {
+  constexpr int CP = D / 16, H = D / 2;
+  const DevView& v = args.v;
+  const int r = tid / CP, cp = tid % CP;
+  const int group = v.n_q_heads / v.n_kv_heads, nq = v.q_per_step;
+  if (r < group * nq) {
+    const int t = r / group, h = un.kvh * group + r % group;
+    const uint16_t* x =
+        args.q + un.lz * args.q_layer_stride + ((static_cast<int64_t>(un.a) * nq + t) * v.n_q_heads + h) * D;
+    pf.xa = *reinterpret_cast<const uint4*>(x + cp * 8);
+    pf.xb = *reinterpret_cast<const uint4*>(x + H + cp * 8);
+    const float4* cs = reinterpret_cast<const float4*>(v.cs_new + ((static_cast<int64_t>(un.a) * nq + t) * H + cp * 8) * 2);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) pf.cs[j] = cs[j];
+  } else {
+    pf.xa = pf.xb = make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) pf.cs[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// Rotate, scale to log2 units and split into fp16 hi + lo; write the tiles.
+template <int D, int NT>
+__device__ __forceinline__ void q_build(const QPrefetch<D>& pf, float scale_log2, int tid, uint16_t* qh_s,
+                                        uint16_t* ql_s) {
+  constexpr int CP = D / 16, H = D / 2, QSTR = D + 8;
+  const int r = tid / CP, cp = tid % CP;
+  if (r >= 8 * NT) return;
+  const uint32_t wa[4] = {pf.xa.x, pf.xa.y, pf.xa.z, pf.xa.w}, wb[4] = {pf.xb.x, pf.xb.y, pf.xb.z, pf.xb.w};
+  const float* cs = reinterpret_cast<const float*>(pf.cs);
+  uint32_t ha[4], hb[4], la[4], lb[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float ya[2], yb[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float xa = __uint_as_float(e ? (wa[j] & 0xFFFF0000u) : (wa[j] << 16));
+      const float xb = __uint_as_float(e ? (wb[j] & 0xFFFF0000u) : (wb[j] << 16));
+      const float c = cs[4 * j + 2 * e], s = cs[4 * j + 2 * e + 1];
+      ya[e] = (xa * c - xb * s) * scale_log2;
+      yb[e] = (xa * s + xb * c) * scale_log2;
+    }
+    const __half2 hA = __floats2half2_rn(ya[0], ya[1]), hB = __floats2half2_rn(yb[0], yb[1]);
+    const float2 fA = __half22float2(hA), fB = __half22float2(hB);
+    ha[j] = *reinterpret_cast<const uint32_t*>(&hA);
+    hb[j] = *reinterpret_cast<const uint32_t*>(&hB);
+    la[j] = pack_f16(ya[0] - fA.x, ya[1] - fA.y);
+    lb[j] = pack_f16(yb[0] - fB.x, yb[1] - fB.y);
+  }
+  *reinterpret_cast<uint4*>(qh_s + r * QSTR + cp * 8) = make_uint4(ha[0], ha[1], ha[2], ha[3]);
+  *reinterpret_cast<uint4*>(qh_s + r * QSTR + H + cp * 8) = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+  *reinterpret_cast<uint4*>(ql_s + r * QSTR + cp * 8) = make_uint4(la[0], la[1], la[2], la[3]);
+  *reinterpret_cast<uint4*>(ql_s + r * QSTR + H + cp * 8) = make_uint4(lb[0], lb[1], lb[2], lb[3]);
+}
+
+// One CTA per SM slot.  Without a cluster the CTA walks units u = blockIdx.x,
+// blockIdx.x + gridDim.x, ... (whole windows, no split), its producer warp
+// streaming the next unit's pages while the consumers finish the current
+// one.  With a cluster (few units, window split over `splits` CTAs) every
+// CTA takes exactly one (unit, split).
+template <int D, int NT, bool ON_READ>
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const __grid_constant__ AttnArgs args) {
+  constexpr int KSTEPS = D / 16;  // k-steps of QK^T, m-tiles of PV
+  constexpr int QSTR = D + 8;     // padded fp16 row stride of the query tiles
+  constexpr int OSTR = D + 4;     // padded fp32 row stride of the output accumulator
+  constexpr int ROWS = 8 * NT;
+  constexpr int STAGE_ELEMS = kKS * D;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint16_t* kv_s = reinterpret_cast<uint16_t*>(smem);  // [stage][K | V][64][D]
+  uint16_t* qh_s = kv_s + kStages * 2 * STAGE_ELEMS;   // [ROWS][QSTR] fp16 hi
+  uint16_t* ql_s = qh_s + ROWS * QSTR;                 // [ROWS][QSTR] fp16 lo
+  float* obuf = reinterpret_cast<float*>(ql_s + ROWS * QSTR);  // [ROWS][OSTR] fp32
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
+  __shared__ float red_m[kCW][ROWS], red_l[kCW][ROWS];
+  __shared__ float row_m[ROWS], row_l[ROWS];
+  __shared__ int abort_flag, poisoned_s;
+
+  const DevView& v = args.v;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int splits = args.splits;
+  const int hkv = v.n_kv_heads, hq = v.n_q_heads, group = hq / hkv, nq = v.q_per_step;
+  const int rows = group * nq;
+  const int n_active = args.n_active;
+  const int n_units = n_active * hkv * args.n_layers;
+  // this CTA's units: [u_first, n_units) with stride u_step; one unit when split
+  const int split = splits > 1 ? static_cast<int>(blockIdx.x % splits) : 0;
+  const int u_first = splits > 1 ? static_cast<int>(blockIdx.x / splits) : static_cast<int>(blockIdx.x);
+  const int u_step = splits > 1 ? n_units : static_cast<int>(gridDim.x);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), kCW);
+    }
+    abort_flag = 0;
+    // after a timed-out wait anywhere, later launches skip their copies (the
+    // status word already reports the failure; each CTA ends quickly)
+    poisoned_s = *reinterpret_cast<volatile int32_t*>(v.status) == DEV_TIMEOUT;
+    asm volatile("fence.mbarrier_init.release.cluster;\n\tfence.proxy.async.shared::cta;" ::: "memory");
+  }
+  for (int e = threadIdx.x; e < ROWS * OSTR; e += kThreads) obuf[e] = 0.f;
+  __syncthreads();
+  const bool poisoned = poisoned_s != 0;
+
+  if (warp == kCW) {
+    // ---------------- producer: one lane issues the bulk copies of every stage of every unit
+    if (lane == 0 && !poisoned) {
+      const int ps = v.page_size;
+      const uint16_t* kreg = ON_READ ? v.k_raw : v.k_rot;
+      const int copies = ps >= kKS ? 1 : kKS / ps;
+      const int rows_per_copy = ps >= kKS ? kKS : ps;
+      const uint32_t bytes = static_cast<uint32_t>(rows_per_copy) * D * 2;
+      int k = 0;  // stages issued so far (ring position)
+      bool stop = false;
+      for (int u = u_first; u < n_units && !stop; u += u_step) {
+        const Unit un = unit_of(u, n_active, hkv);
+        const StepDesc dsc = v.desc[un.a];
+        const int layer = args.layer0 + un.lz;
+        const int n_st = (slots_in_use(dsc) + kKS - 1) / kKS;
+        const int st0 = split * args.stages_per_split;
+        const int st1 = min(st0 + args.stages_per_split, n_st);
+        const int stream_pages = (dsc.window + ps - 1) / ps;
+        const int32_t* ptab = v.page_table + static_cast<int64_t>(dsc.stream) * v.max_pages;
+        for (int st = st0; st < st1; ++st, ++k) {
+          const int buf = k % kStages;
+          if (k >= kStages && !mbar_wait(smem_u32(&empty_bar[buf]), ((k / kStages) - 1) & 1)) {
+            record_error(v.status, DEV_TIMEOUT, 20, k);
+            atomicExch(&abort_flag, 1);
+            stop = true;
+            break;
+          }
+          if (*reinterpret_cast<volatile int*>(&abort_flag)) {
+            stop = true;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full_bar[buf]);
+          mbar_arrive_expect_tx(fb, 2u * kKS * D * 2);
+          for (int c = 0; c < copies; ++c) {
+            const int slot = st * kKS + c * rows_per_copy;
+            int rp = slot / ps;
+            const int off = slot % ps;
+            if (rp >= stream_pages) rp = 0;  // past the window: any finite page (masked)
+            int page = ptab[rp];
+            if (page < 0 || page >= v.n_pages) {
+              record_error(v.status, DEV_BOUNDS, 21, page);
+              page = 0;
+            }
+            const int64_t src = pool_offset(v, layer, page, un.kvh, off);
+            const uint32_t dk = smem_u32(kv_s + buf * 2 * STAGE_ELEMS + c * rows_per_copy * D);
+            bulk_copy_g2s(dk, kreg + src, bytes, fb);
+            bulk_copy_g2s(dk + STAGE_ELEMS * 2, v.v + src, bytes, fb);
+          }
+        }
+      }
+      // never leave with copies in flight (only reachable on an aborted run)
+      for (int i = max(0, k - kStages); i < k; ++i)
+        if (!mbar_wait(smem_u32(&full_bar[i % kStages]), (i / kStages) & 1)) record_error(v.status, DEV_TIMEOUT, 22, i);
+    }
+  } else if (!poisoned) {
+    // ---------------- consumers
+    const int tid = threadIdx.x;
+    const int g = lane >> 2, tq = lane & 3;
+    // ldmatrix lane roles: matrix mi = lane / 8, row ri = lane % 8
+    const int mi = lane >> 3, ri = lane & 7;
+    const int krow = warp * 16 + ri + (mi & 1) * 8, kchunk = mi >> 1;  // K as the A operand
+    const int vrow = warp * 16 + ri + (mi >> 1) * 8, vchunk = mi & 1;  // V^T as the A operand
+    QPrefetch<D> pf;
+    if (u_first < n_units) q_prefetch<D>(args, unit_of(u_first, n_active, hkv), tid, pf);
+    int k = 0;  // stages consumed so far (ring position)
+    for (int u = u_first; u < n_units; u += u_step) {
+      const Unit un = unit_of(u, n_active, hkv);
+      const StepDesc dsc = v.desc[un.a];
+      const int W = dsc.window, len = dsc.len;
+      const int nslots = slots_in_use(dsc);
+      const int n_st = (nslots + kKS - 1) / kKS;
+      const int st0 = split * args.stages_per_split;
+      const int my_st = max(0, min(st0 + args.stages_per_split, n_st) - st0);
+
+      q_build<D, NT>(pf, v.scale_log2, tid, qh_s, ql_s);
+      consumer_sync();  // S1: query tiles ready; the previous unit's output pass is over
+      uint32_t qh[NT][KSTEPS][2], ql[NT][KSTEPS][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+          const int base = (nt * 8 + g) * QSTR + ks * 16 + 2 * tq;
+          qh[nt][ks][0] = *reinterpret_cast<const uint32_t*>(qh_s + base);
+          qh[nt][ks][1] = *reinterpret_cast<const uint32_t*>(qh_s + base + 8);
+          ql[nt][ks][0] = *reinterpret_cast<const uint32_t*>(ql_s + base);
+          ql[nt][ks][1] = *reinterpret_cast<const uint32_t*>(ql_s + base + 8);
+        }
+      if (u + u_step < n_units) q_prefetch<D>(args, unit_of(u + u_step, n_active, hkv), tid, pf);
+
+      float m_run[NT][2], l_run[NT][2], o_acc[KSTEPS][NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        m_run[nt][0] = m_run[nt][1] = -CUDART_INF_F;
+        l_run[nt][0] = l_run[nt][1] = 0.f;
+      }
+#pragma unroll
+      for (int mt = 0; mt < KSTEPS; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o_acc[mt][nt][e] = 0.f;
+
+      const int ev_mod = static_cast<int>(dsc.evicted % W);
+      const int first_new = len - nq;  // window index of the step's first new token
+      const int rel_shift = static_cast<int>(dsc.evicted - dsc.rope_base);
+      bool aborted = false;
+      for (int i = 0; i < my_st; ++i, ++k) {
+        const int buf = k % kStages;
+        // warp-uniform decision: every lane leaves together if any lane gave up
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[buf]), (k / kStages) & 1))) {
+          if (lane == 0) {
+            record_error(v.status, DEV_TIMEOUT, 23, k);
+            atomicExch(&abort_flag, 1);
+          }
+          aborted = true;
+          break;
+        }
+        const int slot_base = (st0 + i) * kKS + warp * 16;
+        if (slot_base < nslots) {
+          const uint32_t kb = smem_u32(kv_s + buf * 2 * STAGE_ELEMS);
+          const uint32_t vb = kb + STAGE_ELEMS * 2;
+          // window index (token - evicted) of this thread's two keys; -1 = empty slot
+          int widx[2];
+#pragma unroll
+          for (int hk = 0; hk < 2; ++hk) {
+            const int slot = slot_base + g + 8 * hk;
+            int w = slot - ev_mod;
+            if (w < 0) w += W;
+            widx[hk] = slot < nslots ? w : -1;
+          }
+          float sh[NT][4], sl[NT][4];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sh[nt][e] = sl[nt][e] = 0.f;
+          if constexpr (ON_READ) {
+            const float4* tab = reinterpret_cast<const float4*>(v.rope_table);
+            int rel[2];
+#pragma unroll
+            for (int hk = 0; hk < 2; ++hk) rel[hk] = widx[hk] < 0 ? 0 : min(widx[hk] + rel_shift, v.t_rows - 1);
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS / 2; ++ks) {
+              uint32_t fa[4], fb[4];
+              ldsm_x4(kb + krow * D * 2 + (swizzle_chunk(2 * ks + kchunk, ri) << 4), fa);
+              ldsm_x4(kb + krow * D * 2 + (swizzle_chunk(2 * (ks + KSTEPS / 2) + kchunk, ri) << 4), fb);
+              // this thread's frequencies: i0 = 16ks + 2tq (+1) and i0 + 8 (+1)
+              const int i0 = ks * 16 + 2 * tq;
+#pragma unroll
+              for (int hk = 0; hk < 2; ++hk) {
+                const float4 c0 = __ldg(tab + (static_cast<int64_t>(rel[hk]) * (D / 2) + i0) / 2);
+                const float4 c1 = __ldg(tab + (static_cast<int64_t>(rel[hk]) * (D / 2) + i0 + 8) / 2);
+                rotate_pair_regs(fa[hk], fb[hk], c0);          // a0/a1: dims i0, i0+1 of key g (+8)
+                rotate_pair_regs(fa[2 + hk], fb[2 + hk], c1);  // a2/a3: dims i0+8, i0+9
+              }
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                mma_f16(sh[nt], fa, qh[nt][ks][0], qh[nt][ks][1]);
+                mma_f16(sl[nt], fa, ql[nt][ks][0], ql[nt][ks][1]);
+                mma_f16(sh[nt], fb, qh[nt][ks + KSTEPS / 2][0], qh[nt][ks + KSTEPS / 2][1]);
+                mma_f16(sl[nt], fb, ql[nt][ks + KSTEPS / 2][0], ql[nt][ks + KSTEPS / 2][1]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+              uint32_t fa[4];
+              ldsm_x4(kb + krow * D * 2 + (swizzle_chunk(2 * ks + kchunk, ri) << 4), fa);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                mma_f16(sh[nt], fa, qh[nt][ks][0], qh[nt][ks][1]);
+                mma_f16(sl[nt], fa, ql[nt][ks][0], ql[nt][ks][1]);
+              }
+            }
+          }
+          // online softmax; C layout: e = 0,1 key g rows 2tq, 2tq+1; e = 2,3 key g+8
+          uint32_t pb[NT][2];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            float s[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int wi = widx[e >> 1];
+              const int row = nt * 8 + 2 * tq + (e & 1);
+              // causal inside the step: query t sees window index <= first_new + t
+              const bool ok = wi >= 0 && wi <= first_new + min(row / group, nq - 1);
+              s[e] = ok ? sh[nt][e] + sl[nt][e] : -CUDART_INF_F;
+            }
+            float p[4];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              float mx = fmaxf(s[c], s[c + 2]);
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+              const float m_new = fmaxf(m_run[nt][c], mx);
+              const float base = m_new == -CUDART_INF_F ? 0.f : m_new;
+              const float alpha = exp2f(m_run[nt][c] - base);
+              p[c] = exp2f(s[c] - base);
+              p[c + 2] = exp2f(s[c + 2] - base);
+              l_run[nt][c] = l_run[nt][c] * alpha + p[c] + p[c + 2];
+              m_run[nt][c] = m_new;
+#pragma unroll
+              for (int mt = 0; mt < KSTEPS; ++mt) {
+                o_acc[mt][nt][c] *= alpha;
+                o_acc[mt][nt][c + 2] *= alpha;
+              }
+            }
+            pb[nt][0] = movmatrix_t(pack_bf16(p[0], p[1]));
+            pb[nt][1] = movmatrix_t(pack_bf16(p[2], p[3]));
+          }
+#pragma unroll
+          for (int mt = 0; mt < KSTEPS; ++mt) {
+            uint32_t fv[4];
+            ldsm_x4_t(vb + vrow * D * 2 + (swizzle_chunk(2 * mt + vchunk, ri) << 4), fv);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_bf16(o_acc[mt][nt], fv, pb[nt][0], pb[nt][1]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty_bar[buf]));
+      }
+      // ---------------- combine the four warps: rescale in registers, add in shared memory
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float l = l_run[nt][c];
+          l += __shfl_xor_sync(0xffffffffu, l, 4);
+          l += __shfl_xor_sync(0xffffffffu, l, 8);
+          l += __shfl_xor_sync(0xffffffffu, l, 16);
+          l_run[nt][c] = l;
+          if (g == 0) {
+            red_m[warp][nt * 8 + 2 * tq + c] = m_run[nt][c];
+            red_l[warp][nt * 8 + 2 * tq + c] = l;
+          }
+        }
+      consumer_sync();  // S2
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int row = nt * 8 + 2 * tq + c;
+          float mx = -CUDART_INF_F;
+#pragma unroll
+          for (int w = 0; w < kCW; ++w) mx = fmaxf(mx, red_m[w][row]);
+          const float f = m_run[nt][c] == -CUDART_INF_F ? 0.f : exp2f(m_run[nt][c] - mx);
+          if (warp == 0 && g == 0) {
+            float lsum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kCW; ++w)
+              if (red_m[w][row] != -CUDART_INF_F) lsum += red_l[w][row] * exp2f(red_m[w][row] - mx);
+            row_m[row] = mx;
+            row_l[row] = lsum;
+          }
+#pragma unroll
+          for (int mt = 0; mt < KSTEPS; ++mt) {
+            red_add_shared(&obuf[row * OSTR + mt * 16 + g], o_acc[mt][nt][c] * f);
+            red_add_shared(&obuf[row * OSTR + mt * 16 + g + 8], o_acc[mt][nt][c + 2] * f);
+          }
+        }
+      // S3: obuf holds the CTA's unnormalised output, row_m / row_l its statistics; a wait that
+      // gave up in any warp ends the unit loop for all of them
+      if (consumer_sync_or(aborted)) break;
+
+      if (args.mode == 1) break;  // the cluster combine below finishes this (single) unit
+      // ---------------- output pass: thread -> (row, 8 consecutive dims)
+      constexpr int CH = D / 8;
+      for (int e = tid; e < rows * CH; e += kCW * 32) {
+        const int row = e / CH, ch = e % CH;
+        float* src = obuf + row * OSTR + ch * 8;
+        const float4 o0 = *reinterpret_cast<const float4*>(src), o1 = *reinterpret_cast<const float4*>(src + 4);
+        *reinterpret_cast<float4*>(src) = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(src + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float mx = row_m[row], lsum = row_l[row];
+        const int t = row / group, h = un.kvh * group + row % group;
+        const int64_t orow = (static_cast<int64_t>(un.a) * nq + t) * hq + h;
+        if (args.mode == 0) {
+          const float inv = 1.f / lsum;
+          const float o[8] = {o0.x * inv, o0.y * inv, o0.z * inv, o0.w * inv,
+                              o1.x * inv, o1.y * inv, o1.z * inv, o1.w * inv};
+          *reinterpret_cast<uint4*>(args.out + un.lz * args.q_layer_stride + orow * D + ch * 8) = pack8_bf16(o);
+          if (args.lse && ch == 0) args.lse[un.lz * args.lse_layer_stride + orow] = (mx + log2f(lsum)) * 0.69314718055994531f;
+        } else {  // mode 2: normalised partials of this split
+          const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+          const int64_t prow = orow * splits + split;
+          float4* dst = reinterpret_cast<float4*>(v.part_o + prow * D + ch * 8);
+          dst[0] = make_float4(o0.x * inv, o0.y * inv, o0.z * inv, o0.w * inv);
+          dst[1] = make_float4(o1.x * inv, o1.y * inv, o1.z * inv, o1.w * inv);
+          if (ch == 0) {
+            v.part_ml[prow * 2] = mx;
+            v.part_ml[prow * 2 + 1] = lsum;
+          }
+        }
+      }
+    }
+  }
+
+  if (args.mode == 1) {
+    // ---------------- combine the cluster's splits through distributed shared memory
+    __syncwarp();
+    cluster_sync_all();
+    const uint32_t rank = cluster_rank();
+    if (warp < kCW && !poisoned) {
+      const Unit un = unit_of(u_first, n_active, hkv);
+      constexpr int CH = D / 8;
+      for (int e = static_cast<int>(rank) * kCW * 32 + threadIdx.x; e < rows * CH; e += splits * kCW * 32) {
+        const int row = e / CH, ch = e % CH;
+        float mr[8], lr[8];
+        float mx = -CUDART_INF_F;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          if (r < splits) {
+            mr[r] = ld_dsmem_f32(&row_m[row], r);
+            lr[r] = ld_dsmem_f32(&row_l[row], r);
+          } else {
+            mr[r] = -CUDART_INF_F;
+            lr[r] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) mx = fmaxf(mx, mr[r]);
+        float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float lsum = 0.f;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          if (r < splits && mr[r] != -CUDART_INF_F) {
+            const float f = exp2f(mr[r] - mx);
+            const float4 a0 = ld_dsmem_f32x4(obuf + row * OSTR + ch * 8, r);
+            const float4 a1 = ld_dsmem_f32x4(obuf + row * OSTR + ch * 8 + 4, r);
+            lsum += lr[r] * f;
+            o[0] += a0.x * f;
+            o[1] += a0.y * f;
+            o[2] += a0.z * f;
+            o[3] += a0.w * f;
+            o[4] += a1.x * f;
+            o[5] += a1.y * f;
+            o[6] += a1.z * f;
+            o[7] += a1.w * f;
+          }
+        }
+        const float inv = 1.f / lsum;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[j] *= inv;
+        const int t = row / group, h = un.kvh * group + row % group;
+        const int64_t orow = (static_cast<int64_t>(un.a) * nq + t) * hq + h;
+        *reinterpret_cast<uint4*>(args.out + un.lz * args.q_layer_stride + orow * D + ch * 8) = pack8_bf16(o);
+        if (args.lse && ch == 0) args.lse[un.lz * args.lse_layer_stride + orow] = (mx + log2f(lsum)) * 0.69314718055994531f;
+      }
+    }
+    cluster_sync_all();  // keep this CTA's shared memory alive until every rank has read it
+  }
+}
+
+// One block per (active stream, query row): combine the splits' partials.
+template <int D>
+__global__ void __launch_bounds__(128) merge_kernel(DevView v, int splits, uint16_t* __restrict__ out,
+                                                    float* __restrict__ lse) {
   const int64_t prow0 = static_cast<int64_t>(blockIdx.x) * splits;
   const float* ml = v.part_ml + prow0 * 2;
   float mx = -CUDART_INF_F;
@@ -166,38 +725,136 @@ __global__ void __launch_bounds__(128) merge_kernel(DevView v, uint16_t* __restr
   if (lse && threadIdx.x == 0) lse[blockIdx.x] = (mx + log2f(lsum)) * 0.69314718055994531f;
 }
 
-template <int D, int R>
-cudaError_t launch_partial(const DevView& v, int n_active, int layer, const uint16_t* q, cudaStream_t st) {
-  dim3 grid(n_active * v.splits, v.n_kv_heads);
-  attn_partial_kernel<D, R><<<grid, kWarps * 32, 0, st>>>(v, layer, q);
-  return cudaGetLastError();
+template <int D, int NT, bool ON_READ>
+struct Kernel {
+  static int occupancy() {
+    static std::once_flag once;
+    static int occ = 0;
+    std::call_once(once, [] {
+      cudaFuncSetAttribute(attn_kernel<D, NT, ON_READ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem_bytes<D, NT>());
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_kernel<D, NT, ON_READ>, kThreads,
+                                                        smem_bytes<D, NT>()) != cudaSuccess)
+        occ = 1;
+      occ = occ < 1 ? 1 : occ;
+    });
+    return occ;
+  }
+  static cudaError_t launch(const AttnArgs& args, int grid, cudaStream_t st) {
+    occupancy();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes<D, NT>();
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    cfg.attrs = attr;
+    cfg.numAttrs = 0;
+    if (args.mode == 1) {
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = args.splits;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, attn_kernel<D, NT, ON_READ>, args);
+  }
+};
+
+template <int D, int NT>
+int occupancy_of(bool on_read) {
+  return on_read ? Kernel<D, NT, true>::occupancy() : Kernel<D, NT, false>::occupancy();
 }
 
-template <int D>
-cudaError_t launch_partial_d(const DevView& v, int n_active, int layer, const uint16_t* q, cudaStream_t st) {
-  const int rows = v.n_q_heads / v.n_kv_heads * v.q_per_step;
-  if (rows <= 1) return launch_partial<D, 1>(v, n_active, layer, q, st);
-  if (rows <= 2) return launch_partial<D, 2>(v, n_active, layer, q, st);
-  if (rows <= 4) return launch_partial<D, 4>(v, n_active, layer, q, st);
-  if (rows <= 8) return launch_partial<D, 8>(v, n_active, layer, q, st);
-  return launch_partial<D, 16>(v, n_active, layer, q, st);
+int occupancy_for(const DevView& v) {
+  const bool two = v.n_q_heads / v.n_kv_heads * v.q_per_step > 8;
+  const bool on_read = v.scheme == RKV_SCHEME_EXACT_ON_READ;
+  if (v.head_dim == 128) return two ? occupancy_of<128, 2>(on_read) : occupancy_of<128, 1>(on_read);
+  return two ? occupancy_of<64, 2>(on_read) : occupancy_of<64, 1>(on_read);
+}
+
+template <int D, int NT>
+cudaError_t dispatch_on_read(const AttnArgs& args, int grid, cudaStream_t st) {
+  if (args.v.scheme == RKV_SCHEME_EXACT_ON_READ) return Kernel<D, NT, true>::launch(args, grid, st);
+  return Kernel<D, NT, false>::launch(args, grid, st);
+}
+
+cudaError_t dispatch(const AttnArgs& args, int grid, cudaStream_t st) {
+  const DevView& v = args.v;
+  const bool two = v.n_q_heads / v.n_kv_heads * v.q_per_step > 8;
+  if (v.head_dim == 128) return two ? dispatch_on_read<128, 2>(args, grid, st) : dispatch_on_read<128, 1>(args, grid, st);
+  return two ? dispatch_on_read<64, 2>(args, grid, st) : dispatch_on_read<64, 1>(args, grid, st);
+}
+
+int64_t resident_ctas(const DevView& v) {
+  return static_cast<int64_t>(v.num_sms > 0 ? v.num_sms : 148) * occupancy_for(v);
+}
+
+AttnArgs make_args(const DevView& v, int n_active, int layer0, int n_layers, const uint16_t* q, uint16_t* out,
+                   float* lse, int64_t q_layer_stride, int64_t lse_layer_stride, const AttnPlan& p) {
+  AttnArgs args;
+  args.v = v;
+  args.q = q;
+  args.out = out;
+  args.lse = lse;
+  args.q_layer_stride = q_layer_stride;
+  args.lse_layer_stride = lse_layer_stride;
+  args.layer0 = layer0;
+  args.n_layers = n_layers;
+  args.n_active = n_active;
+  args.splits = p.splits;
+  args.stages_per_split = p.stages_per_split;
+  return args;
 }
 
 }  // namespace
 
-cudaError_t launch_decode_attn(const DevView& v, int n_active, int layer, const uint16_t* q, uint16_t* out,
-                               float* lse, cudaStream_t st) {
-  cudaError_t err;
+AttnPlan plan_decode_attn(const DevView& v, int n_active, int n_layers, bool cluster) {
+  // the page table bounds every stream's window by max_pages * page_size
+  const int max_stages = (v.max_pages * v.page_size + kKS - 1) / kKS;
+  const int64_t units = static_cast<int64_t>(n_active) * v.n_kv_heads * n_layers;
+  const int64_t resident = resident_ctas(v);
+  int splits = 1;
+  // fewer units than CTA slots: split every window over several CTAs
+  if (units < resident) splits = static_cast<int>(resident / units);
+  const int cap = cluster ? 8 : 64;
+  splits = splits > cap ? cap : splits;
+  splits = splits > max_stages ? max_stages : splits;
+  splits = splits < 1 ? 1 : splits;
+  const int sps = (max_stages + splits - 1) / splits;
+  splits = (max_stages + sps - 1) / sps;
+  AttnPlan p;
+  p.splits = splits;
+  p.stages_per_split = splits > 1 ? sps : max_stages;
+  p.cluster = cluster && splits > 1;
+  return p;
+}
+
+cudaError_t launch_decode_attn(const DevView& v, int n_active, int layer0, int n_layers, const uint16_t* q,
+                               uint16_t* out, float* lse, int64_t q_layer_stride, int64_t lse_layer_stride,
+                               cudaStream_t st) {
+  const AttnPlan p = plan_decode_attn(v, n_active, n_layers, true);
+  AttnArgs args = make_args(v, n_active, layer0, n_layers, q, out, lse, q_layer_stride, lse_layer_stride, p);
+  const int64_t units = static_cast<int64_t>(n_active) * v.n_kv_heads * n_layers;
+  args.mode = p.cluster ? 1 : 0;
+  const int64_t grid = p.cluster ? units * p.splits : (units < resident_ctas(v) ? units : resident_ctas(v));
+  return dispatch(args, static_cast<int>(grid), st);
+}
+
+cudaError_t launch_decode_attn_scratch(const DevView& v, int n_active, int layer, const uint16_t* q, uint16_t* out,
+                                       float* lse, cudaStream_t st) {
+  const AttnPlan p = plan_decode_attn(v, n_active, 1, false);
+  AttnArgs args = make_args(v, n_active, layer, 1, q, out, lse, 0, 0, p);
+  const int64_t units = static_cast<int64_t>(n_active) * v.n_kv_heads;
+  args.mode = p.splits > 1 ? 2 : 0;
+  const int64_t grid = p.splits > 1 ? units * p.splits : (units < resident_ctas(v) ? units : resident_ctas(v));
+  cudaError_t e = dispatch(args, static_cast<int>(grid), st);
+  if (e != cudaSuccess || p.splits == 1) return e;
   const int blocks = n_active * v.q_per_step * v.n_q_heads;
-  if (v.head_dim == 128) {
-    err = launch_partial_d<128>(v, n_active, layer, q, st);
-    if (err != cudaSuccess) return err;
-    merge_kernel<128><<<blocks, 128, 0, st>>>(v, out, lse);
-  } else {
-    err = launch_partial_d<64>(v, n_active, layer, q, st);
-    if (err != cudaSuccess) return err;
-    merge_kernel<64><<<blocks, 64, 0, st>>>(v, out, lse);
-  }
+  if (v.head_dim == 128)
+    merge_kernel<128><<<blocks, 128, 0, st>>>(v, p.splits, out, lse);
+  else
+    merge_kernel<64><<<blocks, 64, 0, st>>>(v, p.splits, out, lse);
   return cudaGetLastError();
 }
 

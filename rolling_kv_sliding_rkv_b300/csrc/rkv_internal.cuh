@@ -40,15 +40,28 @@ struct DevView {
   float* part_ml;        // [S][Q*Hq][splits][2] (running max in log2 units, sum)
   float* part_o;         // [S][Q*Hq][splits][d] normalised partial outputs
   int32_t* status;       // [4]: code, detail, detail2, unused
-  uint16_t* k_rot;       // pool: [L][n_pages][Hkv][ps][d] rotated keys, fp16 bits
+  uint16_t* k_rot;       // pool: [L][n_pages][Hkv][ps][d] rotated keys, fp16 bits (NULL: rotate-on-read scheme)
   uint16_t* v;           // pool: values (bf16 bits), same layout
-  uint16_t* k_raw;       // pool: pre-RoPE keys (bf16 bits, exact scheme), same layout
+  uint16_t* k_raw;       // pool: pre-RoPE keys (bf16 bits; exact schemes), same layout
   int64_t layer_stride;  // elements of one layer in one pool region
   int32_t n_streams, n_layers, n_q_heads, n_kv_heads, head_dim, q_per_step;
-  int32_t page_size, n_pages, max_pages, splits, pages_per_split, t_rows;
+  int32_t page_size, n_pages, max_pages, t_rows;
   int32_t scheme, rebase_interval;
+  int32_t num_sms;       // host-side launch planning only
   float scale_log2;      // softmax scale * log2(e)
 };
+
+// Both exact schemes keep window-relative key positions and a rope_base.
+__host__ __device__ __forceinline__ bool exact_scheme(int scheme) {
+  return scheme == RKV_SCHEME_EXACT_REBASE || scheme == RKV_SCHEME_EXACT_ON_READ;
+}
+
+// Pool rows are d 16-bit elements = d/8 chunks of 16 bytes.  Chunk c of the
+// row at offset `off` inside its page lives at chunk position c ^ (off & 7):
+// eight consecutive rows put any one chunk in eight different shared-memory
+// bank groups once a page is copied verbatim into shared memory, so 8x8
+// matrix loads (ldmatrix) of the page are conflict-free.
+__host__ __device__ __forceinline__ int swizzle_chunk(int chunk, int off) { return chunk ^ (off & 7); }
 
 struct Omegas {
   double w[64];  // omega_i = theta^(-2i/d), i < d/2, rounded to fp64 on the host
@@ -121,11 +134,28 @@ __device__ __forceinline__ int64_t pool_offset(const DevView& v, int layer, int 
 // ---- launchers (host functions, one translation unit each) ----
 cudaError_t launch_init_tables(const DevView& v, cudaStream_t st);
 cudaError_t launch_begin_step(const DevView& v, const ActiveIds& ids, cudaStream_t st);
-cudaError_t launch_append_rope(const DevView& v, int n_active, int layer, const uint16_t* k, const uint16_t* vv,
+// Layers [layer0, layer0 + n_layers) in one launch; per-layer tensors of the
+// step's inputs/outputs are `*_layer_stride` elements apart.
+cudaError_t launch_append_rope(const DevView& v, int n_active, int layer0, int n_layers, const uint16_t* k,
+                               const uint16_t* vv, int64_t kv_layer_stride, cudaStream_t st);
+cudaError_t launch_rebase(const DevView& v, int n_active, int layer0, int n_layers, cudaStream_t st);
+
+// How decode attention splits the window of one (layer, stream, kv head).
+struct AttnPlan {
+  int splits;            // CTAs per (layer, stream, kv head)
+  int stages_per_split;  // 64-slot stages each CTA streams
+  bool cluster;          // splits merged through distributed shared memory
+};
+// cluster = true: splits combine in distributed shared memory (no scratch);
+// false: every split writes (m, l, o) to part_ml / part_o and a merge kernel
+// combines them (single layer only).
+AttnPlan plan_decode_attn(const DevView& v, int n_active, int n_layers, bool cluster);
+cudaError_t launch_decode_attn(const DevView& v, int n_active, int layer0, int n_layers, const uint16_t* q,
+                               uint16_t* out, float* lse, int64_t q_layer_stride, int64_t lse_layer_stride,
                                cudaStream_t st);
-cudaError_t launch_rebase(const DevView& v, int n_active, int layer, cudaStream_t st);
-cudaError_t launch_decode_attn(const DevView& v, int n_active, int layer, const uint16_t* q, uint16_t* out,
-                               float* lse, cudaStream_t st);
+// the split-K form with partials in v.part_ml / v.part_o (one layer)
+cudaError_t launch_decode_attn_scratch(const DevView& v, int n_active, int layer, const uint16_t* q, uint16_t* out,
+                                       float* lse, cudaStream_t st);
 // decode attention with its split-K scratch in the library's fixed array (rkv_noalloc.cu)
 size_t static_scratch_floats();
 size_t static_scratch_need(const DevView& v, int n_active);

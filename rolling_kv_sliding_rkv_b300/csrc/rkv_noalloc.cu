@@ -43,9 +43,13 @@ cudaError_t scratch_address(float** out) {
   return cudaSuccess;
 }
 
+size_t partial_rows(const DevView& v, int n_active) {
+  const AttnPlan p = plan_decode_attn(v, n_active, 1, false);
+  return static_cast<size_t>(n_active) * v.q_per_step * v.n_q_heads * p.splits;
+}
+
 size_t ml_floats(const DevView& v, int n_active) {
-  const size_t rows = static_cast<size_t>(n_active) * v.q_per_step * v.n_q_heads * v.splits;
-  return (rows * 2 + 63) / 64 * 64;  // keeps the outputs that follow 256-byte aligned
+  return (partial_rows(v, n_active) * 2 + 63) / 64 * 64;  // keeps the outputs that follow 256-byte aligned
 }
 
 }  // namespace
@@ -53,8 +57,7 @@ size_t ml_floats(const DevView& v, int n_active) {
 size_t static_scratch_floats() { return kStaticScratchFloats; }
 
 size_t static_scratch_need(const DevView& v, int n_active) {
-  const size_t rows = static_cast<size_t>(n_active) * v.q_per_step * v.n_q_heads * v.splits;
-  return ml_floats(v, n_active) + rows * v.head_dim;
+  return ml_floats(v, n_active) + partial_rows(v, n_active) * v.head_dim;
 }
 
 cudaError_t launch_decode_attn_static(const DevView& v, int n_active, int layer, const uint16_t* q, uint16_t* out,
@@ -65,7 +68,7 @@ cudaError_t launch_decode_attn_static(const DevView& v, int n_active, int layer,
   DevView w = v;
   w.part_ml = base;
   w.part_o = base + ml_floats(v, n_active);
-  return launch_decode_attn(w, n_active, layer, q, out, lse, st);
+  return launch_decode_attn_scratch(w, n_active, layer, q, out, lse, st);
 }
 
 }  // namespace rkv

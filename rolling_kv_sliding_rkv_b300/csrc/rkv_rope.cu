@@ -54,7 +54,7 @@ __global__ void begin_step_kernel(DevView v, ActiveIds ids) {
     const int64_t len = n < w ? n : w;
     const int64_t ev = n - len;
     int64_t delta = 0;
-    if (v.scheme == RKV_SCHEME_EXACT_REBASE && ev - rope_base >= v.rebase_interval) {
+    if (exact_scheme(v.scheme) && ev - rope_base >= v.rebase_interval) {
       delta = ev - rope_base;
       rope_base = ev;
     }
@@ -75,7 +75,7 @@ __global__ void begin_step_kernel(DevView v, ActiveIds ids) {
     d.pad = 0;
     v.desc[a] = d;
     // the logical position P0 + j (offset-only), or j - rope_base (exact)
-    pos0 = v.scheme == RKV_SCHEME_EXACT_REBASE ? n_old - rope_base : p0 + n_old;
+    pos0 = exact_scheme(v.scheme) ? n_old - rope_base : p0 + n_old;
   }
   __syncthreads();
   const int half = v.head_dim / 2;

@@ -27,12 +27,14 @@ class Run:
     ring: dict = field(default_factory=dict)      # stream -> oracle StreamRing after the run
 
 
-def run_gpu(wl: synth.Workload, n_ticks: int, want: set, streams_of_interest=None, graph=False):
+def run_gpu(wl: synth.Workload, n_ticks: int, want: set, streams_of_interest=None, whole_step=False):
     """Run `n_ticks` steps (ticks for the mixed-clock workload) and copy sampled outputs.
 
     want: set of (stream, layer, n_old) to record, n_old = the stream's token
     count before the step.  A mixed-clock workload first brings every stream
     to its initial fill with extra steps of the lagging streams.
+    whole_step: drive rkv_step (all layers per launch) instead of the
+    per-layer calls; the inputs are the same generator draws.
     """
     import torch
 
@@ -44,19 +46,54 @@ def run_gpu(wl: synth.Workload, n_ticks: int, want: set, streams_of_interest=Non
     h = rkv.RollingKV(windows.tolist(), p0.tolist(), device=dev, n_layers=wl.n_layers, n_streams=wl.n_streams,
                       n_q_heads=wl.n_q_heads, n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim,
                       q_per_step=wl.q_per_step, scheme=wl.scheme, rebase_interval=wl.rebase_interval,
-                      rope_theta=wl.rope_theta)
+                      rope_theta=wl.rope_theta, page_size=int(wl.extra.get("page_size", 64)))
     S, L, Q, hq, hkv, d = wl.n_streams, wl.n_layers, wl.q_per_step, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
     q = torch.empty(S * Q * hq * d, dtype=torch.bfloat16, device=dev)
     k = torch.empty(S * Q * hkv * d, dtype=torch.bfloat16, device=dev)
     v = torch.empty_like(k)
     out = torch.empty_like(q)
     lse = torch.empty(S * Q * hq, dtype=torch.float32, device=dev)
-    rings = {s: StreamRing(int(windows[s]), int(p0[s]), Q, wl.scheme, wl.rebase_interval) for s in range(S)}
-    exact = wl.scheme == rkv.RKV_SCHEME_EXACT_REBASE
+    exact = wl.scheme in (rkv.RKV_SCHEME_EXACT_REBASE, rkv.RKV_SCHEME_EXACT_ON_READ)
+    # both exact schemes keep the same bookkeeping; they differ only in what the pool stores
+    ring_scheme = rkv.RKV_SCHEME_EXACT_REBASE if exact else rkv.RKV_SCHEME_OFFSET_ONLY
+    rings = {s: StreamRing(int(windows[s]), int(p0[s]), Q, ring_scheme, wl.rebase_interval) for s in range(S)}
     run = Run()
     want_streams = {s for s, _, _ in want}
+    if whole_step:
+        qa = torch.empty(L * S * Q * hq * d, dtype=torch.bfloat16, device=dev)
+        ka = torch.empty(L * S * Q * hkv * d, dtype=torch.bfloat16, device=dev)
+        va = torch.empty_like(ka)
+        outa = torch.empty_like(qa)
+        lsea = torch.empty(L * S * Q * hq, dtype=torch.float32, device=dev)
+
+    def record(active, n_old, layer, o_all, l_all):
+        a = len(active)
+        for idx, s in enumerate(active):
+            if s in want_streams and (s, layer, n_old[s]) in want:
+                o = o_all[: a * Q * hq * d].view(a, Q, hq, d)[idx].float().cpu().numpy()
+                lv = l_all[: a * Q * hq].view(a, Q, hq)[idx].cpu().numpy()
+                run.samples[(s, layer, n_old[s])] = (o, lv)
+
+    def one_whole_step(active):
+        a = len(active)
+        n_old = {s: rings[s].n for s in active}
+        for s in active:
+            rings[s].step()
+        nqe, nke = a * Q * hq * d, a * Q * hkv * d
+        for layer in range(L):
+            for idx, s in enumerate(active):
+                for tag, buf, width in ((synth.TAG_Q, qa, hq * d), (synth.TAG_K, ka, hkv * d),
+                                        (synth.TAG_V, va, hkv * d)):
+                    base = layer * (nqe if tag == synth.TAG_Q else nke) + idx * Q * width
+                    rkv.rkv_gen_tokens(wl.seed, tag, s, layer, n_old[s], Q, width, wl.input_scale,
+                                       buf[base:base + Q * width])
+        h.step(active, qa[: L * nqe], ka[: L * nke], va[: L * nke], outa[: L * nqe], lsea[: L * a * Q * hq])
+        for layer in range(L):
+            record(active, n_old, layer, outa[layer * nqe:], lsea[layer * a * Q * hq:])
 
     def one_step(active):
+        if whole_step:
+            return one_whole_step(active)
         a = len(active)
         h.begin_step(active)
         n_old = {s: rings[s].n for s in active}
@@ -68,11 +105,7 @@ def run_gpu(wl: synth.Workload, n_ticks: int, want: set, streams_of_interest=Non
                 h.rebase(layer)
             h.append_rope(layer, k, v)
             h.decode_attn(layer, q, out, lse)
-            for idx, s in enumerate(active):
-                if s in want_streams and (s, layer, n_old[s]) in want:
-                    o = out[: a * Q * hq * d].view(a, Q, hq, d)[idx].float().cpu().numpy()
-                    lv = lse[: a * Q * hq].view(a, Q, hq)[idx].cpu().numpy()
-                    run.samples[(s, layer, n_old[s])] = (o, lv)
+            record(active, n_old, layer, out, lse)
 
     # initial fill (ragged), one extra step at a time for the streams still short of it
     fill = wl.initial_fill()

@@ -22,12 +22,27 @@ SMALL = {
     "encoder_q4_exact": ("encoder", dict(n_layers=1, n_streams=2, extra={"window": 70}, scheme=1), 30),
     "qwen_scaled": ("qwen", dict(n_layers=2, n_streams=3, extra={"window": 100}), 120),
     "mixed_small": ("mixed", dict(n_layers=1, n_streams=9, extra={}), 60),
+    # exact re-base applied as attention reads the pre-RoPE keys (no stored re-based copy)
+    "tiny_on_read": ("tiny", dict(n_layers=2, n_streams=3, extra={"window": 150}, scheme=2), 190),
+    "tiny_on_read_interval5": ("tiny", dict(n_layers=1, n_streams=2, extra={"window": 150}, scheme=2,
+                                            rebase_interval=5), 190),
+    "encoder_q4_on_read": ("encoder", dict(n_layers=1, n_streams=2, extra={"window": 70}, scheme=2), 30),
+    "qwen_on_read_p0": ("qwen", dict(n_layers=2, n_streams=3, extra={"window": 100}, scheme=2), 120),
+    # the whole step (all layers per launch) through rkv_step
+    "qwen_whole_step": ("qwen", dict(n_layers=3, n_streams=3, extra={"window": 100}), 120, True),
+    "voxtral_whole_step": ("voxtral", dict(n_layers=2, n_streams=2, extra={"window": 130}), 150, True),
+    "encoder_whole_step": ("encoder", dict(n_layers=2, n_streams=2, extra={"window": 70}), 30, True),
+    "mixed_whole_step_on_read": ("mixed", dict(n_layers=2, n_streams=9, extra={}, scheme=2), 60, True),
+    # page sizes other than one stage (16 slots: four pages per stage; 128: half a page per stage)
+    "tiny_page16": ("tiny", dict(n_layers=1, n_streams=2, extra={"window": 150, "page_size": 16}), 190),
+    "tiny_page128_on_read": ("tiny", dict(n_layers=1, n_streams=2, extra={"window": 150, "page_size": 128},
+                                          scheme=2), 190),
 }
 
 
 @pytest.mark.parametrize("case", sorted(SMALL))
 def test_small_every_output(case):
-    name, over, ticks = SMALL[case]
+    name, over, ticks, *opt = SMALL[case]
     wl = synth.workload(name, **over)
     want = set()
     w = wl.windows()
@@ -39,7 +54,7 @@ def test_small_every_output(case):
         for layer in range(wl.n_layers):
             for n_old in range(int(fill[s]) * wl.q_per_step, int(counts[s]) * wl.q_per_step, wl.q_per_step):
                 want.add((s, layer, n_old))
-    run = run_gpu(wl, ticks, want)
+    run = run_gpu(wl, ticks, want, whole_step=bool(opt and opt[0]))
     assert len(run.samples) == len(want)
     e_o, e_l = compare(run, wl)
     print(case, "max out err", e_o, "max lse err", e_l)

@@ -65,13 +65,15 @@ def test_static_scratch_rejects_oversized_calls():
     import rolling_kv_sliding_rkv_b300 as rkv
 
     dev = torch.device("cuda")
-    # 4 streams x 16 query heads x 512 one-page splits x (128 + 2) floats is above 8 MiB
-    h = rkv.RollingKV([8192] * 4, [0] * 4, device=dev, n_layers=1, n_streams=4, n_q_heads=16, n_kv_heads=1,
+    # 1024 streams x 16 query heads x (128 + 2) floats of partials is above 8 MiB; with 1024
+    # (stream, kv head) units there are more than enough CTAs, so the window is never split
+    S = 1024
+    h = rkv.RollingKV([8] * S, [0] * S, device=dev, n_layers=1, n_streams=S, n_q_heads=16, n_kv_heads=1,
                       head_dim=128, q_per_step=1, scheme=0, page_size=16)
-    q = torch.zeros(4, 1, 16, 128, dtype=torch.bfloat16, device=dev)
-    k = torch.zeros(4, 1, 1, 128, dtype=torch.bfloat16, device=dev)
+    q = torch.zeros(S, 1, 16, 128, dtype=torch.bfloat16, device=dev)
+    k = torch.zeros(S, 1, 1, 128, dtype=torch.bfloat16, device=dev)
     out = torch.empty_like(q)
-    h.begin_step([0, 1, 2, 3])
+    h.begin_step(list(range(S)))
     h.append_rope(0, k, k)
     with pytest.raises(rkv.RkvError) as e:
         rkv.rkv_decode_attn_static(h.handle, 0, q, out)
