@@ -41,10 +41,12 @@
 namespace rkv {
 namespace {
 
-constexpr int kCW = 4;                    // consumer warps
+constexpr int kTeamWarps = 4;             // consumer warps per team: 16 slots of a stage each
+constexpr int kTeams = 1;                 // teams take alternate stages
+constexpr int kCW = kTeamWarps * kTeams;  // consumer warps
 constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
 constexpr int kKS = 64;                   // ring slots per stage
-constexpr int kStages = 3;                // stages in flight per CTA
+constexpr int kStages = 3;                // shared-memory ring per CTA (a multiple of kTeams)
 constexpr unsigned long long kWaitNs = 1000000000ull;  // give up on a barrier after 1 s
 
 struct AttnArgs {
@@ -107,6 +109,14 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
+}
+
+// 2^x with the hardware approximation (relative error about 2^-22; subnormal
+// results flush to zero, which softmax weights below 2^-126 can afford)
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -202,6 +212,8 @@ constexpr int smem_bytes() {
   // stages (K | V), query tiles hi + lo, fp32 output accumulator
   return kStages * 2 * kKS * D * 2 + 2 * (8 * NT) * (D + 8) * 2 + (8 * NT) * (D + 4) * 4;
 }
+static_assert(smem_bytes<128, 2>() <= 227 * 1024, "shared memory budget");
+static_assert(kStages % kTeams == 0, "a ring slot must always be consumed by the same team");
 
 __device__ __forceinline__ void red_add_shared(float* p, float x) {
   asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(smem_u32(p)), "f"(x) : "memory");
@@ -302,11 +314,17 @@ __device__ __forceinline__ void q_build(const QPrefetch<D>& pf, float scale_log2
   *reinterpret_cast<uint4*>(ql_s + r * QSTR + H + cp * 8) = make_uint4(lb[0], lb[1], lb[2], lb[3]);
 }
 
-// One CTA per SM slot.  Without a cluster the CTA walks units u = blockIdx.x,
+// Two CTAs per SM.  Without a cluster the CTA walks units u = blockIdx.x,
 // blockIdx.x + gridDim.x, ... (whole windows, no split), its producer warp
 // streaming the next unit's pages while the consumers finish the current
 // one.  With a cluster (few units, window split over `splits` CTAs) every
 // CTA takes exactly one (unit, split).
+//
+// Each of the four consumer warps takes 16 of a stage's 64 slots.  A warp
+// moves its K fragments into registers, runs QK^T, moves its V fragments
+// into registers and frees the ring slot before the softmax and PV, so the
+// slot refills while the warp computes.  (The team split generalises this
+// to teams of warps taking alternate stages; one team is used.)
 template <int D, int NT, bool ON_READ>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const __grid_constant__ AttnArgs args) {
   constexpr int KSTEPS = D / 16;  // k-steps of QK^T, m-tiles of PV
@@ -339,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
-      mbar_init(smem_u32(&empty_bar[s]), kCW);
+      mbar_init(smem_u32(&empty_bar[s]), kTeamWarps);
     }
     abort_flag = 0;
     // after a timed-out wait anywhere, later launches skip their copies (the
@@ -352,8 +370,10 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
   const bool poisoned = poisoned_s != 0;
 
   if (warp == kCW) {
-    // ---------------- producer: one lane issues the bulk copies of every stage of every unit
-    if (lane == 0 && !poisoned) {
+    // ---------------- producer: the warp walks every stage of every unit in the order the
+    // consumers take them; lane 0 issues the bulk copies, the lanes hold 32 page-table
+    // entries at a time, the next unit's descriptor is loaded a unit ahead
+    if (!poisoned) {
       const int ps = v.page_size;
       const uint16_t* kreg = ON_READ ? v.k_raw : v.k_rot;
       const int copies = ps >= kKS ? 1 : kKS / ps;
@@ -361,64 +381,85 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
       const uint32_t bytes = static_cast<uint32_t>(rows_per_copy) * D * 2;
       int k = 0;  // stages issued so far (ring position)
       bool stop = false;
+      StepDesc dnext;
+      if (u_first < n_units) dnext = v.desc[unit_of(u_first, n_active, hkv).a];
       for (int u = u_first; u < n_units && !stop; u += u_step) {
         const Unit un = unit_of(u, n_active, hkv);
-        const StepDesc dsc = v.desc[un.a];
+        const StepDesc dsc = dnext;
+        if (u + u_step < n_units) dnext = v.desc[unit_of(u + u_step, n_active, hkv).a];  // lands during this unit
         const int layer = args.layer0 + un.lz;
         const int n_st = (slots_in_use(dsc) + kKS - 1) / kKS;
         const int st0 = split * args.stages_per_split;
         const int st1 = min(st0 + args.stages_per_split, n_st);
         const int stream_pages = (dsc.window + ps - 1) / ps;
         const int32_t* ptab = v.page_table + static_cast<int64_t>(dsc.stream) * v.max_pages;
+        int pbase = -64, pt_lane = 0;
         for (int st = st0; st < st1; ++st, ++k) {
           const int buf = k % kStages;
-          if (k >= kStages && !mbar_wait(smem_u32(&empty_bar[buf]), ((k / kStages) - 1) & 1)) {
-            record_error(v.status, DEV_TIMEOUT, 20, k);
-            atomicExch(&abort_flag, 1);
+          if (k >= kStages &&
+              !__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty_bar[buf]), ((k / kStages) - 1) & 1))) {
+            if (lane == 0) {
+              record_error(v.status, DEV_TIMEOUT, 20, k);
+              atomicExch(&abort_flag, 1);
+            }
             stop = true;
             break;
           }
-          if (*reinterpret_cast<volatile int*>(&abort_flag)) {
+          if (__any_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&abort_flag) != 0)) {
             stop = true;
             break;
           }
           const uint32_t fb = smem_u32(&full_bar[buf]);
-          mbar_arrive_expect_tx(fb, 2u * kKS * D * 2);
+          if (lane == 0) mbar_arrive_expect_tx(fb, 2u * kKS * D * 2);
           for (int c = 0; c < copies; ++c) {
             const int slot = st * kKS + c * rows_per_copy;
             int rp = slot / ps;
             const int off = slot % ps;
             if (rp >= stream_pages) rp = 0;  // past the window: any finite page (masked)
-            int page = ptab[rp];
+            if (rp < pbase || rp >= pbase + 32) {  // warp-uniform: refill the lanes' page-table window
+              pbase = rp;
+              pt_lane = pbase + lane < v.max_pages ? ptab[pbase + lane] : 0;
+            }
+            int page = __shfl_sync(0xffffffffu, pt_lane, rp - pbase);
             if (page < 0 || page >= v.n_pages) {
-              record_error(v.status, DEV_BOUNDS, 21, page);
+              if (lane == 0) record_error(v.status, DEV_BOUNDS, 21, page);
               page = 0;
             }
-            const int64_t src = pool_offset(v, layer, page, un.kvh, off);
-            const uint32_t dk = smem_u32(kv_s + buf * 2 * STAGE_ELEMS + c * rows_per_copy * D);
-            bulk_copy_g2s(dk, kreg + src, bytes, fb);
-            bulk_copy_g2s(dk + STAGE_ELEMS * 2, v.v + src, bytes, fb);
+            if (lane == 0) {
+              const int64_t src = pool_offset(v, layer, page, un.kvh, off);
+              const uint32_t dk = smem_u32(kv_s + buf * 2 * STAGE_ELEMS + c * rows_per_copy * D);
+              bulk_copy_g2s(dk, kreg + src, bytes, fb);
+              bulk_copy_g2s(dk + STAGE_ELEMS * 2, v.v + src, bytes, fb);
+            }
           }
         }
       }
       // never leave with copies in flight (only reachable on an aborted run)
-      for (int i = max(0, k - kStages); i < k; ++i)
-        if (!mbar_wait(smem_u32(&full_bar[i % kStages]), (i / kStages) & 1)) record_error(v.status, DEV_TIMEOUT, 22, i);
+      if (lane == 0)
+        for (int i = max(0, k - kStages); i < k; ++i)
+          if (!mbar_wait(smem_u32(&full_bar[i % kStages]), (i / kStages) & 1))
+            record_error(v.status, DEV_TIMEOUT, 22, i);
     }
   } else if (!poisoned) {
     // ---------------- consumers
     const int tid = threadIdx.x;
+    const int team = warp / kTeamWarps, wt = warp % kTeamWarps;
     const int g = lane >> 2, tq = lane & 3;
     // ldmatrix lane roles: matrix mi = lane / 8, row ri = lane % 8
     const int mi = lane >> 3, ri = lane & 7;
-    const int krow = warp * 16 + ri + (mi & 1) * 8, kchunk = mi >> 1;  // K as the A operand
-    const int vrow = warp * 16 + ri + (mi >> 1) * 8, vchunk = mi & 1;  // V^T as the A operand
+    const int krow = wt * 16 + ri + (mi & 1) * 8, kchunk = mi >> 1;  // K as the A operand
+    const int vrow = wt * 16 + ri + (mi >> 1) * 8, vchunk = mi & 1;  // V^T as the A operand
     QPrefetch<D> pf;
-    if (u_first < n_units) q_prefetch<D>(args, unit_of(u_first, n_active, hkv), tid, pf);
-    int k = 0;  // stages consumed so far (ring position)
+    StepDesc dnext;
+    if (u_first < n_units) {
+      const Unit un0 = unit_of(u_first, n_active, hkv);
+      q_prefetch<D>(args, un0, tid, pf);
+      dnext = v.desc[un0.a];
+    }
+    int k0 = 0;  // ring position of the unit's first stage
     for (int u = u_first; u < n_units; u += u_step) {
       const Unit un = unit_of(u, n_active, hkv);
-      const StepDesc dsc = v.desc[un.a];
+      const StepDesc dsc = dnext;
       const int W = dsc.window, len = dsc.len;
       const int nslots = slots_in_use(dsc);
       const int n_st = (nslots + kKS - 1) / kKS;
@@ -438,7 +479,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
           ql[nt][ks][0] = *reinterpret_cast<const uint32_t*>(ql_s + base);
           ql[nt][ks][1] = *reinterpret_cast<const uint32_t*>(ql_s + base + 8);
         }
-      if (u + u_step < n_units) q_prefetch<D>(args, unit_of(u + u_step, n_active, hkv), tid, pf);
+      if (u + u_step < n_units) {  // the next unit's query and descriptor land during this unit
+        const Unit un1 = unit_of(u + u_step, n_active, hkv);
+        q_prefetch<D>(args, un1, tid, pf);
+        dnext = v.desc[un1.a];
+      }
 
       float m_run[NT][2], l_run[NT][2], o_acc[KSTEPS][NT][4];
 #pragma unroll
@@ -457,7 +502,9 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
       const int first_new = len - nq;  // window index of the step's first new token
       const int rel_shift = static_cast<int>(dsc.evicted - dsc.rope_base);
       bool aborted = false;
-      for (int i = 0; i < my_st; ++i, ++k) {
+      // this team's stages of the unit: ring positions k0 + i with (k0 + i) % kTeams == team
+      for (int i = (team - k0 % kTeams + kTeams) % kTeams; i < my_st; i += kTeams) {
+        const int k = k0 + i;
         const int buf = k % kStages;
         // warp-uniform decision: every lane leaves together if any lane gave up
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[buf]), (k / kStages) & 1))) {
@@ -468,111 +515,121 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
           aborted = true;
           break;
         }
-        const int slot_base = (st0 + i) * kKS + warp * 16;
-        if (slot_base < nslots) {
-          const uint32_t kb = smem_u32(kv_s + buf * 2 * STAGE_ELEMS);
-          const uint32_t vb = kb + STAGE_ELEMS * 2;
-          // window index (token - evicted) of this thread's two keys; -1 = empty slot
-          int widx[2];
+        const int slot_base = (st0 + i) * kKS + wt * 16;
+        const uint32_t kb = smem_u32(kv_s + buf * 2 * STAGE_ELEMS);
+        const uint32_t vb = kb + STAGE_ELEMS * 2;
+        if (slot_base >= nslots) {  // none of this warp's slots holds a token
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&empty_bar[buf]));
+          continue;
+        }
+        // window index (token - evicted) of this thread's two keys; -1 = empty slot
+        int widx[2];
 #pragma unroll
-          for (int hk = 0; hk < 2; ++hk) {
-            const int slot = slot_base + g + 8 * hk;
-            int w = slot - ev_mod;
-            if (w < 0) w += W;
-            widx[hk] = slot < nslots ? w : -1;
-          }
-          float sh[NT][4], sl[NT][4];
+        for (int hk = 0; hk < 2; ++hk) {
+          const int slot = slot_base + g + 8 * hk;
+          int w = slot - ev_mod;
+          if (w < 0) w += W;
+          widx[hk] = slot < nslots ? w : -1;
+        }
+        // K fragments of this warp's 16 slots (the A operand, one per k-step)
+        uint32_t kf[KSTEPS][4];
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
+        for (int ks = 0; ks < KSTEPS; ++ks) ldsm_x4(kb + krow * D * 2 + (swizzle_chunk(2 * ks + kchunk, ri) << 4), kf[ks]);
+        if constexpr (ON_READ) {
+          // rotate each pre-RoPE key by its window-relative position: pairs (i, i + d/2) sit in
+          // k-steps ks and ks + d/32 at the same register positions
+          const float4* tab = reinterpret_cast<const float4*>(v.rope_table);
+          int rel[2];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sh[nt][e] = sl[nt][e] = 0.f;
-          if constexpr (ON_READ) {
-            const float4* tab = reinterpret_cast<const float4*>(v.rope_table);
-            int rel[2];
+          for (int hk = 0; hk < 2; ++hk) rel[hk] = widx[hk] < 0 ? 0 : min(widx[hk] + rel_shift, v.t_rows - 1);
 #pragma unroll
-            for (int hk = 0; hk < 2; ++hk) rel[hk] = widx[hk] < 0 ? 0 : min(widx[hk] + rel_shift, v.t_rows - 1);
+          for (int ks = 0; ks < KSTEPS / 2; ++ks) {
+            const int i0 = ks * 16 + 2 * tq;  // this thread's frequencies i0, i0+1 and i0+8, i0+9
 #pragma unroll
-            for (int ks = 0; ks < KSTEPS / 2; ++ks) {
-              uint32_t fa[4], fb[4];
-              ldsm_x4(kb + krow * D * 2 + (swizzle_chunk(2 * ks + kchunk, ri) << 4), fa);
-              ldsm_x4(kb + krow * D * 2 + (swizzle_chunk(2 * (ks + KSTEPS / 2) + kchunk, ri) << 4), fb);
-              // this thread's frequencies: i0 = 16ks + 2tq (+1) and i0 + 8 (+1)
-              const int i0 = ks * 16 + 2 * tq;
-#pragma unroll
-              for (int hk = 0; hk < 2; ++hk) {
-                const float4 c0 = __ldg(tab + (static_cast<int64_t>(rel[hk]) * (D / 2) + i0) / 2);
-                const float4 c1 = __ldg(tab + (static_cast<int64_t>(rel[hk]) * (D / 2) + i0 + 8) / 2);
-                rotate_pair_regs(fa[hk], fb[hk], c0);          // a0/a1: dims i0, i0+1 of key g (+8)
-                rotate_pair_regs(fa[2 + hk], fb[2 + hk], c1);  // a2/a3: dims i0+8, i0+9
-              }
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                mma_f16(sh[nt], fa, qh[nt][ks][0], qh[nt][ks][1]);
-                mma_f16(sl[nt], fa, ql[nt][ks][0], ql[nt][ks][1]);
-                mma_f16(sh[nt], fb, qh[nt][ks + KSTEPS / 2][0], qh[nt][ks + KSTEPS / 2][1]);
-                mma_f16(sl[nt], fb, ql[nt][ks + KSTEPS / 2][0], ql[nt][ks + KSTEPS / 2][1]);
-              }
+            for (int hk = 0; hk < 2; ++hk) {
+              const float4 c0 = __ldg(tab + (static_cast<int64_t>(rel[hk]) * (D / 2) + i0) / 2);
+              const float4 c1 = __ldg(tab + (static_cast<int64_t>(rel[hk]) * (D / 2) + i0 + 8) / 2);
+              rotate_pair_regs(kf[ks][hk], kf[ks + KSTEPS / 2][hk], c0);
+              rotate_pair_regs(kf[ks][2 + hk], kf[ks + KSTEPS / 2][2 + hk], c1);
             }
-          } else {
-#pragma unroll
-            for (int ks = 0; ks < KSTEPS; ++ks) {
-              uint32_t fa[4];
-              ldsm_x4(kb + krow * D * 2 + (swizzle_chunk(2 * ks + kchunk, ri) << 4), fa);
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                mma_f16(sh[nt], fa, qh[nt][ks][0], qh[nt][ks][1]);
-                mma_f16(sl[nt], fa, ql[nt][ks][0], ql[nt][ks][1]);
-              }
-            }
-          }
-          // online softmax; C layout: e = 0,1 key g rows 2tq, 2tq+1; e = 2,3 key g+8
-          uint32_t pb[NT][2];
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            float s[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int wi = widx[e >> 1];
-              const int row = nt * 8 + 2 * tq + (e & 1);
-              // causal inside the step: query t sees window index <= first_new + t
-              const bool ok = wi >= 0 && wi <= first_new + min(row / group, nq - 1);
-              s[e] = ok ? sh[nt][e] + sl[nt][e] : -CUDART_INF_F;
-            }
-            float p[4];
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              float mx = fmaxf(s[c], s[c + 2]);
-              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-              const float m_new = fmaxf(m_run[nt][c], mx);
-              const float base = m_new == -CUDART_INF_F ? 0.f : m_new;
-              const float alpha = exp2f(m_run[nt][c] - base);
-              p[c] = exp2f(s[c] - base);
-              p[c + 2] = exp2f(s[c + 2] - base);
-              l_run[nt][c] = l_run[nt][c] * alpha + p[c] + p[c + 2];
-              m_run[nt][c] = m_new;
-#pragma unroll
-              for (int mt = 0; mt < KSTEPS; ++mt) {
-                o_acc[mt][nt][c] *= alpha;
-                o_acc[mt][nt][c + 2] *= alpha;
-              }
-            }
-            pb[nt][0] = movmatrix_t(pack_bf16(p[0], p[1]));
-            pb[nt][1] = movmatrix_t(pack_bf16(p[2], p[3]));
-          }
-#pragma unroll
-          for (int mt = 0; mt < KSTEPS; ++mt) {
-            uint32_t fv[4];
-            ldsm_x4_t(vb + vrow * D * 2 + (swizzle_chunk(2 * mt + vchunk, ri) << 4), fv);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_bf16(o_acc[mt][nt], fv, pb[nt][0], pb[nt][1]);
           }
         }
+        float sh[NT][4], sl[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sh[nt][e] = sl[nt][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_f16(sh[nt], kf[ks], qh[nt][ks][0], qh[nt][ks][1]);
+            mma_f16(sl[nt], kf[ks], ql[nt][ks][0], ql[nt][ks][1]);
+          }
+        // V fragments (V^T as the A operand, one per m-tile), then the slot refills while we compute
+        uint32_t vf[KSTEPS][4];
+#pragma unroll
+        for (int mt = 0; mt < KSTEPS; ++mt) ldsm_x4_t(vb + vrow * D * 2 + (swizzle_chunk(2 * mt + vchunk, ri) << 4), vf[mt]);
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty_bar[buf]));
+        // online softmax; C layout: e = 0,1 key g rows 2tq, 2tq+1; e = 2,3 key g+8.  A chunk
+        // of a one-query step whose slots all hold tokens needs no mask.
+        const bool full_chunk = nq == 1 && slot_base + 16 <= nslots;
+        uint32_t pb[NT][2];
+        float alpha[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float s[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int wi = widx[e >> 1];
+            const int row = nt * 8 + 2 * tq + (e & 1);
+            // causal inside the step: query t sees window index <= first_new + t
+            const bool ok = full_chunk || (wi >= 0 && wi <= first_new + min(row / group, nq - 1));
+            s[e] = ok ? sh[nt][e] + sl[nt][e] : -CUDART_INF_F;
+          }
+          float p[4];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            float mx = fmaxf(s[c], s[c + 2]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float m_new = fmaxf(m_run[nt][c], mx);
+            const float base = m_new == -CUDART_INF_F ? 0.f : m_new;
+            alpha[nt][c] = fast_exp2(m_run[nt][c] - base);
+            p[c] = fast_exp2(s[c] - base);
+            p[c + 2] = fast_exp2(s[c + 2] - base);
+            l_run[nt][c] = l_run[nt][c] * alpha[nt][c] + p[c] + p[c + 2];
+            m_run[nt][c] = m_new;
+          }
+          pb[nt][0] = movmatrix_t(pack_bf16(p[0], p[1]));
+          pb[nt][1] = movmatrix_t(pack_bf16(p[2], p[3]));
+        }
+        // rescale the accumulators only when some row's running max moved in this warp
+        bool moved = false;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) moved = moved || alpha[nt][0] != 1.f || alpha[nt][1] != 1.f;
+        if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+          for (int mt = 0; mt < KSTEPS; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              o_acc[mt][nt][0] *= alpha[nt][0];
+              o_acc[mt][nt][1] *= alpha[nt][1];
+              o_acc[mt][nt][2] *= alpha[nt][0];
+              o_acc[mt][nt][3] *= alpha[nt][1];
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < KSTEPS; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16(o_acc[mt][nt], vf[mt], pb[nt][0], pb[nt][1]);
       }
-      // ---------------- combine the four warps: rescale in registers, add in shared memory
+      k0 += my_st;
+
+      // ---------------- combine the warps: rescale in registers, add in shared memory
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -605,10 +662,12 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
             row_m[row] = mx;
             row_l[row] = lsum;
           }
+          if (f != 0.f) {
 #pragma unroll
-          for (int mt = 0; mt < KSTEPS; ++mt) {
-            red_add_shared(&obuf[row * OSTR + mt * 16 + g], o_acc[mt][nt][c] * f);
-            red_add_shared(&obuf[row * OSTR + mt * 16 + g + 8], o_acc[mt][nt][c + 2] * f);
+            for (int mt = 0; mt < KSTEPS; ++mt) {
+              red_add_shared(&obuf[row * OSTR + mt * 16 + g], o_acc[mt][nt][c] * f);
+              red_add_shared(&obuf[row * OSTR + mt * 16 + g + 8], o_acc[mt][nt][c + 2] * f);
+            }
           }
         }
       // S3: obuf holds the CTA's unnormalised output, row_m / row_l its statistics; a wait that
@@ -632,7 +691,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
           const float o[8] = {o0.x * inv, o0.y * inv, o0.z * inv, o0.w * inv,
                               o1.x * inv, o1.y * inv, o1.z * inv, o1.w * inv};
           *reinterpret_cast<uint4*>(args.out + un.lz * args.q_layer_stride + orow * D + ch * 8) = pack8_bf16(o);
-          if (args.lse && ch == 0) args.lse[un.lz * args.lse_layer_stride + orow] = (mx + log2f(lsum)) * 0.69314718055994531f;
+          if (args.lse && ch == 0)
+            args.lse[un.lz * args.lse_layer_stride + orow] = (mx + log2f(lsum)) * 0.69314718055994531f;
         } else {  // mode 2: normalised partials of this split
           const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
           const int64_t prow = orow * splits + split;
