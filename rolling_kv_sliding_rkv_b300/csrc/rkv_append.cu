@@ -106,48 +106,79 @@ __global__ void __launch_bounds__(128) append_rope_kernel(DevView v, int layer0,
   }
 }
 
-// One thread per (layer, active stream, ring slot, kv head, chunk pair).  For
-// a stream that re-bases this step, every retained key written before the
-// step (tokens evicted .. n_old - 1) becomes R(j - rope_base) applied to its
-// pre-RoPE copy: the exact result of rotating the previously stored key by
-// R(-delta), with one rounding however many re-bases the key has seen.
-__global__ void __launch_bounds__(256) rebase_kernel(DevView v, int layer0) {
+// Work items are (ring slot, kv head, chunk pair) of one stream and layer; a
+// thread takes kRebaseItems of them, 256 apart, and issues all their loads
+// (keys and cos/sin rows) before any arithmetic, so enough bytes are in
+// flight to cover HBM latency.
+// For a stream that re-bases this step, every retained key written before
+// the step (tokens evicted .. n_old - 1) becomes R(j - rope_base) applied to
+// its pre-RoPE copy: the exact result of rotating the previously stored key
+// by R(-delta), with one rounding however many re-bases the key has seen.
+constexpr int kRebaseThreads = 256;
+constexpr int kRebaseItems = 2;
+
+__global__ void __launch_bounds__(kRebaseThreads) rebase_kernel(DevView v, int layer0) {
   const int d = v.head_dim, half = d / 2, cpairs = d / 16;
   const int a = blockIdx.y;
   const int lz = blockIdx.z;
   const StepDesc dsc = v.desc[a];
   if (dsc.delta == 0) return;
   const int per_slot = v.n_kv_heads * cpairs;
-  const int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-  const int slot = static_cast<int>(idx / per_slot);
-  if (slot >= dsc.window) return;
-  const int kvh = static_cast<int>((idx / cpairs) % v.n_kv_heads);
-  const int cp = static_cast<int>(idx % cpairs);
-  const int64_t tok = token_in_slot(slot, dsc.evicted, dsc.window);
-  if (tok >= dsc.n_old) return;  // a slot of this step's new tokens, or never written
-  const int64_t rel = tok - dsc.rope_base;
-  if (rel < 0 || rel >= v.t_rows) {
-    record_error(v.status, DEV_BOUNDS, 4, static_cast<int>(rel));
-    return;
+  const int ev_mod = static_cast<int>(dsc.evicted % dsc.window);
+  const int old_len = static_cast<int>(dsc.n_old - dsc.evicted);  // window index of the first new token
+  const int rel_shift = static_cast<int>(dsc.evicted - dsc.rope_base);
+  const int32_t* ptab = v.page_table + static_cast<int64_t>(dsc.stream) * v.max_pages;
+  const int64_t item0 = static_cast<int64_t>(blockIdx.x) * kRebaseThreads * kRebaseItems + threadIdx.x;
+  uint4 ka[kRebaseItems], kb[kRebaseItems];
+  int64_t dst[kRebaseItems];
+  int rel[kRebaseItems], pa[kRebaseItems], pb[kRebaseItems];
+  bool live[kRebaseItems];
+  float4 tb[kRebaseItems][4];
+#pragma unroll
+  for (int j = 0; j < kRebaseItems; ++j) {
+    const int64_t item = item0 + j * kRebaseThreads;
+    const int slot = static_cast<int>(item / per_slot);
+    const int kvh = static_cast<int>((item / cpairs) % v.n_kv_heads);
+    const int cp = static_cast<int>(item % cpairs);
+    int w = slot - ev_mod;  // window index of the slot's token
+    if (w < 0) w += dsc.window;
+    live[j] = slot < dsc.window && w < old_len;  // retained tokens from before this step
+    rel[j] = w + rel_shift;
+    dst[j] = 0;
+    if (live[j] && (rel[j] < 0 || rel[j] >= v.t_rows)) {
+      record_error(v.status, DEV_BOUNDS, 4, rel[j]);
+      live[j] = false;
+    }
+    if (live[j]) {
+      const int page = ptab[slot / v.page_size];
+      if (page < 0 || page >= v.n_pages) {
+        record_error(v.status, DEV_BOUNDS, 3, page);
+        live[j] = false;
+      } else {
+        const int off = slot % v.page_size;
+        dst[j] = pool_offset(v, layer0 + lz, page, kvh, off);
+        pa[j] = swizzle_chunk(cp, off) * 8;
+        pb[j] = swizzle_chunk(cp + cpairs, off) * 8;
+        ka[j] = *reinterpret_cast<const uint4*>(v.k_raw + dst[j] + pa[j]);
+        kb[j] = *reinterpret_cast<const uint4*>(v.k_raw + dst[j] + pb[j]);
+        const float4* t4 = reinterpret_cast<const float4*>(v.rope_table + (static_cast<int64_t>(rel[j]) * half + cp * 8) * 2);
+        tb[j][0] = t4[0]; tb[j][1] = t4[1]; tb[j][2] = t4[2]; tb[j][3] = t4[3];
+      }
+    }
   }
-  const int ring_page = slot / v.page_size;
-  const int page = v.page_table[static_cast<int64_t>(dsc.stream) * v.max_pages + ring_page];
-  if (page < 0 || page >= v.n_pages) {
-    record_error(v.status, DEV_BOUNDS, 3, page);
-    return;
+#pragma unroll
+  for (int j = 0; j < kRebaseItems; ++j) {
+    if (!live[j]) continue;
+    float xa[8], xb[8];
+    unpack8(ka[j], xa);
+    unpack8(kb[j], xb);
+    const float* cs = reinterpret_cast<const float*>(tb[j]);
+    uint4 ya, yb;
+    bool fits;
+    rotate8(xa, xb, cs, &ya, &yb, &fits);
+    *reinterpret_cast<uint4*>(v.k_rot + dst[j] + pa[j]) = ya;
+    *reinterpret_cast<uint4*>(v.k_rot + dst[j] + pb[j]) = yb;
   }
-  const int off = slot % v.page_size;
-  const int64_t base = pool_offset(v, layer0 + lz, page, kvh, off);
-  const int pa = swizzle_chunk(cp, off) * 8, pb = swizzle_chunk(cp + cpairs, off) * 8;
-  float xa[8], xb[8];
-  unpack8(*reinterpret_cast<const uint4*>(v.k_raw + base + pa), xa);
-  unpack8(*reinterpret_cast<const uint4*>(v.k_raw + base + pb), xb);
-  const float* cs = v.rope_table + (rel * half + cp * 8) * 2;
-  uint4 ya, yb;
-  bool fits;
-  rotate8(xa, xb, cs, &ya, &yb, &fits);
-  *reinterpret_cast<uint4*>(v.k_rot + base + pa) = ya;
-  *reinterpret_cast<uint4*>(v.k_rot + base + pb) = yb;
 }
 
 }  // namespace
@@ -164,8 +195,9 @@ cudaError_t launch_append_rope(const DevView& v, int n_active, int layer0, int n
 cudaError_t launch_rebase(const DevView& v, int n_active, int layer0, int n_layers, cudaStream_t st) {
   if (v.k_rot == nullptr) return cudaSuccess;  // rotate-on-read: nothing is stored re-based
   const int64_t per_stream = static_cast<int64_t>(v.max_pages) * v.page_size * v.n_kv_heads * (v.head_dim / 16);
-  dim3 grid(static_cast<unsigned>((per_stream + 255) / 256), n_active, n_layers);
-  rebase_kernel<<<grid, 256, 0, st>>>(v, layer0);
+  const int64_t per_block = static_cast<int64_t>(kRebaseThreads) * kRebaseItems;
+  dim3 grid(static_cast<unsigned>((per_stream + per_block - 1) / per_block), n_active, n_layers);
+  rebase_kernel<<<grid, kRebaseThreads, 0, st>>>(v, layer0);
   return cudaGetLastError();
 }
 
