@@ -46,7 +46,11 @@ constexpr int kTeams = 1;                 // teams take alternate stages
 constexpr int kCW = kTeamWarps * kTeams;  // consumer warps
 constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
 constexpr int kKS = 64;                   // ring slots per stage
-constexpr int kStages = 3;                // shared-memory ring per CTA (a multiple of kTeams)
+// shared-memory ring per CTA: 96 KB of K/V stages whatever the head dim (a multiple of kTeams)
+template <int D>
+__host__ __device__ constexpr int stages_for() {
+  return 3 * 128 / D;
+}
 constexpr unsigned long long kWaitNs = 1000000000ull;  // give up on a barrier after 1 s
 
 struct AttnArgs {
@@ -208,12 +212,13 @@ __device__ __forceinline__ void rotate_pair_regs(uint32_t& a, uint32_t& b, const
 }
 
 template <int D, int NT>
-constexpr int smem_bytes() {
+__host__ __device__ constexpr int smem_bytes() {
   // stages (K | V), query tiles hi + lo, fp32 output accumulator
-  return kStages * 2 * kKS * D * 2 + 2 * (8 * NT) * (D + 8) * 2 + (8 * NT) * (D + 4) * 4;
+  return stages_for<D>() * 2 * kKS * D * 2 + 2 * (8 * NT) * (D + 8) * 2 + (8 * NT) * (D + 4) * 4;
 }
 static_assert(smem_bytes<128, 2>() <= 227 * 1024, "shared memory budget");
-static_assert(kStages % kTeams == 0, "a ring slot must always be consumed by the same team");
+static_assert(stages_for<128>() % kTeams == 0 && stages_for<64>() % kTeams == 0,
+              "a ring slot must always be consumed by the same team");
 
 __device__ __forceinline__ void red_add_shared(float* p, float x) {
   asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(smem_u32(p)), "f"(x) : "memory");
@@ -332,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
   constexpr int OSTR = D + 4;     // padded fp32 row stride of the output accumulator
   constexpr int ROWS = 8 * NT;
   constexpr int STAGE_ELEMS = kKS * D;
+  constexpr int kStages = stages_for<D>();
   extern __shared__ __align__(1024) uint8_t smem[];
   uint16_t* kv_s = reinterpret_cast<uint16_t*>(smem);  // [stage][K | V][64][D]
   uint16_t* qh_s = kv_s + kStages * 2 * STAGE_ELEMS;   // [ROWS][QSTR] fp16 hi
@@ -574,8 +580,9 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty_bar[buf]));
         // online softmax; C layout: e = 0,1 key g rows 2tq, 2tq+1; e = 2,3 key g+8.  A chunk
-        // of a one-query step whose slots all hold tokens needs no mask.
-        const bool full_chunk = nq == 1 && slot_base + 16 <= nslots;
+        // whose slots all hold tokens that every query of the step sees needs no mask.
+        const bool full_chunk = slot_base + 16 <= nslots &&
+                                (nq == 1 || __all_sync(0xffffffffu, widx[0] <= first_new && widx[1] <= first_new));
         uint32_t pb[NT][2];
         float alpha[NT][2];
 #pragma unroll
