@@ -33,6 +33,12 @@ if ROOT not in sys.path:
 METRIC = "stream-steps/sec (all layers) and decode-attn HBM GB/s as % of B300 peak"
 UNIT = "stream-steps/s"
 SCHEMES = {"offset": 0, "exact": 1, "on-read": 2}
+
+# DRAM traffic (read + write bytes) of one decode-attention launch, from the ncu launch list
+# committed under profiles/ (launch_list_qwen36x64_exact.md), valid only while the attention
+# kernel's source is the one that was profiled: a different source hash reports null.
+TRAFFIC = [{"workload": "qwen", "layers": 36, "schemes": (0, 1), "attn_src_sha256_16": "8e4363ef3d23e54e",
+            "bytes_per_launch": 915.6e6 + 9.0e6}]
 SCHEME_NAMES = {0: "offset-only", 1: "exact re-base", 2: "exact re-base applied on read"}
 
 
@@ -122,6 +128,22 @@ class ClockSampler:
                 "sm_max_mhz": max(float(r[2]) for r in rows),
                 "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit()) if rows else None,
                 "reasons": reasons, "samples": len(rows)}
+
+
+def profiled_traffic(wl):
+    """ncu DRAM bytes per attention launch for this workload, or None (not profiled / kernel changed)."""
+    import hashlib
+    src = os.path.join(ROOT, "rolling_kv_sliding_rkv_b300", "csrc", "rkv_attn.cu")
+    try:
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    for t in TRAFFIC:
+        if (t["workload"] == wl.name and t["layers"] == wl.n_layers and wl.scheme in t["schemes"]
+                and t["attn_src_sha256_16"] == sha):
+            return t["bytes_per_launch"]
+    return None
 
 
 def measured_peak():
@@ -432,7 +454,7 @@ def run_ours(args):
                            "graph": "one CUDA graph per step (per tick phase for mixed clocks), replayed",
                            "parallelism": "replicas" if world == 1 else f"replicas x{world}"},
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                             "frac": achieved / peak, "traffic": None,
+                             "frac": achieved / peak, "traffic": profiled_traffic(wl),
                              "kernel": f"attn_kernel: decode attention over all {wl.n_layers} layers in one "
                                        "launch (as inside the timed step)",
                              "algorithmic_bytes_per_launch": m["attn_bytes"],
