@@ -57,6 +57,8 @@ def parse_args():
     p.add_argument("--layers", type=int, default=None, help="override the workload's layer count (profiling cases)")
     p.add_argument("--no-variants", dest="variants", action="store_false",
                    help="skip timing the workload under the other two schemes")
+    p.add_argument("--no-flatness", dest="flatness", action="store_false",
+                   help="skip the per-step time at five start offsets (Qwen-shaped workload)")
     return p.parse_args()
 
 
@@ -245,8 +247,10 @@ def step_phases(wl):
     return [wl.active_at_tick(t).tolist() for t in range(period)]
 
 
-def measure(wl, args, dev, rank, world, timed=True):
-    """Time the step of workload `wl` on this GPU; returns the figures of one JSON line."""
+def measure(wl, args, dev, rank, world, timed=True, p0=None, attention=True):
+    """Time the step of workload `wl` on this GPU; returns the figures of one JSON line.
+
+    p0: start offset given to every stream (default: the workload's draws)."""
     import torch
 
     import rolling_kv_sliding_rkv_b300 as rkv
@@ -254,7 +258,8 @@ def measure(wl, args, dev, rank, world, timed=True):
 
     S, L, Q, hq, hkv, d = wl.n_streams, wl.n_layers, wl.q_per_step, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
     windows = wl.windows()
-    h = rkv.RollingKV(windows.tolist(), wl.start_offsets().tolist(), device=dev, n_layers=L, n_streams=S,
+    starts = wl.start_offsets().tolist() if p0 is None else [int(p0)] * S
+    h = rkv.RollingKV(windows.tolist(), starts, device=dev, n_layers=L, n_streams=S,
                       n_q_heads=hq, n_kv_heads=hkv, head_dim=d, q_per_step=Q, scheme=wl.scheme,
                       rebase_interval=wl.rebase_interval, rope_theta=wl.rope_theta)
     phases = [ph for ph in step_phases(wl)]
@@ -305,6 +310,7 @@ def measure(wl, args, dev, rank, world, timed=True):
             graphs[i % R].replay()
     torch.cuda.synchronize()
     h.sync_status()
+    free_before = torch.cuda.mem_get_info(dev)[0]
 
     cur = torch.cuda.current_stream()
 
@@ -345,7 +351,10 @@ def measure(wl, args, dev, rank, world, timed=True):
     h.sync_status()
     stream_steps = sum(len(plan[i % R]) for i in range(args.steps))
     out.update(value=world * stream_steps / (ms / 1000.0), ms=ms, stream_steps=stream_steps,
-               launches=launches_per_step * sum(1 for i in range(args.steps) if graphs[i % R] is not None))
+               launches=launches_per_step * sum(1 for i in range(args.steps) if graphs[i % R] is not None),
+               free_bytes_delta=torch.cuda.mem_get_info(dev)[0] - free_before)
+    if not attention:
+        return out
 
     # decode attention alone: the all-layers launch the step makes (the dominant kernel), and,
     # for reference, per-layer launches as a model that interleaves other work would make them;
@@ -437,6 +446,18 @@ def run_ours(args):
                 "decode_attn_gbs": vm["attn_bytes"] / (vm["attn_all_ms"] / 1000.0) / 1e9,
                 "decode_attn_frac": vm["attn_bytes"] / (vm["attn_all_ms"] / 1000.0) / 1e9 / peak}
 
+    flat = None
+    if args.flatness and rank == 0 and wl.name == "qwen" and not args.layers:
+        # cost per step must not depend on how far the streams are into their logical timelines
+        offsets = [0, 540_000, 1_080_000, 2_000_000, 2 ** 31 + 5]
+        per = []
+        for p0 in offsets:
+            fm = measure(wl, args, dev, rank, 1, timed=False, p0=p0, attention=False)
+            fm.pop("h").close()
+            per.append(fm["ms"] / args.steps)
+        flat = {"p0": offsets, "ms_per_step": per, "spread": max(per) / min(per) - 1.0,
+                "free_bytes_delta_over_timed_steps": m["free_bytes_delta"]}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = oracle_timing(wl, args.cpu_seconds)
@@ -469,6 +490,8 @@ def run_ours(args):
                 "clocks": m["clocks"]}
         if variants:
             line["schemes"] = variants
+        if flat is not None:
+            line["flatness"] = flat
         if e2e is not None:
             line["e2e"] = e2e
         if cpu is not None:

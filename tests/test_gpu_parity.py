@@ -37,6 +37,20 @@ SMALL = {
     "tiny_page16": ("tiny", dict(n_layers=1, n_streams=2, extra={"window": 150, "page_size": 16}), 190),
     "tiny_page128_on_read": ("tiny", dict(n_layers=1, n_streams=2, extra={"window": 150, "page_size": 128},
                                           scheme=2), 190),
+    "tiny_page32": ("tiny", dict(n_layers=1, n_streams=2, extra={"window": 100, "page_size": 32}, scheme=0), 130),
+    # 16 query rows per kv head: GQA group 16, and group 4 with 4 queries per step
+    "gqa16_exact": ("tiny", dict(n_layers=1, n_streams=2, n_q_heads=16, n_kv_heads=1, extra={"window": 150}),
+                    190),
+    "gqa16_on_read": ("tiny", dict(n_layers=1, n_streams=2, n_q_heads=16, n_kv_heads=1, extra={"window": 150},
+                                   scheme=2), 190),
+    "gqa4_q4_d64": ("encoder", dict(n_layers=1, n_streams=2, n_q_heads=8, n_kv_heads=2, extra={"window": 90}), 40),
+    "gqa4_q4_d64_on_read": ("encoder", dict(n_layers=1, n_streams=2, n_q_heads=8, n_kv_heads=2,
+                                            extra={"window": 90}, scheme=2), 40),
+    "gqa16_whole_step": ("tiny", dict(n_layers=2, n_streams=3, n_q_heads=16, n_kv_heads=1, extra={"window": 150}),
+                         170, True),
+    # head_dim 64 with GQA, one query per step
+    "d64_gqa4": ("tiny", dict(n_layers=1, n_streams=2, n_q_heads=8, n_kv_heads=2, head_dim=64,
+                              extra={"window": 150}), 190),
 }
 
 
