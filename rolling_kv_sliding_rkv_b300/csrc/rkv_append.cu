@@ -106,78 +106,98 @@ __global__ void __launch_bounds__(128) append_rope_kernel(DevView v, int layer0,
   }
 }
 
-// Work items are (ring slot, kv head, chunk pair) of one stream and layer; a
-// thread takes kRebaseItems of them, 256 apart, and issues all their loads
-// (keys and cos/sin rows) before any arithmetic, so enough bytes are in
-// flight to cover HBM latency.
-// For a stream that re-bases this step, every retained key written before
-// the step (tokens evicted .. n_old - 1) becomes R(j - rope_base) applied to
-// its pre-RoPE copy: the exact result of rotating the previously stored key
-// by R(-delta), with one rounding however many re-bases the key has seen.
-constexpr int kRebaseThreads = 256;
-constexpr int kRebaseItems = 2;
+// A thread re-bases one chunk pair (elements 8c .. 8c+7 and their partners
+// + d/2) of one kv head for a run of kRebaseRun consecutive ring slots of one
+// stream and layer.  Consecutive slots hold consecutive window positions
+// (except where the ring wraps), so the cos/sin of the next slot's angles
+// follow from the current ones by one complex multiplication with
+// (cos, sin)(omega_i); the table row is read only for the run's first slot
+// and after a wrap (at most 8 multiplications: ~1e-6 relative, far below the
+// fp16 rounding of the result).  All of the run's key loads are issued before
+// any arithmetic.  For a stream that re-bases this step, every retained key
+// written before the step (tokens evicted .. n_old - 1) becomes
+// R(j - rope_base) applied to its pre-RoPE copy: the exact result of rotating
+// the previously stored key by R(-delta), with one rounding however many
+// re-bases the key has seen.
+constexpr int kRebaseThreads = 128;
+constexpr int kRebaseRun = 8;  // divides every page size (16 .. 128)
 
-__global__ void __launch_bounds__(kRebaseThreads) rebase_kernel(DevView v, int layer0) {
+__global__ void __launch_bounds__(kRebaseThreads, 3) rebase_kernel(DevView v, int layer0) {
   const int d = v.head_dim, half = d / 2, cpairs = d / 16;
   const int a = blockIdx.y;
   const int lz = blockIdx.z;
   const StepDesc dsc = v.desc[a];
   if (dsc.delta == 0) return;
-  const int per_slot = v.n_kv_heads * cpairs;
-  const int ev_mod = static_cast<int>(dsc.evicted % dsc.window);
+  const int item = blockIdx.x * kRebaseThreads + threadIdx.x;
+  const int cp = item % cpairs;
+  const int kvh = (item / cpairs) % v.n_kv_heads;
+  const int slot0 = (item / (cpairs * v.n_kv_heads)) * kRebaseRun;
+  const int W = dsc.window;
+  if (slot0 >= W) return;
+  const int ev_mod = static_cast<int>(dsc.evicted % W);
   const int old_len = static_cast<int>(dsc.n_old - dsc.evicted);  // window index of the first new token
   const int rel_shift = static_cast<int>(dsc.evicted - dsc.rope_base);
-  const int32_t* ptab = v.page_table + static_cast<int64_t>(dsc.stream) * v.max_pages;
-  const int64_t item0 = static_cast<int64_t>(blockIdx.x) * kRebaseThreads * kRebaseItems + threadIdx.x;
-  uint4 ka[kRebaseItems], kb[kRebaseItems];
-  int64_t dst[kRebaseItems];
-  int rel[kRebaseItems], pa[kRebaseItems], pb[kRebaseItems];
-  bool live[kRebaseItems];
-  float4 tb[kRebaseItems][4];
+  const int page = v.page_table[static_cast<int64_t>(dsc.stream) * v.max_pages + slot0 / v.page_size];
+  if (page < 0 || page >= v.n_pages) {
+    record_error(v.status, DEV_BOUNDS, 3, page);
+    return;
+  }
+  const int64_t row0 = pool_offset(v, layer0 + lz, page, kvh, slot0 % v.page_size);
+  uint4 ka[kRebaseRun], kb[kRebaseRun];
+  int rel[kRebaseRun];
+  bool live[kRebaseRun];
 #pragma unroll
-  for (int j = 0; j < kRebaseItems; ++j) {
-    const int64_t item = item0 + j * kRebaseThreads;
-    const int slot = static_cast<int>(item / per_slot);
-    const int kvh = static_cast<int>((item / cpairs) % v.n_kv_heads);
-    const int cp = static_cast<int>(item % cpairs);
+  for (int j = 0; j < kRebaseRun; ++j) {
+    const int slot = slot0 + j;
     int w = slot - ev_mod;  // window index of the slot's token
-    if (w < 0) w += dsc.window;
-    live[j] = slot < dsc.window && w < old_len;  // retained tokens from before this step
+    if (w < 0) w += W;
+    live[j] = slot < W && w < old_len;  // retained tokens from before this step
     rel[j] = w + rel_shift;
-    dst[j] = 0;
     if (live[j] && (rel[j] < 0 || rel[j] >= v.t_rows)) {
       record_error(v.status, DEV_BOUNDS, 4, rel[j]);
       live[j] = false;
     }
     if (live[j]) {
-      const int page = ptab[slot / v.page_size];
-      if (page < 0 || page >= v.n_pages) {
-        record_error(v.status, DEV_BOUNDS, 3, page);
-        live[j] = false;
-      } else {
-        const int off = slot % v.page_size;
-        dst[j] = pool_offset(v, layer0 + lz, page, kvh, off);
-        pa[j] = swizzle_chunk(cp, off) * 8;
-        pb[j] = swizzle_chunk(cp + cpairs, off) * 8;
-        ka[j] = *reinterpret_cast<const uint4*>(v.k_raw + dst[j] + pa[j]);
-        kb[j] = *reinterpret_cast<const uint4*>(v.k_raw + dst[j] + pb[j]);
-        const float4* t4 = reinterpret_cast<const float4*>(v.rope_table + (static_cast<int64_t>(rel[j]) * half + cp * 8) * 2);
-        tb[j][0] = t4[0]; tb[j][1] = t4[1]; tb[j][2] = t4[2]; tb[j][3] = t4[3];
-      }
+      const int off = (slot0 + j) % v.page_size;
+      const int64_t o = row0 + static_cast<int64_t>(j) * d;
+      ka[j] = *reinterpret_cast<const uint4*>(v.k_raw + o + swizzle_chunk(cp, off) * 8);
+      kb[j] = *reinterpret_cast<const uint4*>(v.k_raw + o + swizzle_chunk(cp + cpairs, off) * 8);
     }
   }
+  // (cos, sin)(omega_i) of this thread's eight frequencies: table row 1
+  float step[16], cs[16];
+  if (v.t_rows > 1) {  // (a window of one key keeps nothing to re-base)
+    const float4* t1 = reinterpret_cast<const float4*>(v.rope_table + (static_cast<int64_t>(1) * half + cp * 8) * 2);
 #pragma unroll
-  for (int j = 0; j < kRebaseItems; ++j) {
+    for (int q = 0; q < 4; ++q) reinterpret_cast<float4*>(step)[q] = t1[q];
+  }
+  int rel_cur = -2;
+#pragma unroll
+  for (int j = 0; j < kRebaseRun; ++j) {
     if (!live[j]) continue;
+    if (rel[j] == rel_cur + 1) {  // advance by one position: (c, s) <- (c, s) * (cos, sin)(omega)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float c = cs[2 * i], s = cs[2 * i + 1], c1 = step[2 * i], s1 = step[2 * i + 1];
+        cs[2 * i] = c * c1 - s * s1;
+        cs[2 * i + 1] = s * c1 + c * s1;
+      }
+    } else {  // first live slot of the run, or the ring wrapped: read the row
+      const float4* t = reinterpret_cast<const float4*>(v.rope_table + (static_cast<int64_t>(rel[j]) * half + cp * 8) * 2);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) reinterpret_cast<float4*>(cs)[q] = t[q];
+    }
+    rel_cur = rel[j];
     float xa[8], xb[8];
     unpack8(ka[j], xa);
     unpack8(kb[j], xb);
-    const float* cs = reinterpret_cast<const float*>(tb[j]);
     uint4 ya, yb;
     bool fits;
     rotate8(xa, xb, cs, &ya, &yb, &fits);
-    *reinterpret_cast<uint4*>(v.k_rot + dst[j] + pa[j]) = ya;
-    *reinterpret_cast<uint4*>(v.k_rot + dst[j] + pb[j]) = yb;
+    const int off = (slot0 + j) % v.page_size;
+    const int64_t o = row0 + static_cast<int64_t>(j) * d;
+    *reinterpret_cast<uint4*>(v.k_rot + o + swizzle_chunk(cp, off) * 8) = ya;
+    *reinterpret_cast<uint4*>(v.k_rot + o + swizzle_chunk(cp + cpairs, off) * 8) = yb;
   }
 }
 
@@ -194,9 +214,9 @@ cudaError_t launch_append_rope(const DevView& v, int n_active, int layer0, int n
 
 cudaError_t launch_rebase(const DevView& v, int n_active, int layer0, int n_layers, cudaStream_t st) {
   if (v.k_rot == nullptr) return cudaSuccess;  // rotate-on-read: nothing is stored re-based
-  const int64_t per_stream = static_cast<int64_t>(v.max_pages) * v.page_size * v.n_kv_heads * (v.head_dim / 16);
-  const int64_t per_block = static_cast<int64_t>(kRebaseThreads) * kRebaseItems;
-  dim3 grid(static_cast<unsigned>((per_stream + per_block - 1) / per_block), n_active, n_layers);
+  const int64_t per_stream =
+      static_cast<int64_t>(v.max_pages) * v.page_size / kRebaseRun * v.n_kv_heads * (v.head_dim / 16);
+  dim3 grid(static_cast<unsigned>((per_stream + kRebaseThreads - 1) / kRebaseThreads), n_active, n_layers);
   rebase_kernel<<<grid, kRebaseThreads, 0, st>>>(v, layer0);
   return cudaGetLastError();
 }
