@@ -245,6 +245,18 @@ RKV_API int rkv_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active,
 RKV_API int rkv_decode_attn_static(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv_bf16* out,
                                    float* lse, void* stream);
 
+/* Empty one stream so that its next step starts a new history: n = len =
+ * evicted = rope_base = 0, kv_pos_offset = P0 = start_offset (0 <= P0 <
+ * 2^52); its window and pages are kept.  This is voxtral.c's continuous-mode
+ * restart (voxtral.c article §四: a hard reset of the decoder cache while the
+ * audio keeps flowing), and the way a serving loop hands a stream slot to a
+ * new audio stream.  Enqueued on `stream` (graph-capturable), so it takes
+ * effect for the next rkv_begin_step on that stream; kernels of an open step
+ * use the step's own descriptors and are not affected.  The stale keys and
+ * values left in the pages are never read: a slot is attended only once the
+ * new history has written it. */
+RKV_API int rkv_reset_stream(rkv_handle* h, int32_t stream_id, int64_t start_offset, void* stream);
+
 /* Copy one stream's device state to host `out` (RKV_STATE_FIELDS int64):
  * n, len, evicted, kv_pos_offset, rope_base, head_slot, W, P0.  Waits for
  * `stream`. */

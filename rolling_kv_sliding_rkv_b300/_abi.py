@@ -68,6 +68,7 @@ _SIGS = {
     "rkv_decode_attn_layers": [_vp, _i32, _i32, _vp, _vp, _vp, _vp],
     "rkv_step": [_vp, C.POINTER(_i32), _i32, _vp, _vp, _vp, _vp, _vp, _vp],
     "rkv_get_stream_state": [_vp, _i32, C.POINTER(_i64), _vp],
+    "rkv_reset_stream": [_vp, _i32, _i64, _vp],
     "rkv_sync_status": [_vp, _vp],
     "rkv_destroy": [_vp],
     "rkv_rope_cossin": [_vp, _i32, _i32, _f64, _vp, _vp],
@@ -185,6 +186,10 @@ def rkv_decode_attn_layers(h: int, layer0: int, n_layers: int, q, out, lse=None,
 def rkv_step(h: int, active_ids, q, k, v, out, lse=None, stream=None) -> None:
     ids, n = _i32_array(active_ids)
     _check(_lib.rkv_step(h, ids, n, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _stream(stream)), h)
+
+
+def rkv_reset_stream(h: int, stream_id: int, start_offset: int, stream=None) -> None:
+    _check(_lib.rkv_reset_stream(h, stream_id, start_offset, _stream(stream)), h)
 
 
 def rkv_get_stream_state(h: int, stream_id: int, stream=None) -> list:

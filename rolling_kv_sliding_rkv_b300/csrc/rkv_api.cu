@@ -387,6 +387,15 @@ int rkv_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active, const r
   return RKV_OK;
 }
 
+int rkv_reset_stream(rkv_handle* h, int32_t stream_id, int64_t start_offset, void* stream) {
+  if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
+  if (stream_id < 0 || stream_id >= h->cfg.n_streams) return fail(h, RKV_ERR_INVALID_ARG, "stream id out of range");
+  if (start_offset < 0 || start_offset >= (int64_t(1) << 52))
+    return fail(h, RKV_ERR_CONFIG, "start_offset must be in [0, 2^52)");
+  cudaError_t e = rkv::launch_reset_stream(h->view, stream_id, start_offset, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RKV_OK : cuda_fail(h, e, "reset_stream launch");
+}
+
 int rkv_get_stream_state(rkv_handle* h, int32_t stream_id, int64_t* out, void* stream) {
   if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
   if (!out || stream_id < 0 || stream_id >= h->cfg.n_streams) return fail(h, RKV_ERR_INVALID_ARG, "bad stream id or out");

@@ -134,6 +134,7 @@ __device__ __forceinline__ int64_t pool_offset(const DevView& v, int layer, int 
 // ---- launchers (host functions, one translation unit each) ----
 cudaError_t launch_init_tables(const DevView& v, cudaStream_t st);
 cudaError_t launch_begin_step(const DevView& v, const ActiveIds& ids, cudaStream_t st);
+cudaError_t launch_reset_stream(const DevView& v, int s, int64_t p0, cudaStream_t st);
 // Layers [layer0, layer0 + n_layers) in one launch; per-layer tensors of the
 // step's inputs/outputs are `*_layer_stride` elements apart.
 cudaError_t launch_append_rope(const DevView& v, int n_active, int layer0, int n_layers, const uint16_t* k,

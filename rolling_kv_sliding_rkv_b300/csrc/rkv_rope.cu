@@ -89,7 +89,25 @@ __global__ void begin_step_kernel(DevView v, ActiveIds ids) {
   }
 }
 
+// One thread: empty stream s (its pages keep stale data, which the ring
+// bookkeeping masks: slots at or beyond len are never read before rewritten).
+__global__ void reset_stream_kernel(DevView v, int s, int64_t p0) {
+  int64_t* st = v.state + static_cast<int64_t>(s) * kStateFields;
+  st[F_N] = 0;
+  st[F_LEN] = 0;
+  st[F_EVICTED] = 0;
+  st[F_KV_POS_OFFSET] = p0;
+  st[F_ROPE_BASE] = 0;
+  st[F_HEAD_SLOT] = 0;
+  st[F_P0] = p0;  // F_W is kept: the stream's pages fix its window
+}
+
 }  // namespace
+
+cudaError_t launch_reset_stream(const DevView& v, int s, int64_t p0, cudaStream_t st) {
+  reset_stream_kernel<<<1, 1, 0, st>>>(v, s, p0);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rope_cossin(const int64_t* pos, int n, int head_dim, const Omegas& w, float* cs,
                                cudaStream_t st) {
