@@ -257,6 +257,22 @@ RKV_API int rkv_decode_attn_static(rkv_handle* h, int32_t layer, const rkv_bf16*
  * new history has written it. */
 RKV_API int rkv_reset_stream(rkv_handle* h, int32_t stream_id, int64_t start_offset, void* stream);
 
+/* Snapshot of one stream for resume: its ring state and the contents of its
+ * pages in every layer (no page describes this; it is how a 24/7 serving
+ * loop moves or checkpoints a live stream).  rkv_stream_snapshot_bytes gives
+ * the size: a 128-byte header (configuration, window, scheme), the
+ * RKV_STATE_FIELDS int64 state, then the stream's pages, region by region and
+ * layer by layer.  rkv_save_stream writes it to `dst`; rkv_load_stream
+ * restores it into a stream slot of a handle with the same configuration and
+ * the same window for that slot (else RKV_ERR_CONFIG), after which the stream
+ * continues exactly where it was saved.  dst / src may be host or device
+ * memory.  Both wait for `stream` before returning (not graph-capturable) and
+ * return RKV_ERR_STATE while a step is in progress (some layer of the open
+ * step lacks rkv_append_rope or rkv_rebase). */
+RKV_API int rkv_stream_snapshot_bytes(const rkv_handle* h, int32_t stream_id, size_t* bytes);
+RKV_API int rkv_save_stream(rkv_handle* h, int32_t stream_id, void* dst, size_t bytes, void* stream);
+RKV_API int rkv_load_stream(rkv_handle* h, int32_t stream_id, const void* src, size_t bytes, void* stream);
+
 /* Copy one stream's device state to host `out` (RKV_STATE_FIELDS int64):
  * n, len, evicted, kv_pos_offset, rope_base, head_slot, W, P0.  Waits for
  * `stream`. */

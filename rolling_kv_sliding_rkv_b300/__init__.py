@@ -14,7 +14,8 @@ from ._abi import (  # noqa: F401
     RKV_ERR_STATE, RKV_ERR_TIMEOUT, RKV_OK, RKV_SCHEME_EXACT_ON_READ, RKV_SCHEME_EXACT_REBASE, RKV_SCHEME_OFFSET_ONLY,
     STATE_FIELDS, RkvError, make_config, rkv_append_rope, rkv_begin_step, rkv_clock_resolve,
     rkv_create, rkv_decode_attn, rkv_decode_attn_layers, rkv_decode_attn_static, rkv_destroy, rkv_gen_step_inputs, rkv_gen_tokens,
-    rkv_get_stream_state, rkv_last_error, rkv_rebase, rkv_required_bytes, rkv_reset_stream, rkv_rope_cossin,
+    rkv_get_stream_state, rkv_last_error, rkv_load_stream, rkv_rebase, rkv_required_bytes, rkv_reset_stream,
+    rkv_rope_cossin, rkv_save_stream, rkv_stream_snapshot_bytes,
     rkv_step, rkv_sync_status,
 )
 
@@ -61,6 +62,17 @@ class RollingKV:
 
     def reset_stream(self, stream_id, start_offset=0, stream=None):
         rkv_reset_stream(self.handle, stream_id, start_offset, stream)
+
+    def save_stream(self, stream_id, stream=None):
+        """The stream's snapshot as a uint8 tensor on the handle's device."""
+        import torch
+        n = rkv_stream_snapshot_bytes(self.handle, stream_id)
+        buf = torch.empty(n, dtype=torch.uint8, device=self.pool.device)
+        rkv_save_stream(self.handle, stream_id, buf, n, stream)
+        return buf
+
+    def load_stream(self, stream_id, snapshot, stream=None):
+        rkv_load_stream(self.handle, stream_id, snapshot, snapshot.numel() * snapshot.element_size(), stream)
 
     def stream_state(self, stream_id, stream=None) -> dict:
         return dict(zip(STATE_FIELDS, rkv_get_stream_state(self.handle, stream_id, stream)))

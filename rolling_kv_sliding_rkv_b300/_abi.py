@@ -69,6 +69,9 @@ _SIGS = {
     "rkv_step": [_vp, C.POINTER(_i32), _i32, _vp, _vp, _vp, _vp, _vp, _vp],
     "rkv_get_stream_state": [_vp, _i32, C.POINTER(_i64), _vp],
     "rkv_reset_stream": [_vp, _i32, _i64, _vp],
+    "rkv_stream_snapshot_bytes": [_vp, _i32, C.POINTER(_sz)],
+    "rkv_save_stream": [_vp, _i32, _vp, _sz, _vp],
+    "rkv_load_stream": [_vp, _i32, _vp, _sz, _vp],
     "rkv_sync_status": [_vp, _vp],
     "rkv_destroy": [_vp],
     "rkv_rope_cossin": [_vp, _i32, _i32, _f64, _vp, _vp],
@@ -190,6 +193,20 @@ def rkv_step(h: int, active_ids, q, k, v, out, lse=None, stream=None) -> None:
 
 def rkv_reset_stream(h: int, stream_id: int, start_offset: int, stream=None) -> None:
     _check(_lib.rkv_reset_stream(h, stream_id, start_offset, _stream(stream)), h)
+
+
+def rkv_stream_snapshot_bytes(h: int, stream_id: int) -> int:
+    n = _sz()
+    _check(_lib.rkv_stream_snapshot_bytes(h, stream_id, C.byref(n)))
+    return n.value
+
+
+def rkv_save_stream(h: int, stream_id: int, dst, nbytes: int, stream=None) -> None:
+    _check(_lib.rkv_save_stream(h, stream_id, _ptr(dst), nbytes, _stream(stream)), h)
+
+
+def rkv_load_stream(h: int, stream_id: int, src, nbytes: int, stream=None) -> None:
+    _check(_lib.rkv_load_stream(h, stream_id, _ptr(src), nbytes, _stream(stream)), h)
 
 
 def rkv_get_stream_state(h: int, stream_id: int, stream=None) -> list:

@@ -18,6 +18,10 @@ struct rkv_handle {
   bool step_open = false;
   int32_t n_active = 0;
   std::vector<uint8_t> appended, rebased;
+  std::vector<int32_t> first_page, n_pages_of;  // per stream: its contiguous run of pages
+  int32_t regions = 0;
+  uint16_t* pool = nullptr;
+  size_t region_elems = 0;
   std::string last_error;
 };
 
@@ -245,6 +249,8 @@ int rkv_create(const rkv_config* cfg, const int32_t* window, const int64_t* star
     st[rkv::F_W] = window[s];
     st[rkv::F_P0] = start_offset[s];
     const int pages = (window[s] + cfg->page_size - 1) / cfg->page_size;
+    h->first_page.push_back(next_page);
+    h->n_pages_of.push_back(pages);
     for (int p = 0; p < pages; ++p) table[static_cast<size_t>(s) * L.max_pages + p] = next_page++;
   }
   std::vector<double> omega(half);
@@ -268,6 +274,9 @@ int rkv_create(const rkv_config* cfg, const int32_t* window, const int64_t* star
   }
   h->appended.assign(cfg->n_layers, 0);
   h->rebased.assign(cfg->n_layers, 0);
+  h->regions = L.regions;
+  h->pool = pool;
+  h->region_elems = L.pool_region_elems;
   *out = h;
   return RKV_OK;
 }
@@ -394,6 +403,113 @@ int rkv_reset_stream(rkv_handle* h, int32_t stream_id, int64_t start_offset, voi
     return fail(h, RKV_ERR_CONFIG, "start_offset must be in [0, 2^52)");
   cudaError_t e = rkv::launch_reset_stream(h->view, stream_id, start_offset, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? RKV_OK : cuda_fail(h, e, "reset_stream launch");
+}
+
+namespace {
+
+constexpr int64_t kSnapMagic = 0x31504e5356524bLL;  // "KRVSNP1" little-endian tag
+constexpr int kSnapHeader = 16;                    // int64 words of the header
+constexpr int kSnapState = rkv::kStateFields;
+
+void snap_header(const rkv_handle* h, int32_t s, int64_t* hdr) {
+  const rkv_config& c = h->cfg;
+  const int64_t fields[kSnapHeader] = {kSnapMagic, 1, c.n_layers, c.n_kv_heads, c.head_dim, c.page_size,
+                                       c.scheme, c.q_per_step, c.rebase_interval,
+                                       static_cast<int64_t>(h->n_pages_of[s]), h->regions, 0, 0, 0, 0, 0};
+  std::memcpy(hdr, fields, sizeof fields);
+}
+
+// elements of one (region, layer) run of a stream's pages
+size_t snap_run_elems(const rkv_handle* h, int32_t s) {
+  const rkv_config& c = h->cfg;
+  return static_cast<size_t>(h->n_pages_of[s]) * c.n_kv_heads * c.page_size * c.head_dim;
+}
+
+size_t snap_bytes(const rkv_handle* h, int32_t s) {
+  return (kSnapHeader + kSnapState) * sizeof(int64_t) +
+         static_cast<size_t>(h->regions) * h->cfg.n_layers * snap_run_elems(h, s) * sizeof(uint16_t);
+}
+
+bool step_in_progress(const rkv_handle* h) {
+  if (!h->step_open) return false;
+  const bool exact = rkv::exact_scheme(h->cfg.scheme);
+  for (int l = 0; l < h->cfg.n_layers; ++l)
+    if (!h->appended[l] || (exact && !h->rebased[l])) return true;
+  return false;
+}
+
+// pointer to (region r, layer l) of stream s's pages
+uint16_t* snap_run(const rkv_handle* h, int32_t s, int r, int l) {
+  const rkv_config& c = h->cfg;
+  return h->pool + static_cast<size_t>(r) * h->region_elems + static_cast<size_t>(l) * h->view.layer_stride +
+         static_cast<size_t>(h->first_page[s]) * c.n_kv_heads * c.page_size * c.head_dim;
+}
+
+}  // namespace
+
+int rkv_stream_snapshot_bytes(const rkv_handle* h, int32_t stream_id, size_t* bytes) {
+  if (!h || !bytes) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle or bytes is NULL");
+  if (stream_id < 0 || stream_id >= h->cfg.n_streams) return fail(nullptr, RKV_ERR_INVALID_ARG, "stream id out of range");
+  *bytes = snap_bytes(h, stream_id);
+  return RKV_OK;
+}
+
+int rkv_save_stream(rkv_handle* h, int32_t stream_id, void* dst, size_t bytes, void* stream) {
+  if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
+  if (stream_id < 0 || stream_id >= h->cfg.n_streams || !dst) return fail(h, RKV_ERR_INVALID_ARG, "bad stream id or dst");
+  if (bytes < snap_bytes(h, stream_id)) return fail(h, RKV_ERR_CAPACITY, "dst smaller than rkv_stream_snapshot_bytes");
+  if (step_in_progress(h)) return fail(h, RKV_ERR_STATE, "a step is in progress (a layer lacks rkv_append_rope or rkv_rebase)");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int64_t hdr[kSnapHeader];
+  snap_header(h, stream_id, hdr);
+  char* d = static_cast<char*>(dst);
+  cudaError_t e = cudaMemcpyAsync(d, hdr, sizeof hdr, cudaMemcpyDefault, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(d + sizeof hdr, h->view.state + static_cast<int64_t>(stream_id) * rkv::kStateFields,
+                        kSnapState * sizeof(int64_t), cudaMemcpyDefault, st);
+  size_t off = (kSnapHeader + kSnapState) * sizeof(int64_t);
+  const size_t run = snap_run_elems(h, stream_id) * sizeof(uint16_t);
+  for (int r = 0; r < h->regions && e == cudaSuccess; ++r)
+    for (int l = 0; l < h->cfg.n_layers && e == cudaSuccess; ++l, off += run)
+      e = cudaMemcpyAsync(d + off, snap_run(h, stream_id, r, l), run, cudaMemcpyDefault, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return e == cudaSuccess ? RKV_OK : cuda_fail(h, e, "saving a stream");
+}
+
+int rkv_load_stream(rkv_handle* h, int32_t stream_id, const void* src, size_t bytes, void* stream) {
+  if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
+  if (stream_id < 0 || stream_id >= h->cfg.n_streams || !src) return fail(h, RKV_ERR_INVALID_ARG, "bad stream id or src");
+  if (bytes < snap_bytes(h, stream_id)) return fail(h, RKV_ERR_CAPACITY, "src smaller than rkv_stream_snapshot_bytes");
+  if (step_in_progress(h)) return fail(h, RKV_ERR_STATE, "a step is in progress (a layer lacks rkv_append_rope or rkv_rebase)");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const char* sp = static_cast<const char*>(src);
+  int64_t hdr[kSnapHeader], want[kSnapHeader], state[kSnapState];
+  cudaError_t e = cudaMemcpyAsync(hdr, sp, sizeof hdr, cudaMemcpyDefault, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(state, sp + sizeof hdr, sizeof state, cudaMemcpyDefault, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "reading a snapshot header");
+  snap_header(h, stream_id, want);
+  if (std::memcmp(hdr, want, sizeof hdr) != 0)
+    return fail(h, RKV_ERR_CONFIG, "snapshot taken under another configuration, window or scheme");
+  if (state[rkv::F_N] < 0 ||
+      state[rkv::F_LEN] < 0 || state[rkv::F_LEN] > state[rkv::F_W])
+    return fail(h, RKV_ERR_CONFIG, "snapshot state is inconsistent");
+  // the window is part of the stream's layout: it must be the slot's own
+  int64_t w_dev = 0;
+  e = cudaMemcpyAsync(&w_dev, h->view.state + static_cast<int64_t>(stream_id) * rkv::kStateFields + rkv::F_W,
+                      sizeof w_dev, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "reading the stream's window");
+  if (w_dev != state[rkv::F_W]) return fail(h, RKV_ERR_CONFIG, "snapshot window differs from the stream's window");
+  e = cudaMemcpyAsync(h->view.state + static_cast<int64_t>(stream_id) * rkv::kStateFields, sp + sizeof hdr,
+                      kSnapState * sizeof(int64_t), cudaMemcpyDefault, st);
+  size_t off = (kSnapHeader + kSnapState) * sizeof(int64_t);
+  const size_t run = snap_run_elems(h, stream_id) * sizeof(uint16_t);
+  for (int r = 0; r < h->regions && e == cudaSuccess; ++r)
+    for (int l = 0; l < h->cfg.n_layers && e == cudaSuccess; ++l, off += run)
+      e = cudaMemcpyAsync(snap_run(h, stream_id, r, l), sp + off, run, cudaMemcpyDefault, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return e == cudaSuccess ? RKV_OK : cuda_fail(h, e, "loading a stream");
 }
 
 int rkv_get_stream_state(rkv_handle* h, int32_t stream_id, int64_t* out, void* stream) {

@@ -45,6 +45,7 @@ constexpr int kTeamWarps = 4;             // consumer warps per team: 16 slots o
 constexpr int kTeams = 1;                 // teams take alternate stages
 constexpr int kCW = kTeamWarps * kTeams;  // consumer warps
 constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
+static_assert(kCW == 4, "the epilogue sums warps 0 + 2 and 1 + 3");
 constexpr int kKS = 64;                   // ring slots per stage
 // shared-memory ring per CTA: 96 KB of K/V stages whatever the head dim (a multiple of kTeams)
 template <int D>
@@ -213,16 +214,12 @@ __device__ __forceinline__ void rotate_pair_regs(uint32_t& a, uint32_t& b, const
 
 template <int D, int NT>
 __host__ __device__ constexpr int smem_bytes() {
-  // stages (K | V), query tiles hi + lo, fp32 output accumulator
-  return stages_for<D>() * 2 * kKS * D * 2 + 2 * (8 * NT) * (D + 8) * 2 + (8 * NT) * (D + 4) * 4;
+  // stages (K | V), query tiles hi + lo, two fp32 output tiles
+  return stages_for<D>() * 2 * kKS * D * 2 + 2 * (8 * NT) * (D + 8) * 2 + 2 * (8 * NT) * (D + 4) * 4;
 }
 static_assert(smem_bytes<128, 2>() <= 227 * 1024, "shared memory budget");
 static_assert(stages_for<128>() % kTeams == 0 && stages_for<64>() % kTeams == 0,
               "a ring slot must always be consumed by the same team");
-
-__device__ __forceinline__ void red_add_shared(float* p, float x) {
-  asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(smem_u32(p)), "f"(x) : "memory");
-}
 
 __device__ __forceinline__ float4 ld_dsmem_f32x4(const void* local, uint32_t rank) {
   uint32_t remote;
@@ -342,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
   uint16_t* kv_s = reinterpret_cast<uint16_t*>(smem);  // [stage][K | V][64][D]
   uint16_t* qh_s = kv_s + kStages * 2 * STAGE_ELEMS;   // [ROWS][QSTR] fp16 hi
   uint16_t* ql_s = qh_s + ROWS * QSTR;                 // [ROWS][QSTR] fp16 lo
-  float* obuf = reinterpret_cast<float*>(ql_s + ROWS * QSTR);  // [ROWS][OSTR] fp32
+  float* obuf = reinterpret_cast<float*>(ql_s + ROWS * QSTR);  // [2][ROWS][OSTR] fp32 partial sums
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
   __shared__ float red_m[kCW][ROWS], red_l[kCW][ROWS];
   __shared__ float row_m[ROWS], row_l[ROWS];
@@ -371,7 +368,6 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
     poisoned_s = *reinterpret_cast<volatile int32_t*>(v.status) == DEV_TIMEOUT;
     asm volatile("fence.mbarrier_init.release.cluster;\n\tfence.proxy.async.shared::cta;" ::: "memory");
   }
-  for (int e = threadIdx.x; e < ROWS * OSTR; e += kThreads) obuf[e] = 0.f;
   __syncthreads();
   const bool poisoned = poisoned_s != 0;
 
@@ -652,6 +648,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
           }
         }
       consumer_sync();  // S2
+      float sc[NT][2];  // this warp's rescale factor per row
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -669,15 +666,32 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
             row_m[row] = mx;
             row_l[row] = lsum;
           }
-          if (f != 0.f) {
+          // deterministic sum: warps 0, 1 store into tiles 0, 1, then warps 2, 3 add theirs
+          if (warp < 2) {
+            float* tile = obuf + warp * ROWS * OSTR + row * OSTR;
 #pragma unroll
             for (int mt = 0; mt < KSTEPS; ++mt) {
-              red_add_shared(&obuf[row * OSTR + mt * 16 + g], o_acc[mt][nt][c] * f);
-              red_add_shared(&obuf[row * OSTR + mt * 16 + g + 8], o_acc[mt][nt][c + 2] * f);
+              tile[mt * 16 + g] = o_acc[mt][nt][c] * f;
+              tile[mt * 16 + g + 8] = o_acc[mt][nt][c + 2] * f;
             }
           }
+          sc[nt][c] = f;
         }
-      // S3: obuf holds the CTA's unnormalised output, row_m / row_l its statistics; a wait that
+      consumer_sync();  // S2b: tiles 0 and 1 hold warps 0 and 1
+      if (warp >= 2) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            float* tile = obuf + (warp - 2) * ROWS * OSTR + (nt * 8 + 2 * tq + c) * OSTR;
+#pragma unroll
+            for (int mt = 0; mt < KSTEPS; ++mt) {
+              tile[mt * 16 + g] += o_acc[mt][nt][c] * sc[nt][c];
+              tile[mt * 16 + g + 8] += o_acc[mt][nt][c + 2] * sc[nt][c];
+            }
+          }
+      }
+      // S3: tiles 0 + 1 hold the CTA's unnormalised output, row_m / row_l its statistics; a wait that
       // gave up in any warp ends the unit loop for all of them
       if (consumer_sync_or(aborted)) break;
 
@@ -686,10 +700,12 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
       constexpr int CH = D / 8;
       for (int e = tid; e < rows * CH; e += kCW * 32) {
         const int row = e / CH, ch = e % CH;
-        float* src = obuf + row * OSTR + ch * 8;
-        const float4 o0 = *reinterpret_cast<const float4*>(src), o1 = *reinterpret_cast<const float4*>(src + 4);
-        *reinterpret_cast<float4*>(src) = make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4*>(src + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* src = obuf + row * OSTR + ch * 8;
+        const float4 a0 = *reinterpret_cast<const float4*>(src), a1 = *reinterpret_cast<const float4*>(src + 4);
+        const float4 b0 = *reinterpret_cast<const float4*>(src + ROWS * OSTR);
+        const float4 b1 = *reinterpret_cast<const float4*>(src + ROWS * OSTR + 4);
+        const float4 o0 = make_float4(a0.x + b0.x, a0.y + b0.y, a0.z + b0.z, a0.w + b0.w);
+        const float4 o1 = make_float4(a1.x + b1.x, a1.y + b1.y, a1.z + b1.z, a1.w + b1.w);
         const float mx = row_m[row], lsum = row_l[row];
         const int t = row / group, h = un.kvh * group + row % group;
         const int64_t orow = (static_cast<int64_t>(un.a) * nq + t) * hq + h;
@@ -745,8 +761,12 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
         for (int r = 0; r < 8; ++r) {
           if (r < splits && mr[r] != -CUDART_INF_F) {
             const float f = exp2f(mr[r] - mx);
-            const float4 a0 = ld_dsmem_f32x4(obuf + row * OSTR + ch * 8, r);
-            const float4 a1 = ld_dsmem_f32x4(obuf + row * OSTR + ch * 8 + 4, r);
+            const float4 t0 = ld_dsmem_f32x4(obuf + row * OSTR + ch * 8, r);
+            const float4 t1 = ld_dsmem_f32x4(obuf + row * OSTR + ch * 8 + 4, r);
+            const float4 u0 = ld_dsmem_f32x4(obuf + ROWS * OSTR + row * OSTR + ch * 8, r);
+            const float4 u1 = ld_dsmem_f32x4(obuf + ROWS * OSTR + row * OSTR + ch * 8 + 4, r);
+            const float4 a0 = make_float4(t0.x + u0.x, t0.y + u0.y, t0.z + u0.z, t0.w + u0.w);
+            const float4 a1 = make_float4(t1.x + u1.x, t1.y + u1.y, t1.z + u1.z, t1.w + u1.w);
             lsum += lr[r] * f;
             o[0] += a0.x * f;
             o[1] += a0.y * f;

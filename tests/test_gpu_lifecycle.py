@@ -93,3 +93,74 @@ def test_reset_stream_validates_arguments():
         h.reset_stream(0, -1)
     assert e.value.code == rkv.RKV_ERR_CONFIG
     h.close()
+
+
+def _drive(h, wl, steps, q, k, v, out, lse, record_stream=None):
+    """Run `steps` steps of all streams with the generator's inputs; return the recorded outputs."""
+    rec = []
+    S, L = wl.n_streams, wl.n_layers
+    for _ in range(steps):
+        h.begin_step(list(range(S)))
+        for layer in range(L):
+            h.gen_step_inputs(wl.seed, layer, wl.input_scale, q, k, v)
+            if wl.scheme:
+                h.rebase(layer)
+            h.append_rope(layer, k, v)
+            h.decode_attn(layer, q, out, lse)
+            if record_stream is not None:
+                rec.append((out[record_stream].clone(), lse[record_stream].clone()))
+    return rec
+
+
+@pytest.mark.parametrize("scheme,where", [(1, "device"), (2, "host"), (0, "device")])
+def test_snapshot_resumes_a_stream_exactly(scheme, where):
+    """A stream saved from one handle and loaded into another continues bit for bit."""
+    import torch
+
+    import rolling_kv_sliding_rkv_b300 as rkv
+
+    wl = synth.workload("qwen", n_layers=2, n_streams=3, extra={"window": 100}, scheme=scheme)
+    S, L, hq, hkv, d = wl.n_streams, wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+
+    def handle():
+        return rkv.RollingKV(wl.windows().tolist(), wl.start_offsets().tolist(), n_layers=L, n_streams=S,
+                             n_q_heads=hq, n_kv_heads=hkv, head_dim=d, q_per_step=1, scheme=scheme,
+                             rope_theta=wl.rope_theta)
+
+    q = torch.empty(S, 1, hq, d, dtype=torch.bfloat16, device="cuda")
+    k = torch.empty(S, 1, hkv, d, dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    out = torch.empty_like(q)
+    lse = torch.empty(S, 1, hq, dtype=torch.float32, device="cuda")
+    a = handle()
+    _drive(a, wl, 130, q, k, v, out, lse)
+    snap = a.save_stream(1)
+    if where == "host":
+        snap = snap.cpu()
+    state_a = a.stream_state(1)
+    ref = _drive(a, wl, 20, q, k, v, out, lse, record_stream=1)
+
+    b = handle()
+    _drive(b, wl, 7, q, k, v, out, lse)          # b's other streams are elsewhere in their histories
+    b.load_stream(1, snap)
+    assert b.stream_state(1) == state_a
+    got = _drive(b, wl, 20, q, k, v, out, lse, record_stream=1)
+    for (o_ref, l_ref), (o, lv) in zip(ref, got):
+        assert torch.equal(o_ref, o) and torch.equal(l_ref, lv)
+    assert b.stream_state(1) == a.stream_state(1)
+    a.sync_status()
+    b.sync_status()
+
+    # a slot with another window cannot take the snapshot
+    c = rkv.RollingKV([100, 90, 100], wl.start_offsets().tolist(), n_layers=L, n_streams=S, n_q_heads=hq,
+                      n_kv_heads=hkv, head_dim=d, q_per_step=1, scheme=scheme, rope_theta=wl.rope_theta)
+    with pytest.raises(rkv.RkvError) as e:
+        c.load_stream(1, snap)
+    assert e.value.code == rkv.RKV_ERR_CONFIG
+    # nor can a handle in the middle of a step save or load
+    b.begin_step(list(range(S)))
+    with pytest.raises(rkv.RkvError) as e:
+        b.save_stream(0)
+    assert e.value.code == rkv.RKV_ERR_STATE
+    for hh in (a, b, c):
+        hh.close()
