@@ -51,6 +51,8 @@ __device__ __forceinline__ void rotate8(const float (&xa)[8], const float (&xb)[
 // One thread per (layer, active stream, new token, kv head, chunk pair).
 __global__ void __launch_bounds__(128) append_rope_kernel(DevView v, int layer0, int n_rows, const uint16_t* __restrict__ k,
                                                           const uint16_t* __restrict__ val, int64_t kv_layer_stride) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int d = v.head_dim, half = d / 2, cpairs = d / 16, hkv = v.n_kv_heads;
   const int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   const int64_t per_layer = static_cast<int64_t>(n_rows) * hkv * cpairs;
@@ -123,6 +125,8 @@ constexpr int kRebaseThreads = 128;
 constexpr int kRebaseRun = 8;  // divides every page size (16 .. 128)
 
 __global__ void __launch_bounds__(kRebaseThreads, 3) rebase_kernel(DevView v, int layer0) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int d = v.head_dim, half = d / 2, cpairs = d / 16;
   const int a = blockIdx.y;
   const int lz = blockIdx.z;
@@ -208,8 +212,7 @@ cudaError_t launch_append_rope(const DevView& v, int n_active, int layer0, int n
   const int n_rows = n_active * v.q_per_step;
   const int64_t per_layer = static_cast<int64_t>(n_rows) * v.n_kv_heads * (v.head_dim / 16);
   dim3 grid(static_cast<unsigned>((per_layer + 127) / 128), n_layers);
-  append_rope_kernel<<<grid, 128, 0, st>>>(v, layer0, n_rows, k, vv, kv_layer_stride);
-  return cudaGetLastError();
+  return launch_pdl(append_rope_kernel, grid, dim3(128), 0, st, v, layer0, n_rows, k, vv, kv_layer_stride);
 }
 
 cudaError_t launch_rebase(const DevView& v, int n_active, int layer0, int n_layers, cudaStream_t st) {
@@ -217,8 +220,7 @@ cudaError_t launch_rebase(const DevView& v, int n_active, int layer0, int n_laye
   const int64_t per_stream =
       static_cast<int64_t>(v.max_pages) * v.page_size / kRebaseRun * v.n_kv_heads * (v.head_dim / 16);
   dim3 grid(static_cast<unsigned>((per_stream + kRebaseThreads - 1) / kRebaseThreads), n_active, n_layers);
-  rebase_kernel<<<grid, kRebaseThreads, 0, st>>>(v, layer0);
-  return cudaGetLastError();
+  return launch_pdl(rebase_kernel, grid, dim3(kRebaseThreads), 0, st, v, layer0);
 }
 
 }  // namespace rkv

@@ -36,6 +36,7 @@
 
 #include <mutex>
 
+#include "rkv_async.cuh"
 #include "rkv_internal.cuh"
 
 namespace rkv {
@@ -52,7 +53,6 @@ template <int D>
 __host__ __device__ constexpr int stages_for() {
   return 3 * 128 / D;
 }
-constexpr unsigned long long kWaitNs = 1000000000ull;  // give up on a barrier after 1 s
 
 struct AttnArgs {
   DevView v;
@@ -64,57 +64,6 @@ struct AttnArgs {
   int splits, stages_per_split;
   int mode;            // 0: whole windows; 1: split, cluster merge; 2: split, partials to part_ml / part_o
 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Wait for the phase with the given parity to complete; false after kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_test(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
-  for (;;) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_test(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitNs) return false;
-  }
-}
-
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
 
 // 2^x with the hardware approximation (relative error about 2^-22; subnormal
 // results flush to zero, which softmax weights below 2^-126 can afford)
@@ -357,12 +306,16 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
   const int u_first = splits > 1 ? static_cast<int>(blockIdx.x / splits) : static_cast<int>(blockIdx.x);
   const int u_step = splits > 1 ? n_units : static_cast<int>(gridDim.x);
 
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), kTeamWarps);
     }
     abort_flag = 0;
+  }
+  pdl_wait();  // the step's descriptors, the pages and the queries come from earlier kernels
+  if (threadIdx.x == 0) {
     // after a timed-out wait anywhere, later launches skip their copies (the
     // status word already reports the failure; each CTA ends quickly)
     poisoned_s = *reinterpret_cast<volatile int32_t*>(v.status) == DEV_TIMEOUT;
@@ -795,6 +748,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
 template <int D>
 __global__ void __launch_bounds__(128) merge_kernel(DevView v, int splits, uint16_t* __restrict__ out,
                                                     float* __restrict__ lse) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t prow0 = static_cast<int64_t>(blockIdx.x) * splits;
   const float* ml = v.part_ml + prow0 * 2;
   float mx = -CUDART_INF_F;
@@ -834,15 +789,17 @@ struct Kernel {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem_bytes<D, NT>();
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.attrs = attr;
-    cfg.numAttrs = 0;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 1;
     if (args.mode == 1) {
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = args.splits;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.numAttrs = 1;
+      attr[1].id = cudaLaunchAttributeClusterDimension;
+      attr[1].val.clusterDim.x = args.splits;
+      attr[1].val.clusterDim.y = 1;
+      attr[1].val.clusterDim.z = 1;
+      cfg.numAttrs = 2;
     }
     return cudaLaunchKernelEx(&cfg, attn_kernel<D, NT, ON_READ>, args);
   }
@@ -938,11 +895,8 @@ cudaError_t launch_decode_attn_scratch(const DevView& v, int n_active, int layer
   cudaError_t e = dispatch(args, static_cast<int>(grid), st);
   if (e != cudaSuccess || p.splits == 1) return e;
   const int blocks = n_active * v.q_per_step * v.n_q_heads;
-  if (v.head_dim == 128)
-    merge_kernel<128><<<blocks, 128, 0, st>>>(v, p.splits, out, lse);
-  else
-    merge_kernel<64><<<blocks, 64, 0, st>>>(v, p.splits, out, lse);
-  return cudaGetLastError();
+  if (v.head_dim == 128) return launch_pdl(merge_kernel<128>, dim3(blocks), dim3(128), 0, st, v, p.splits, out, lse);
+  return launch_pdl(merge_kernel<64>, dim3(blocks), dim3(64), 0, st, v, p.splits, out, lse);
 }
 
 }  // namespace rkv

@@ -72,6 +72,31 @@ struct ActiveIds {
   int32_t id[RKV_MAX_STREAMS];
 };
 
+// Programmatic dependent launch: the hot-path kernels are launched so that the
+// next kernel in the stream may be scheduled while this one finishes; each
+// kernel lets its dependents launch at once and then waits for its own
+// predecessor to complete (memory visible) before reading anything.  A
+// dependent grid launches only after every CTA of its predecessor has
+// started, so waiting CTAs never hold resources the predecessor still needs.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 __device__ __forceinline__ void record_error(int32_t* status, int code, int detail, int detail2) {
   if (atomicCAS(status, DEV_OK, code) == DEV_OK) {
     status[1] = detail;

@@ -41,6 +41,8 @@ __global__ void init_tables_kernel(DevView v) {
 // rkv.h, rkv_begin_step), record the step descriptor, then cos/sin of the
 // positions of the step's new tokens.
 __global__ void begin_step_kernel(DevView v, ActiveIds ids) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int a = blockIdx.x;
   const int s = ids.id[a];
   __shared__ int64_t pos0;
@@ -128,8 +130,7 @@ cudaError_t launch_init_tables(const DevView& v, cudaStream_t st) {
 }
 
 cudaError_t launch_begin_step(const DevView& v, const ActiveIds& ids, cudaStream_t st) {
-  begin_step_kernel<<<ids.n, 64, 0, st>>>(v, ids);
-  return cudaGetLastError();
+  return launch_pdl(begin_step_kernel, dim3(ids.n), dim3(64), 0, st, v, ids);
 }
 
 }  // namespace rkv
