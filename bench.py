@@ -236,6 +236,24 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- GPU leg
 
+def aggregate(ms_local, stream_steps_local, world, device=None):
+    """Whole-job figures over the ranks: the slowest rank's time and all ranks' stream-steps.
+
+    Every rank runs its own streams (replicas: no exchange on the data path); the job is done
+    when the slowest rank is, so value = (sum of stream-steps) / (max of times)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(ms_local)], dtype=torch.float64, device=device)
+        n = torch.tensor([float(stream_steps_local)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(n, op=dist.ReduceOp.SUM)
+        ms, total = float(t.item()), float(n.item())
+    else:
+        ms, total = float(ms_local), float(stream_steps_local)
+    return {"ms": ms, "stream_steps": total, "value": total / (ms / 1000.0)}
+
+
 def step_phases(wl):
     """Active stream lists of one period of the workload's schedule (one list if every stream steps)."""
     if not wl.tick_ms:
@@ -344,13 +362,9 @@ def measure(wl, args, dev, rank, world, timed=True, p0=None, attention=True):
         torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1)
     barrier()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
     h.sync_status()
-    stream_steps = sum(len(plan[i % R]) for i in range(args.steps))
-    out.update(value=world * stream_steps / (ms / 1000.0), ms=ms, stream_steps=stream_steps,
+    job = aggregate(ms, sum(len(plan[i % R]) for i in range(args.steps)), world, dev)
+    out.update(value=job["value"], ms=job["ms"], stream_steps=job["stream_steps"],
                launches=launches_per_step * sum(1 for i in range(args.steps) if graphs[i % R] is not None),
                free_bytes_delta=torch.cuda.mem_get_info(dev)[0] - free_before)
     if not attention:

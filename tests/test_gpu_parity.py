@@ -48,6 +48,12 @@ SMALL = {
                                             extra={"window": 90}, scheme=2), 40),
     "gqa16_whole_step": ("tiny", dict(n_layers=2, n_streams=3, n_q_heads=16, n_kv_heads=1, extra={"window": 150}),
                          170, True),
+    # degenerate windows: one key (the current token only), two keys, and W = Q for the encoder
+    # (each step evicts everything before it)
+    "tiny_w1": ("tiny", dict(n_layers=1, n_streams=2, extra={"window": 1}), 20),
+    "tiny_w2_on_read": ("tiny", dict(n_layers=1, n_streams=2, extra={"window": 2}, scheme=2), 20),
+    "tiny_w2_exact": ("tiny", dict(n_layers=1, n_streams=2, extra={"window": 2}), 20),
+    "encoder_w4": ("encoder", dict(n_layers=1, n_streams=2, extra={"window": 4}), 12),
     # head_dim 64 with GQA, one query per step
     "d64_gqa4": ("tiny", dict(n_layers=1, n_streams=2, n_q_heads=8, n_kv_heads=2, head_dim=64,
                               extra={"window": 150}), 190),
@@ -80,6 +86,9 @@ FULL = {
     "encoder": ("encoder", dict(), 200, [0, 4, 744, 748, 752, 796], [0, 31]),
     "mixed": ("mixed", dict(), 400, None, [0, 1, 2, 3]),
     "voxtral": ("voxtral", dict(), 8200, [0, 8191, 8192, 8193, 8199], [0, 15]),
+    # the most streams a handle takes (RKV_MAX_STREAMS)
+    "max_streams": ("qwen", dict(n_layers=1, n_streams=1024, extra={"window": 40}), 50, [0, 39, 40, 49],
+                    [0, 511, 1023]),
 }
 
 

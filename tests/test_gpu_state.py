@@ -110,3 +110,43 @@ def test_memory_constant_over_steps():
             assert torch.cuda.mem_get_info()[0] == free0
     h.sync_status()
     h.close()
+
+
+def test_decode_attn_layers_matches_per_layer_calls():
+    """rkv_decode_attn_layers (several layers in one launch) gives the per-layer results."""
+    import torch
+
+    import rolling_kv_sliding_rkv_b300 as rkv
+
+    wl = synth.workload("qwen", n_layers=3, n_streams=4, extra={"window": 100})
+    S, L, hq, hkv, d = wl.n_streams, wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    h = rkv.RollingKV(wl.windows().tolist(), wl.start_offsets().tolist(), n_layers=L, n_streams=S, n_q_heads=hq,
+                      n_kv_heads=hkv, head_dim=d, q_per_step=1, scheme=1, rope_theta=wl.rope_theta)
+    q = torch.randn(L, S, 1, hq, d, device="cuda").mul_(0.1).to(torch.bfloat16)
+    k = torch.randn(L, S, 1, hkv, d, device="cuda").mul_(0.1).to(torch.bfloat16)
+    v = torch.randn(L, S, 1, hkv, d, device="cuda").to(torch.bfloat16)
+    out = torch.empty_like(q)
+    lse = torch.empty(L, S, 1, hq, device="cuda")
+    act = list(range(S))
+    for _ in range(120):
+        h.step(act, q, k, v, out, lse)
+    h.begin_step(act)
+    with pytest.raises(rkv.RkvError) as e:
+        h.decode_attn_layers(0, L, q, out, lse)        # before the layers are appended
+    assert e.value.code == rkv.RKV_ERR_STATE
+    for layer in range(L):
+        h.rebase(layer)
+        h.append_rope(layer, k[layer], v[layer])
+    out_a, lse_a = torch.empty_like(out), torch.empty_like(lse)
+    for layer in range(L):
+        h.decode_attn(layer, q[layer], out_a[layer], lse_a[layer])
+    h.decode_attn_layers(0, L, q, out, lse)
+    h.decode_attn_layers(1, 2, q[1:], out[1:], lse[1:])  # a sub-range
+    h.sync_status()
+    assert (out.float() - out_a.float()).abs().max().item() <= 1e-2
+    assert (lse - lse_a).abs().max().item() <= 1e-4
+    for bad in ((-1, 1), (0, L + 1), (2, 2), (0, 0)):
+        with pytest.raises(rkv.RkvError) as e:
+            h.decode_attn_layers(bad[0], bad[1], q, out, lse)
+        assert e.value.code == rkv.RKV_ERR_INVALID_ARG
+    h.close()
