@@ -144,7 +144,7 @@ RKV_API int rkv_required_bytes(const rkv_config* cfg, const int32_t* window,
  *                token, 0 <= P0_s < 2^52
  *   pool_dev     device buffer >= pool_bytes, 256-byte aligned: the K/V pages
  *   state_dev    device buffer >= state_bytes, 256-byte aligned: stream state,
- *                page tables, RoPE tables, split-K partials, status word
+ *                page tables, RoPE tables, status word
  * Initialises state_dev on `stream` and waits for it (synchronous).  Streams
  * start empty (n = 0).  The handle keeps the two pointers; the caller keeps
  * the buffers alive until rkv_destroy. */

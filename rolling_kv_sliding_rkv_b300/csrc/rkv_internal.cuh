@@ -143,13 +143,6 @@ __device__ __forceinline__ float f16_to_f32(uint16_t b) { return __half2float(__
 // largest finite fp16 value after rounding: |x| >= 65520 rounds to infinity
 __device__ __forceinline__ bool fits_f16(float x) { return fabsf(x) < 65520.0f; }
 
-// token held by ring slot `slot` once `evicted` tokens have left a window of W
-__device__ __forceinline__ int64_t token_in_slot(int64_t slot, int64_t evicted, int32_t window) {
-  int64_t d = (slot - evicted % window) % window;
-  if (d < 0) d += window;
-  return evicted + d;
-}
-
 // element offset of (layer, physical page, kv head, offset in page) in a pool region
 __device__ __forceinline__ int64_t pool_offset(const DevView& v, int layer, int page, int kvh, int off) {
   return static_cast<int64_t>(layer) * v.layer_stride +
