@@ -86,6 +86,9 @@ FULL = {
     "encoder": ("encoder", dict(), 200, [0, 4, 744, 748, 752, 796], [0, 31]),
     "mixed": ("mixed", dict(), 400, None, [0, 1, 2, 3]),
     "voxtral": ("voxtral", dict(), 8200, [0, 8191, 8192, 8193, 8199], [0, 15]),
+    # one stream, a long window: each kv head's window splits over a cluster of 8 CTAs
+    "long_window_cluster8": ("tiny", dict(n_streams=1, extra={"window": 2000}), 2050, [0, 999, 1999, 2000, 2049],
+                             [0]),
     # the most streams a handle takes (RKV_MAX_STREAMS)
     "max_streams": ("qwen", dict(n_layers=1, n_streams=1024, extra={"window": 40}), 50, [0, 39, 40, 49],
                     [0, 511, 1023]),
