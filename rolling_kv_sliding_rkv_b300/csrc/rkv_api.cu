@@ -6,7 +6,18 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "rkv_internal.cuh"
+
+namespace {
+// An NVTX range around each call that enqueues work (rkv:<call>), so a profiler can
+// select one step or one call (ncu --nvtx --nvtx-include); free without a tool attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+}  // namespace
 
 struct rkv_handle {
   rkv_config cfg;
@@ -282,6 +293,7 @@ int rkv_create(const rkv_config* cfg, const int32_t* window, const int64_t* star
 }
 
 int rkv_begin_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active, void* stream) {
+  NvtxRange nvtx_range("rkv:begin_step");
   if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
   if (!active_ids || n_active < 1 || n_active > h->cfg.n_streams)
     return fail(h, RKV_ERR_INVALID_ARG, "active_ids must list 1 .. n_streams streams");
@@ -311,6 +323,7 @@ int rkv_begin_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active, v
 }
 
 int rkv_append_rope(rkv_handle* h, int32_t layer, const rkv_bf16* k, const rkv_bf16* v, void* stream) {
+  NvtxRange nvtx_range("rkv:append_rope");
   if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
   if (!h->step_open) return fail(h, RKV_ERR_STATE, "no open step (call rkv_begin_step)");
   if (!check_layer(h, layer)) return fail(h, RKV_ERR_INVALID_ARG, "layer out of range");
@@ -324,6 +337,7 @@ int rkv_append_rope(rkv_handle* h, int32_t layer, const rkv_bf16* k, const rkv_b
 }
 
 int rkv_rebase(rkv_handle* h, int32_t layer, void* stream) {
+  NvtxRange nvtx_range("rkv:rebase");
   if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
   if (!rkv::exact_scheme(h->cfg.scheme)) return fail(h, RKV_ERR_STATE, "rkv_rebase needs an exact re-base scheme");
   if (!h->step_open) return fail(h, RKV_ERR_STATE, "no open step (call rkv_begin_step)");
@@ -336,6 +350,7 @@ int rkv_rebase(rkv_handle* h, int32_t layer, void* stream) {
 }
 
 int rkv_decode_attn(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv_bf16* out, float* lse, void* stream) {
+  NvtxRange nvtx_range("rkv:decode_attn");
   if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
   if (!h->step_open) return fail(h, RKV_ERR_STATE, "no open step (call rkv_begin_step)");
   if (!check_layer(h, layer)) return fail(h, RKV_ERR_INVALID_ARG, "layer out of range");
@@ -352,6 +367,7 @@ int rkv_decode_attn(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv_bf16* o
 
 int rkv_decode_attn_layers(rkv_handle* h, int32_t layer0, int32_t n_layers, const rkv_bf16* q, rkv_bf16* out,
                            float* lse, void* stream) {
+  NvtxRange nvtx_range("rkv:decode_attn_layers");
   if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
   if (!h->step_open) return fail(h, RKV_ERR_STATE, "no open step (call rkv_begin_step)");
   if (n_layers < 1 || layer0 < 0 || layer0 + n_layers > h->cfg.n_layers)
@@ -373,6 +389,7 @@ int rkv_decode_attn_layers(rkv_handle* h, int32_t layer0, int32_t n_layers, cons
 
 int rkv_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active, const rkv_bf16* q, const rkv_bf16* k,
              const rkv_bf16* v, rkv_bf16* out, float* lse, void* stream) {
+  NvtxRange nvtx_range("rkv:step");
   if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
   if (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
       (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
@@ -397,6 +414,7 @@ int rkv_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active, const r
 }
 
 int rkv_reset_stream(rkv_handle* h, int32_t stream_id, int64_t start_offset, void* stream) {
+  NvtxRange nvtx_range("rkv:reset_stream");
   if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
   if (stream_id < 0 || stream_id >= h->cfg.n_streams) return fail(h, RKV_ERR_INVALID_ARG, "stream id out of range");
   if (start_offset < 0 || start_offset >= (int64_t(1) << 52))
@@ -455,6 +473,7 @@ int rkv_stream_snapshot_bytes(const rkv_handle* h, int32_t stream_id, size_t* by
 }
 
 int rkv_save_stream(rkv_handle* h, int32_t stream_id, void* dst, size_t bytes, void* stream) {
+  NvtxRange nvtx_range("rkv:save_stream");
   if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
   if (stream_id < 0 || stream_id >= h->cfg.n_streams || !dst) return fail(h, RKV_ERR_INVALID_ARG, "bad stream id or dst");
   if (bytes < snap_bytes(h, stream_id)) return fail(h, RKV_ERR_CAPACITY, "dst smaller than rkv_stream_snapshot_bytes");
@@ -477,6 +496,7 @@ int rkv_save_stream(rkv_handle* h, int32_t stream_id, void* dst, size_t bytes, v
 }
 
 int rkv_load_stream(rkv_handle* h, int32_t stream_id, const void* src, size_t bytes, void* stream) {
+  NvtxRange nvtx_range("rkv:load_stream");
   if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
   if (stream_id < 0 || stream_id >= h->cfg.n_streams || !src) return fail(h, RKV_ERR_INVALID_ARG, "bad stream id or src");
   if (bytes < snap_bytes(h, stream_id)) return fail(h, RKV_ERR_CAPACITY, "src smaller than rkv_stream_snapshot_bytes");
@@ -582,6 +602,7 @@ int rkv_gen_step_inputs(rkv_handle* h, uint64_t seed, int32_t layer, float scale
 
 int rkv_decode_attn_static(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv_bf16* out, float* lse,
                            void* stream) {
+  NvtxRange nvtx_range("rkv:decode_attn_static");
   if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
   if (!h->step_open) return fail(h, RKV_ERR_STATE, "no open step (call rkv_begin_step)");
   if (!check_layer(h, layer)) return fail(h, RKV_ERR_INVALID_ARG, "layer out of range");
