@@ -10,9 +10,10 @@
 // Data movement.  A stage is 64 consecutive ring slots: K and V page blocks
 // (64 x d 16-bit values each, contiguous in the pool) land in shared memory
 // through bulk asynchronous copies (cp.async.bulk) issued by one producer
-// warp and completed on an mbarrier; three stages are in flight per CTA.
-// The pool's chunk swizzle (rkv_internal.cuh) makes the verbatim copies
-// conflict-free for ldmatrix.
+// warp and completed on an mbarrier; 96 KB of stages are in flight per CTA
+// (three at d = 128, six at d = 64), two CTAs per SM.  The pool's chunk
+// swizzle (rkv_internal.cuh) makes the verbatim copies conflict-free for
+// ldmatrix.
 //
 // Arithmetic.  Per warp, 16 keys at a time on the tensor cores (mma.sync
 // m16n8k16, fp32 accumulate), with keys as the M dimension so the query rows
@@ -31,6 +32,7 @@
 // Splits of one (layer, stream, kv head) form a thread-block cluster and
 // combine their (m, l, O) through distributed shared memory; the scratch
 // form writes per-split partials to global memory for a separate merge.
+// Every sum runs in a fixed order, so outputs are reproducible run to run.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -42,13 +44,11 @@
 namespace rkv {
 namespace {
 
-constexpr int kTeamWarps = 4;             // consumer warps per team: 16 slots of a stage each
-constexpr int kTeams = 1;                 // teams take alternate stages
-constexpr int kCW = kTeamWarps * kTeams;  // consumer warps
+constexpr int kCW = 4;                    // consumer warps: 16 slots of every stage each
 constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
 static_assert(kCW == 4, "the epilogue sums warps 0 + 2 and 1 + 3");
 constexpr int kKS = 64;                   // ring slots per stage
-// shared-memory ring per CTA: 96 KB of K/V stages whatever the head dim (a multiple of kTeams)
+// shared-memory ring per CTA: 96 KB of K/V stages whatever the head dim
 template <int D>
 __host__ __device__ constexpr int stages_for() {
   return 3 * 128 / D;
@@ -167,8 +167,6 @@ __host__ __device__ constexpr int smem_bytes() {
   return stages_for<D>() * 2 * kKS * D * 2 + 2 * (8 * NT) * (D + 8) * 2 + 2 * (8 * NT) * (D + 4) * 4;
 }
 static_assert(smem_bytes<128, 2>() <= 227 * 1024, "shared memory budget");
-static_assert(stages_for<128>() % kTeams == 0 && stages_for<64>() % kTeams == 0,
-              "a ring slot must always be consumed by the same team");
 
 __device__ __forceinline__ float4 ld_dsmem_f32x4(const void* local, uint32_t rank) {
   uint32_t remote;
@@ -274,8 +272,7 @@ __device__ __forceinline__ void q_build(const QPrefetch<D>& pf, float scale_log2
 // Each of the four consumer warps takes 16 of a stage's 64 slots.  A warp
 // moves its K fragments into registers, runs QK^T, moves its V fragments
 // into registers and frees the ring slot before the softmax and PV, so the
-// slot refills while the warp computes.  (The team split generalises this
-// to teams of warps taking alternate stages; one team is used.)
+// slot refills while the warp computes.
 template <int D, int NT, bool ON_READ>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const __grid_constant__ AttnArgs args) {
   constexpr int KSTEPS = D / 16;  // k-steps of QK^T, m-tiles of PV
@@ -310,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
-      mbar_init(smem_u32(&empty_bar[s]), kTeamWarps);
+      mbar_init(smem_u32(&empty_bar[s]), kCW);
     }
     abort_flag = 0;
   }
@@ -398,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
   } else if (!poisoned) {
     // ---------------- consumers
     const int tid = threadIdx.x;
-    const int team = warp / kTeamWarps, wt = warp % kTeamWarps;
+    const int wt = warp;  // this warp's 16 slots of each stage: wt*16 .. wt*16+15
     const int g = lane >> 2, tq = lane & 3;
     // ldmatrix lane roles: matrix mi = lane / 8, row ri = lane % 8
     const int mi = lane >> 3, ri = lane & 7;
@@ -457,8 +454,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
       const int first_new = len - nq;  // window index of the step's first new token
       const int rel_shift = static_cast<int>(dsc.evicted - dsc.rope_base);
       bool aborted = false;
-      // this team's stages of the unit: ring positions k0 + i with (k0 + i) % kTeams == team
-      for (int i = (team - k0 % kTeams + kTeams) % kTeams; i < my_st; i += kTeams) {
+      for (int i = 0; i < my_st; ++i) {
         const int k = k0 + i;
         const int buf = k % kStages;
         // warp-uniform decision: every lane leaves together if any lane gave up
