@@ -150,3 +150,23 @@ def test_decode_attn_layers_matches_per_layer_calls():
             h.decode_attn_layers(bad[0], bad[1], q, out, lse)
         assert e.value.code == rkv.RKV_ERR_INVALID_ARG
     h.close()
+
+
+@pytest.mark.parametrize("scheme", [0, 1, 2])
+def test_key_outside_fp16_range_is_reported(scheme):
+    """A rotated key that cannot be stored in fp16 is reported by rkv_sync_status, once."""
+    import torch
+
+    import rolling_kv_sliding_rkv_b300 as rkv
+    h, q, k, v, out = _small(rkv, scheme=scheme, n_layers=1)
+    h.begin_step([0, 1])
+    k.fill_(1.0e5)          # |R(p) k| >= 1e5 > 65504 in at least one element of every pair
+    if scheme:
+        h.rebase(0)
+    h.append_rope(0, k, v)
+    h.decode_attn(0, q, out)
+    with pytest.raises(rkv.RkvError) as e:
+        h.sync_status()
+    assert e.value.code == rkv.RKV_ERR_DEVICE_RANGE
+    h.sync_status()         # the status word was cleared
+    h.close()
