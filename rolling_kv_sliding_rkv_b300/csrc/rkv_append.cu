@@ -51,8 +51,8 @@ __device__ __forceinline__ void rotate8(const float (&xa)[8], const float (&xb)[
 // One thread per (layer, active stream, new token, kv head, chunk pair).
 __global__ void __launch_bounds__(128) append_rope_kernel(DevView v, int layer0, int n_rows, const uint16_t* __restrict__ k,
                                                           const uint16_t* __restrict__ val, int64_t kv_layer_stride) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int d = v.head_dim, half = d / 2, cpairs = d / 16, hkv = v.n_kv_heads;
   const int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   const int64_t per_layer = static_cast<int64_t>(n_rows) * hkv * cpairs;
@@ -125,8 +125,8 @@ constexpr int kRebaseThreads = 128;
 constexpr int kRebaseRun = 8;  // divides every page size (16 .. 128)
 
 __global__ void __launch_bounds__(kRebaseThreads, 3) rebase_kernel(DevView v, int layer0) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int d = v.head_dim, half = d / 2, cpairs = d / 16;
   const int a = blockIdx.y;
   const int lz = blockIdx.z;

@@ -303,16 +303,12 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
   const int u_first = splits > 1 ? static_cast<int>(blockIdx.x / splits) : static_cast<int>(blockIdx.x);
   const int u_step = splits > 1 ? n_units : static_cast<int>(gridDim.x);
 
-  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), kCW);
     }
     abort_flag = 0;
-  }
-  pdl_wait();  // the step's descriptors, the pages and the queries come from earlier kernels
-  if (threadIdx.x == 0) {
     // after a timed-out wait anywhere, later launches skip their copies (the
     // status word already reports the failure; each CTA ends quickly)
     poisoned_s = *reinterpret_cast<volatile int32_t*>(v.status) == DEV_TIMEOUT;
@@ -334,7 +330,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
       int k = 0;  // stages issued so far (ring position)
       bool stop = false;
       StepDesc dnext;
+      // the descriptors and the page table come from kernels at least two launches back (see
+      // pdl_wait); the pages may come from the immediate predecessor: copies start after the wait
       if (u_first < n_units) dnext = v.desc[unit_of(u_first, n_active, hkv).a];
+      pdl_wait();
+      pdl_launch_dependents();
       for (int u = u_first; u < n_units && !stop; u += u_step) {
         const Unit un = unit_of(u, n_active, hkv);
         const StepDesc dsc = dnext;
@@ -403,11 +403,12 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
     const int vrow = wt * 16 + ri + (mi >> 1) * 8, vchunk = mi & 1;  // V^T as the A operand
     QPrefetch<D> pf;
     StepDesc dnext;
-    if (u_first < n_units) {
+    if (u_first < n_units) {  // queries and descriptors: written two or more launches back
       const Unit un0 = unit_of(u_first, n_active, hkv);
       q_prefetch<D>(args, un0, tid, pf);
       dnext = v.desc[un0.a];
     }
+    pdl_wait();
     int k0 = 0;  // ring position of the unit's first stage
     for (int u = u_first; u < n_units; u += u_step) {
       const Unit un = unit_of(u, n_active, hkv);
@@ -744,8 +745,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
 template <int D>
 __global__ void __launch_bounds__(128) merge_kernel(DevView v, int splits, uint16_t* __restrict__ out,
                                                     float* __restrict__ lse) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int64_t prow0 = static_cast<int64_t>(blockIdx.x) * splits;
   const float* ml = v.part_ml + prow0 * 2;
   float mx = -CUDART_INF_F;

@@ -73,9 +73,12 @@ struct ActiveIds {
 };
 
 // Programmatic dependent launch: the hot-path kernels are launched so that the
-// next kernel in the stream may be scheduled while this one finishes; each
-// kernel lets its dependents launch at once and then waits for its own
-// predecessor to complete (memory visible) before reading anything.  A
+// next kernel in the stream may be scheduled while this one runs.  Each kernel
+// waits for its predecessor to complete (memory visible) and only then lets
+// its own dependents launch, so when any of them starts, every kernel two
+// launches back has completed: a kernel may read, before its own wait, data
+// that only those earlier kernels write (the step descriptors, the page table,
+// the caller's queries), never data its immediate predecessor may write.  A
 // dependent grid launches only after every CTA of its predecessor has
 // started, so waiting CTAs never hold resources the predecessor still needs.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }

@@ -41,8 +41,8 @@ __global__ void init_tables_kernel(DevView v) {
 // rkv.h, rkv_begin_step), record the step descriptor, then cos/sin of the
 // positions of the step's new tokens.
 __global__ void begin_step_kernel(DevView v, ActiveIds ids) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int a = blockIdx.x;
   const int s = ids.id[a];
   __shared__ int64_t pos0;
