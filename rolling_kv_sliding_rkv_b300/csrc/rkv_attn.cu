@@ -766,18 +766,25 @@ __global__ void __launch_bounds__(128) merge_kernel(DevView v, int splits, uint1
 
 template <int D, int NT, bool ON_READ>
 struct Kernel {
+  // The dynamic shared-memory opt-in is per device, so it and the occupancy it gives are
+  // set up once for every device the process uses.
   static int occupancy() {
-    static std::once_flag once;
-    static int occ = 0;
-    std::call_once(once, [] {
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static int occ[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (occ[dev] == 0) {
       cudaFuncSetAttribute(attn_kernel<D, NT, ON_READ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem_bytes<D, NT>());
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_kernel<D, NT, ON_READ>, kThreads,
+      int o = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, attn_kernel<D, NT, ON_READ>, kThreads,
                                                         smem_bytes<D, NT>()) != cudaSuccess)
-        occ = 1;
-      occ = occ < 1 ? 1 : occ;
-    });
-    return occ;
+        o = 1;
+      occ[dev] = o < 1 ? 1 : o;
+    }
+    return occ[dev];
   }
   static cudaError_t launch(const AttnArgs& args, int grid, cudaStream_t st) {
     occupancy();
