@@ -418,6 +418,46 @@ def measure(wl, args, dev, rank, world, timed=True, p0=None, attention=True):
     return out
 
 
+def bench_line(wl, scheme_name, args, world, m, peak, peak_kind, variants=None, flat=None, e2e=None, cpu=None):
+    """The one JSON line of a run: the driver's contract keys plus the roofline of the dominant kernel."""
+    achieved = m["attn_bytes"] / (m["attn_all_ms"] / 1000.0) / 1e9
+    achieved_layer = m["attn_bytes_layer"] / (m["attn_layer_ms"] / 1000.0) / 1e9
+    A = len(step_phases(wl)[0]) if not wl.tick_ms else None
+    line = {"metric": METRIC, "value": m["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": m["ms"] / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": describe(wl, scheme_name),
+                       "streams_per_gpu": A if A is not None else
+                       f"{m['stream_steps'] / args.steps / world:.1f} active per 40 ms tick (of {wl.n_streams})",
+                       "layers": wl.n_layers,
+                       "l2": "per-step working set of KV pages > 126 MB L2; no flush between steps",
+                       "graph": "one CUDA graph per step (per tick phase for mixed clocks), replayed",
+                       "parallelism": "replicas" if world == 1 else f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": profiled_traffic(wl),
+                         "kernel": f"attn_kernel: decode attention over all {wl.n_layers} layers in one "
+                                   "launch (as inside the timed step)",
+                         "algorithmic_bytes_per_launch": m["attn_bytes"],
+                         "avg_launch_us": m["attn_all_ms"] * 1000.0,
+                         "streams_in_launch": m["attn_streams"],
+                         "peak_kind": f"{peak_kind} (hbm_gbs, STREAM-style copy, burst)"},
+            "decode_attn_gbs": achieved,
+            "decode_attn_per_layer_launch": {"achieved_gbs": achieved_layer, "frac": achieved_layer / peak,
+                                             "avg_launch_us": m["attn_layer_ms"] * 1000.0,
+                                             "algorithmic_bytes_per_launch": m["attn_bytes_layer"]},
+            "gpu_launches": m["launches"],
+            "clocks": m.get("clocks")}
+    if variants:
+        line["schemes"] = variants
+    if flat is not None:
+        line["flatness"] = flat
+    if e2e is not None:
+        line["e2e"] = e2e
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    return line
+
+
 def run_ours(args):
     import torch
 
@@ -439,8 +479,6 @@ def run_ours(args):
     m = measure(wl, args, dev, rank, world)
     h = m.pop("h")
     peak, peak_kind = measured_peak()
-    achieved = m["attn_bytes"] / (m["attn_all_ms"] / 1000.0) / 1e9
-    achieved_layer = m["attn_bytes_layer"] / (m["attn_layer_ms"] / 1000.0) / 1e9
 
     e2e = None
     if not args.no_e2e:
@@ -478,39 +516,7 @@ def run_ours(args):
         cpu = oracle_timing(wl, args.cpu_seconds)
 
     if rank == 0:
-        A = len(step_phases(wl)[0]) if not wl.tick_ms else None
-        line = {"metric": METRIC, "value": m["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": m["ms"] / args.steps, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": describe(wl, scheme_name),
-                           "streams_per_gpu": A if A is not None else
-                           f"{m['stream_steps'] / args.steps:.1f} active per 40 ms tick (of {wl.n_streams})",
-                           "layers": wl.n_layers,
-                           "l2": "per-step working set of KV pages > 126 MB L2; no flush between steps",
-                           "graph": "one CUDA graph per step (per tick phase for mixed clocks), replayed",
-                           "parallelism": "replicas" if world == 1 else f"replicas x{world}"},
-                "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                             "frac": achieved / peak, "traffic": profiled_traffic(wl),
-                             "kernel": f"attn_kernel: decode attention over all {wl.n_layers} layers in one "
-                                       "launch (as inside the timed step)",
-                             "algorithmic_bytes_per_launch": m["attn_bytes"],
-                             "avg_launch_us": m["attn_all_ms"] * 1000.0,
-                             "streams_in_launch": m["attn_streams"],
-                             "peak_kind": f"{peak_kind} (hbm_gbs, STREAM-style copy, burst)"},
-                "decode_attn_gbs": achieved,
-                "decode_attn_per_layer_launch": {"achieved_gbs": achieved_layer, "frac": achieved_layer / peak,
-                                                 "avg_launch_us": m["attn_layer_ms"] * 1000.0,
-                                                 "algorithmic_bytes_per_launch": m["attn_bytes_layer"]},
-                "gpu_launches": m["launches"],
-                "clocks": m["clocks"]}
-        if variants:
-            line["schemes"] = variants
-        if flat is not None:
-            line["flatness"] = flat
-        if e2e is not None:
-            line["e2e"] = e2e
-        if cpu is not None:
-            line["cpu_baseline"] = cpu
+        line = bench_line(wl, scheme_name, args, world, m, peak, peak_kind, variants, flat, e2e, cpu)
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -1,0 +1,66 @@
+"""bench.py's JSON line: the keys and arithmetic the benchmark driver relies on (no GPU needed)."""
+import json
+import os
+import subprocess
+import sys
+import types
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import synth  # noqa: E402
+
+REQUIRED = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+            "vs_baseline", "dtype", "data", "config", "roofline", "gpu_launches", "clocks")
+
+
+def _fake_measurement(wl, steps, ms_per_step, attn_us):
+    lens = [int(w) for w in wl.windows()]
+    per_layer = bench.algorithmic_attn_bytes(wl, lens)
+    return {"value": wl.n_streams * steps / (ms_per_step * steps / 1000.0), "ms": ms_per_step * steps,
+            "stream_steps": wl.n_streams * steps, "launches": 4 * steps, "attn_all_ms": attn_us / 1000.0,
+            "attn_layer_ms": attn_us / 1000.0 / wl.n_layers * 3.0, "attn_bytes_layer": per_layer,
+            "attn_bytes": per_layer * wl.n_layers, "attn_streams": wl.n_streams,
+            "clocks": {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0, "reasons": []}}
+
+
+def test_line_has_the_contract_keys_and_the_roofline_arithmetic():
+    wl = synth.workload("qwen")
+    args = types.SimpleNamespace(steps=100, warmup=20)
+    m = _fake_measurement(wl, 100, 0.343, 148.0)
+    e2e = {"value": 1.0, "unit": bench.UNIT, "h2d_bytes_per_step": 1, "d2h_bytes_per_step": 1}
+    cpu = {"value": 1.0, "unit": bench.UNIT, "cores": 16, "kind": "oracle", "sample": "x"}
+    line = bench.bench_line(wl, "exact re-base", args, 1, m, 6492.7, "measured", e2e=e2e, cpu=cpu)
+    json.dumps(line)                                   # serialisable
+    for key in REQUIRED:
+        assert key in line, key
+    assert line["metric"] == json.load(open(os.path.join(ROOT, "BASELINE.json")))["metric"]
+    assert line["unit"] == "stream-steps/s" and line["higher_is_better"] is True and line["scaling"] == "weak"
+    assert line["ms_per_step"] == pytest.approx(0.343)
+    assert line["value"] == pytest.approx(64 / 0.343e-3)
+    r = line["roofline"]
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 6492.7
+    # Qwen-shaped layer: 64 streams x 392256 algorithmic bytes; 36 layers per launch
+    assert r["algorithmic_bytes_per_launch"] == 36 * 64 * 392256
+    assert r["achieved"] == pytest.approx(36 * 64 * 392256 / 148e-6 / 1e9)
+    assert r["frac"] == pytest.approx(r["achieved"] / 6492.7)
+    assert set(line["e2e"]) >= {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"}
+    assert set(line["cpu_baseline"]) >= {"value", "unit", "cores", "kind", "sample"}
+
+
+def test_algorithmic_bytes_of_one_stream_layer_step():
+    # K + V of the window, q in, out, lse: 2*375*2*128*2 + 16*128*2*2 + 16*4
+    wl = synth.workload("qwen")
+    assert bench.algorithmic_attn_bytes(wl, [375]) == 392256
+
+
+def test_reference_arm_prints_one_line():
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--steps", "1",
+                          "--warmup", "0"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "stream-steps/s"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
