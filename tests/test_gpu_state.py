@@ -170,3 +170,29 @@ def test_key_outside_fp16_range_is_reported(scheme):
     assert e.value.code == rkv.RKV_ERR_DEVICE_RANGE
     h.sync_status()         # the status word was cleared
     h.close()
+
+
+def test_device_memory_is_constant_over_steps():
+    """Memory does not grow with the stream's length: no allocation after create (T8)."""
+    import torch
+
+    import rolling_kv_sliding_rkv_b300 as rkv
+    wl = synth.workload("qwen", n_layers=2, n_streams=8, extra={"window": 64})
+    S, L, hq, hkv, d = wl.n_streams, wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    h = rkv.RollingKV(wl.windows().tolist(), wl.start_offsets().tolist(), n_layers=L, n_streams=S, n_q_heads=hq,
+                      n_kv_heads=hkv, head_dim=d, q_per_step=1, scheme=1, rope_theta=wl.rope_theta)
+    q = torch.zeros(L, S, 1, hq, d, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(L, S, 1, hkv, d, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    act = list(range(S))
+    for _ in range(5):
+        h.step(act, q, k, k, out)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(600):            # ~9 windows
+        h.step(act, q, k, k, out)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert h.stream_state(0)["n"] == 605
+    h.sync_status()
+    h.close()
