@@ -169,11 +169,19 @@ __global__ void __launch_bounds__(kRebaseThreads, 3) rebase_kernel(DevView v, in
     }
   }
   // (cos, sin)(omega_i) of this thread's eight frequencies: table row 1
-  float step[16], cs[16];
-  if (v.t_rows > 1) {  // (a window of one key keeps nothing to re-base)
+  // Coefficients in packed pairs of adjacent frequencies (i, i+1): c2[p] = (cos, cos), s2[p] =
+  // (sin, sin) of frequencies 8cp + 2p, 8cp + 2p + 1; the rotation and the recurrence run on
+  // paired fp32 FMAs (each lane rounds exactly as a scalar FMA).
+  float2 c1[4], s1[4], ns1[4], c2[4], s2[4];
+  if (v.t_rows > 1) {  // (cos, sin)(omega_i): table row 1 (a window of one key keeps nothing to re-base)
     const float4* t1 = reinterpret_cast<const float4*>(v.rope_table + (static_cast<int64_t>(1) * half + cp * 8) * 2);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) reinterpret_cast<float4*>(step)[q] = t1[q];
+    for (int q = 0; q < 4; ++q) {
+      const float4 t = t1[q];
+      c1[q] = make_float2(t.x, t.z);
+      s1[q] = make_float2(t.y, t.w);
+      ns1[q] = make_float2(-t.y, -t.w);
+    }
   }
   int rel_cur = -2;
 #pragma unroll
@@ -181,27 +189,39 @@ __global__ void __launch_bounds__(kRebaseThreads, 3) rebase_kernel(DevView v, in
     if (!live[j]) continue;
     if (rel[j] == rel_cur + 1) {  // advance by one position: (c, s) <- (c, s) * (cos, sin)(omega)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float c = cs[2 * i], s = cs[2 * i + 1], c1 = step[2 * i], s1 = step[2 * i + 1];
-        cs[2 * i] = c * c1 - s * s1;
-        cs[2 * i + 1] = s * c1 + c * s1;
+      for (int q = 0; q < 4; ++q) {
+        const float2 c = c2[q], sn = s2[q];
+        c2[q] = __ffma2_rn(c, c1[q], __fmul2_rn(sn, ns1[q]));
+        s2[q] = __ffma2_rn(sn, c1[q], __fmul2_rn(c, s1[q]));
       }
     } else {  // first live slot of the run, or the ring wrapped: read the row
-      const float4* t = reinterpret_cast<const float4*>(v.rope_table + (static_cast<int64_t>(rel[j]) * half + cp * 8) * 2);
+      const float4* t4 = reinterpret_cast<const float4*>(v.rope_table + (static_cast<int64_t>(rel[j]) * half + cp * 8) * 2);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) reinterpret_cast<float4*>(cs)[q] = t[q];
+      for (int q = 0; q < 4; ++q) {
+        const float4 t = t4[q];
+        c2[q] = make_float2(t.x, t.z);
+        s2[q] = make_float2(t.y, t.w);
+      }
     }
     rel_cur = rel[j];
-    float xa[8], xb[8];
-    unpack8(ka[j], xa);
-    unpack8(kb[j], xb);
-    uint4 ya, yb;
-    bool fits;
-    rotate8(xa, xb, cs, &ya, &yb, &fits);
+    // (a, b) -> (a cos - b sin, a sin + b cos) on pairs of adjacent elements
+    const uint32_t wa[4] = {ka[j].x, ka[j].y, ka[j].z, ka[j].w}, wb[4] = {kb[j].x, kb[j].y, kb[j].z, kb[j].w};
+    uint32_t ya[4], yb[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 xa = make_float2(__uint_as_float(wa[q] << 16), __uint_as_float(wa[q] & 0xFFFF0000u));
+      const float2 nxb = make_float2(-__uint_as_float(wb[q] << 16), -__uint_as_float(wb[q] & 0xFFFF0000u));
+      const float2 xb = make_float2(-nxb.x, -nxb.y);
+      const float2 ra = __ffma2_rn(nxb, s2[q], __fmul2_rn(xa, c2[q]));
+      const float2 rb = __ffma2_rn(xa, s2[q], __fmul2_rn(xb, c2[q]));
+      const __half2 ha = __floats2half2_rn(ra.x, ra.y), hb = __floats2half2_rn(rb.x, rb.y);
+      ya[q] = *reinterpret_cast<const uint32_t*>(&ha);
+      yb[q] = *reinterpret_cast<const uint32_t*>(&hb);
+    }
     const int off = (slot0 + j) % v.page_size;
     const int64_t o = row0 + static_cast<int64_t>(j) * d;
-    *reinterpret_cast<uint4*>(v.k_rot + o + swizzle_chunk(cp, off) * 8) = ya;
-    *reinterpret_cast<uint4*>(v.k_rot + o + swizzle_chunk(cp + cpairs, off) * 8) = yb;
+    *reinterpret_cast<uint4*>(v.k_rot + o + swizzle_chunk(cp, off) * 8) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+    *reinterpret_cast<uint4*>(v.k_rot + o + swizzle_chunk(cp + cpairs, off) * 8) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
   }
 }
 
