@@ -25,9 +25,10 @@
 //       into the B operand by an 8x8 transpose (movmatrix);
 //   O^T[d][8 rows] += V^T[d][16 keys] . P^T  (V read with ldmatrix.trans).
 // Stored keys are fp16 (offset-only and exact re-base schemes).  In the
-// rotate-on-read scheme the pool holds pre-RoPE bf16 keys and every key is
-// rotated here by R(j - rope_base) in fp32 (cos/sin from the window-relative
-// table), then rounded once to fp16: the exact re-base with no stored copy.
+// rotate-on-read scheme the pool holds pre-RoPE bf16 keys and each consumer
+// warp turns its slots of a landed K stage, in shared memory, into the keys
+// rotated by R(j - rope_base) in fp32 (cos/sin from the window-relative
+// table), rounded once to fp16: the exact re-base with no stored copy.
 //
 // Splits of one (layer, stream, kv head) form a thread-block cluster and
 // combine their (m, l, O) through distributed shared memory; the scratch
@@ -149,18 +150,6 @@ __device__ __forceinline__ float ld_dsmem_f32(const void* local, uint32_t rank) 
   return x;
 }
 
-// Rotate the pairs held by a (first half) and b (second half) of one key's
-// bf16 A-fragment registers: x = (lo, hi) at frequencies (i, i + 1).
-// cs = (cos_i, sin_i, cos_{i+1}, sin_{i+1}).  Results in fp16.
-__device__ __forceinline__ void rotate_pair_regs(uint32_t& a, uint32_t& b, const float4 cs) {
-  const float xa0 = __uint_as_float(a << 16), xa1 = __uint_as_float(a & 0xFFFF0000u);
-  const float xb0 = __uint_as_float(b << 16), xb1 = __uint_as_float(b & 0xFFFF0000u);
-  const float ya0 = xa0 * cs.x - xb0 * cs.y, yb0 = xa0 * cs.y + xb0 * cs.x;
-  const float ya1 = xa1 * cs.z - xb1 * cs.w, yb1 = xa1 * cs.w + xb1 * cs.z;
-  a = pack_f16(ya0, ya1);
-  b = pack_f16(yb0, yb1);
-}
-
 template <int D, int NT>
 __host__ __device__ constexpr int smem_bytes() {
   // stages (K | V), query tiles hi + lo, two fp32 output tiles
@@ -261,6 +250,74 @@ __device__ __forceinline__ void q_build(const QPrefetch<D>& pf, float scale_log2
   *reinterpret_cast<uint4*>(qh_s + r * QSTR + H + cp * 8) = make_uint4(hb[0], hb[1], hb[2], hb[3]);
   *reinterpret_cast<uint4*>(ql_s + r * QSTR + cp * 8) = make_uint4(la[0], la[1], la[2], la[3]);
   *reinterpret_cast<uint4*>(ql_s + r * QSTR + H + cp * 8) = make_uint4(lb[0], lb[1], lb[2], lb[3]);
+}
+
+// ---------------- rotate-on-read
+//
+// In the rotate-on-read scheme the pool holds pre-RoPE bf16 keys.  Each
+// consumer warp turns its 16 slots of a landed K stage, in place in shared
+// memory, into the keys rotated by R(j - rope_base) (window-relative
+// positions, the exact scheme's table) and rounded once to fp16, then runs
+// exactly as over stored rotated keys.
+//
+// Lane layout: a lane owns the frequency pair (2p, 2p + 1) of one key row,
+// i.e. one 32-bit word in each half of the row (D/4 lanes per row, 128/D rows
+// at a time); at D = 128 the 32 words of one half are one conflict-free
+// 128-byte access.  Ring slots hold consecutive window positions except where
+// the ring wraps, so along a run of 8 slots the next slot's (cos, sin) follow
+// from the current ones by one complex multiplication with (cos, sin)(omega)
+// (at most 7 in a row, as in the re-base kernel: ~1e-6 relative, far below
+// the fp16 rounding).  The table row of each run's first slot is loaded
+// before the stage is awaited; the row of the wrap slot (window index 0) once
+// per unit.
+
+// table row (window index + rel_shift) of ring slot `slot`; clamped, since slots
+// past the window hold nothing the consumers use
+__device__ __forceinline__ int rot_row(int slot, int ev_mod, int W, int rel_shift, int t_rows) {
+  int w = slot - ev_mod;
+  if (w < 0) w += W;
+  return min(max(w + rel_shift, 0), t_rows - 1);
+}
+
+// Rotate this lane's words of the 8 rows r0 .. r0+7 of a K block (r0 % 8 == 0, so row r0 + t
+// has swizzle t).  WRAP: the ring wraps at row r0 + t_wrap, whose (cos, sin) is `wrap`.
+template <int D, bool WRAP>
+__device__ __forceinline__ void rot_run(uint8_t* kblk, int r0, int pp, float4 row, float4 wrap, int t_wrap,
+                                        float2 c1, float2 s1, float2 ns1) {
+  uint8_t* p = kblk + r0 * D * 2;
+  uint32_t a[8], b[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    // element 2p of the row sits in chunk p/4 (swizzled to p/4 ^ t), word p%4; its partner
+    // d/2 later in chunk p/4 + d/16
+    const int oa = ((pp * 4) ^ (t << 4)) + t * D * 2;
+    const int ob = oa + (D == 128 ? 128 : ((t & 4) ? -64 : 64));
+    a[t] = *reinterpret_cast<const uint32_t*>(p + oa);
+    b[t] = *reinterpret_cast<const uint32_t*>(p + ob);
+  }
+  float2 c = make_float2(row.x, row.z), s = make_float2(row.y, row.w);
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    if (t > 0) {
+      if (WRAP && t == t_wrap) {
+        c = make_float2(wrap.x, wrap.z);
+        s = make_float2(wrap.y, wrap.w);
+      } else {  // one position on: (c, s) <- (c, s) * (cos, sin)(omega)
+        const float2 cn = __ffma2_rn(c, c1, __fmul2_rn(s, ns1));
+        s = __ffma2_rn(s, c1, __fmul2_rn(c, s1));
+        c = cn;
+      }
+    }
+    const float2 xa = make_float2(__uint_as_float(a[t] << 16), __uint_as_float(a[t] & 0xFFFF0000u));
+    const float2 xb = make_float2(__uint_as_float(b[t] << 16), __uint_as_float(b[t] & 0xFFFF0000u));
+    const float2 nxb = make_float2(-xb.x, -xb.y);
+    const float2 ra = __ffma2_rn(nxb, s, __fmul2_rn(xa, c));  // a cos - b sin
+    const float2 rb = __ffma2_rn(xa, s, __fmul2_rn(xb, c));   // a sin + b cos
+    const int oa = ((pp * 4) ^ (t << 4)) + t * D * 2;
+    const int ob = oa + (D == 128 ? 128 : ((t & 4) ? -64 : 64));
+    *reinterpret_cast<uint32_t*>(p + oa) = pack_f16(ra.x, ra.y);
+    *reinterpret_cast<uint32_t*>(p + ob) = pack_f16(rb.x, rb.y);
+  }
 }
 
 // Two CTAs per SM.  Without a cluster the CTA walks units u = blockIdx.x,
@@ -401,6 +458,15 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
     const int mi = lane >> 3, ri = lane & 7;
     const int krow = wt * 16 + ri + (mi & 1) * 8, kchunk = mi >> 1;  // K as the A operand
     const int vrow = wt * 16 + ri + (mi >> 1) * 8, vchunk = mi & 1;  // V^T as the A operand
+    // rotating on read: this lane's frequency pair (lane % (d/4)) in the table; (cos, sin)(omega)
+    const float4* rtab = reinterpret_cast<const float4*>(v.rope_table) + lane % (D / 4);
+    float2 rc1 = make_float2(1.f, 1.f), rs1 = make_float2(0.f, 0.f), rns1 = rs1;
+    if (ON_READ && v.t_rows > 1) {
+      const float4 t = __ldg(rtab + D / 4);
+      rc1 = make_float2(t.x, t.z);
+      rs1 = make_float2(t.y, t.w);
+      rns1 = make_float2(-t.y, -t.w);
+    }
     QPrefetch<D> pf;
     StepDesc dnext;
     if (u_first < n_units) {  // queries and descriptors: written two or more launches back
@@ -454,11 +520,22 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
       const int ev_mod = static_cast<int>(dsc.evicted % W);
       const int first_new = len - nq;  // window index of the step's first new token
       const int rel_shift = static_cast<int>(dsc.evicted - dsc.rope_base);
+      float4 rwrap = make_float4(1.f, 0.f, 1.f, 0.f);  // (cos, sin) at window index 0
+      if constexpr (ON_READ) rwrap = __ldg(rtab + static_cast<int64_t>(min(max(rel_shift, 0), v.t_rows - 1)) * (D / 4));
       bool aborted = false;
       for (int i = 0; i < my_st; ++i) {
         const int k = k0 + i;
         const int buf = k % kStages;
         // warp-uniform decision: every lane leaves together if any lane gave up
+        // rotating on read: the table rows of this warp's runs, loaded while the stage lands
+        float4 rrow[ON_READ ? 2 / (128 / D) : 1];
+        if constexpr (ON_READ) {
+#pragma unroll
+          for (int j = 0; j < 2 / (128 / D); ++j) {
+            const int run = 2 * wt + (D == 128 ? j : lane / 16);
+            rrow[j] = __ldg(rtab + static_cast<int64_t>(rot_row((st0 + i) * kKS + run * 8, ev_mod, W, rel_shift, v.t_rows)) * (D / 4));
+          }
+        }
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[buf]), (k / kStages) & 1))) {
           if (lane == 0) {
             record_error(v.status, DEV_TIMEOUT, 23, k);
@@ -484,29 +561,25 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
           if (w < 0) w += W;
           widx[hk] = slot < nslots ? w : -1;
         }
+        if constexpr (ON_READ) {
+          // rotate this warp's 16 pre-RoPE keys in place (two runs of 8 slots), then let the
+          // warp's lanes see each other's words
+          uint8_t* kblk = reinterpret_cast<uint8_t*>(kv_s + buf * 2 * STAGE_ELEMS);
+#pragma unroll
+          for (int j = 0; j < 2 / (128 / D); ++j) {
+            const int run = 2 * wt + (D == 128 ? j : lane / 16);
+            const int tw = ev_mod - ((st0 + i) * kKS + run * 8);
+            if (tw > 0 && tw < 8)
+              rot_run<D, true>(kblk, run * 8, lane % (D / 4), rrow[j], rwrap, tw, rc1, rs1, rns1);
+            else
+              rot_run<D, false>(kblk, run * 8, lane % (D / 4), rrow[j], rwrap, 0, rc1, rs1, rns1);
+          }
+          __syncwarp();
+        }
         // K fragments of this warp's 16 slots (the A operand, one per k-step)
         uint32_t kf[KSTEPS][4];
 #pragma unroll
         for (int ks = 0; ks < KSTEPS; ++ks) ldsm_x4(kb + krow * D * 2 + (swizzle_chunk(2 * ks + kchunk, ri) << 4), kf[ks]);
-        if constexpr (ON_READ) {
-          // rotate each pre-RoPE key by its window-relative position: pairs (i, i + d/2) sit in
-          // k-steps ks and ks + d/32 at the same register positions
-          const float4* tab = reinterpret_cast<const float4*>(v.rope_table);
-          int rel[2];
-#pragma unroll
-          for (int hk = 0; hk < 2; ++hk) rel[hk] = widx[hk] < 0 ? 0 : min(widx[hk] + rel_shift, v.t_rows - 1);
-#pragma unroll
-          for (int ks = 0; ks < KSTEPS / 2; ++ks) {
-            const int i0 = ks * 16 + 2 * tq;  // this thread's frequencies i0, i0+1 and i0+8, i0+9
-#pragma unroll
-            for (int hk = 0; hk < 2; ++hk) {
-              const float4 c0 = __ldg(tab + (static_cast<int64_t>(rel[hk]) * (D / 2) + i0) / 2);
-              const float4 c1 = __ldg(tab + (static_cast<int64_t>(rel[hk]) * (D / 2) + i0 + 8) / 2);
-              rotate_pair_regs(kf[ks][hk], kf[ks + KSTEPS / 2][hk], c0);
-              rotate_pair_regs(kf[ks][2 + hk], kf[ks + KSTEPS / 2][2 + hk], c1);
-            }
-          }
-        }
         float sh[NT][4], sl[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -523,6 +596,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
         uint32_t vf[KSTEPS][4];
 #pragma unroll
         for (int mt = 0; mt < KSTEPS; ++mt) ldsm_x4_t(vb + vrow * D * 2 + (swizzle_chunk(2 * mt + vchunk, ri) << 4), vf[mt]);
+        if constexpr (ON_READ) fence_proxy_async_smem();  // the rotated keys precede the slot's next bulk copy
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty_bar[buf]));
         // online softmax; C layout: e = 0,1 key g rows 2tq, 2tq+1; e = 2,3 key g+8.  A chunk
