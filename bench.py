@@ -37,8 +37,8 @@ SCHEMES = {"offset": 0, "exact": 1, "on-read": 2}
 # DRAM traffic (read + write bytes) of one decode-attention launch, from the ncu launch list
 # committed under profiles/ (launch_list_qwen36x64_exact.md), valid only while the attention
 # kernel's source is the one that was profiled: a different source hash reports null.
-TRAFFIC = [{"workload": "qwen", "layers": 36, "schemes": (0, 1), "attn_src_sha256_16": "28d7655c4247ac4b",
-            "bytes_per_launch": 915.6e6 + 9.0e6}]
+TRAFFIC = [{"workload": "qwen", "layers": 36, "schemes": (0, 1), "attn_src_sha256_16": "ad45a807efe036c1",
+            "bytes_per_launch": 915.6e6 + 9.1e6}]
 SCHEME_NAMES = {0: "offset-only", 1: "exact re-base", 2: "exact re-base applied on read"}
 
 
@@ -81,6 +81,31 @@ def algorithmic_attn_bytes(wl, lens):
     Q, hq, hkv, d = wl.q_per_step, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
     kv = sum(2 * int(n) * hkv * d * 2 for n in lens)
     return kv + len(lens) * (Q * hq * d * 2 * 2 + Q * hq * 4)
+
+
+def algorithmic_rebase_bytes(wl, act):
+    """Bytes one exact re-base step moves: every retained key of every active stream, layer and
+    kv head read as its pre-RoPE copy and written rotated (windows full: W - 1 retained keys)."""
+    windows = wl.windows()
+    return sum(wl.n_layers * wl.n_kv_heads * (int(windows[s]) - 1) * wl.head_dim * 2 * 2 for s in act)
+
+
+def rebase_in_step(wl, m, variants, steps, peak):
+    """The exact re-base's share of the step, from two CUDA-event timings of this run: the exact
+    scheme's step minus the offset-only step, which makes the same launches without the re-base."""
+    off = variants.get(SCHEME_NAMES[0]) if variants else None
+    if wl.scheme != 1 or off is None:
+        return None
+    plan = m["plan"]
+    per_step_bytes = sum(algorithmic_rebase_bytes(wl, plan[i % len(plan)]) for i in range(steps)) / steps
+    us = (m["ms"] / steps - off["ms_per_step"]) * 1000.0
+    if us <= 0:
+        return None
+    gbs = per_step_bytes / (us * 1e-6) / 1e9
+    return {"kernel": f"rebase_kernel: exact re-base over all {wl.n_layers} layers in one launch",
+            "us_per_step": us, "algorithmic_bytes_per_step": per_step_bytes, "achieved_gbs": gbs,
+            "frac": gbs / peak, "how": "exact re-base step minus offset-only step (the same launches "
+                                       "without the re-base), both timed with CUDA events in this run"}
 
 
 class ClockSampler:
@@ -449,6 +474,9 @@ def bench_line(wl, scheme_name, args, world, m, peak, peak_kind, variants=None, 
             "clocks": m.get("clocks")}
     if variants:
         line["schemes"] = variants
+        rb = rebase_in_step(wl, m, variants, args.steps, peak)
+        if rb is not None:
+            line["rebase_in_step"] = rb
     if flat is not None:
         line["flatness"] = flat
     if e2e is not None:

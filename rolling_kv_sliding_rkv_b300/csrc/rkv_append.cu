@@ -124,7 +124,9 @@ __global__ void __launch_bounds__(128) append_rope_kernel(DevView v, int layer0,
 constexpr int kRebaseThreads = 128;
 constexpr int kRebaseRun = 8;  // divides every page size (16 .. 128)
 
-__global__ void __launch_bounds__(kRebaseThreads, 3) rebase_kernel(DevView v, int layer0) {
+// Four blocks per SM (at most 128 registers a thread): more runs' loads in flight while other
+// runs compute.
+__global__ void __launch_bounds__(kRebaseThreads, 4) rebase_kernel(DevView v, int layer0) {
   pdl_wait();
   pdl_launch_dependents();
   const int d = v.head_dim, half = d / 2, cpairs = d / 16;

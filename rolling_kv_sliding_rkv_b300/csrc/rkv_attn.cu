@@ -264,12 +264,15 @@ __device__ __forceinline__ void q_build(const QPrefetch<D>& pf, float scale_log2
 // i.e. one 32-bit word in each half of the row (D/4 lanes per row, 128/D rows
 // at a time); at D = 128 the 32 words of one half are one conflict-free
 // 128-byte access.  Ring slots hold consecutive window positions except where
-// the ring wraps, so along a run of 8 slots the next slot's (cos, sin) follow
-// from the current ones by one complex multiplication with (cos, sin)(omega)
-// (at most 7 in a row, as in the re-base kernel: ~1e-6 relative, far below
-// the fp16 rounding).  The table row of each run's first slot is loaded
-// before the stage is awaited; the row of the wrap slot (window index 0) once
-// per unit.
+// the ring wraps, so along a run of 8 slots the (cos, sin) of the following
+// slots come from the run's first row by a recurrence: one complex
+// multiplication with (cos, sin)(omega) for the second slot, then the
+// three-term form y(n+1) = 2 cos(omega) y(n) - y(n-1) (one paired FMA for the
+// cosines, one for the sines).  An error made k positions before the end of a
+// run grows at most k-fold (|sin(k w) / sin(w)| <= k), so after at most 7 steps
+// the pair is within ~2e-6 of the table's, far below the fp16 rounding of the
+// rotated key.  The table row of each run's first slot is loaded before the
+// stage is awaited; the row of the wrap slot (window index 0) once per unit.
 
 // table row (window index + rel_shift) of ring slot `slot`; clamped, since slots
 // past the window hold nothing the consumers use
@@ -296,17 +299,26 @@ __device__ __forceinline__ void rot_run(uint8_t* kblk, int r0, int pp, float4 ro
     b[t] = *reinterpret_cast<const uint32_t*>(p + ob);
   }
   float2 c = make_float2(row.x, row.z), s = make_float2(row.y, row.w);
+  float2 cp = c, sp = s;                                   // one position back
+  const float2 tc1 = make_float2(2.f * c1.x, 2.f * c1.y);  // 2 cos(omega), exact
 #pragma unroll
   for (int t = 0; t < 8; ++t) {
     if (t > 0) {
+      float2 cn, sn;
       if (WRAP && t == t_wrap) {
-        c = make_float2(wrap.x, wrap.z);
-        s = make_float2(wrap.y, wrap.w);
-      } else {  // one position on: (c, s) <- (c, s) * (cos, sin)(omega)
-        const float2 cn = __ffma2_rn(c, c1, __fmul2_rn(s, ns1));
-        s = __ffma2_rn(s, c1, __fmul2_rn(c, s1));
-        c = cn;
+        cn = make_float2(wrap.x, wrap.z);
+        sn = make_float2(wrap.y, wrap.w);
+      } else if (t == 1 || (WRAP && t == t_wrap + 1)) {  // (c, s) * (cos, sin)(omega)
+        cn = __ffma2_rn(c, c1, __fmul2_rn(s, ns1));
+        sn = __ffma2_rn(s, c1, __fmul2_rn(c, s1));
+      } else {  // 2 cos(omega) y(n) - y(n-1)
+        cn = __ffma2_rn(tc1, c, make_float2(-cp.x, -cp.y));
+        sn = __ffma2_rn(tc1, s, make_float2(-sp.x, -sp.y));
       }
+      cp = c;
+      sp = s;
+      c = cn;
+      s = sn;
     }
     const float2 xa = make_float2(__uint_as_float(a[t] << 16), __uint_as_float(a[t] & 0xFFFF0000u));
     const float2 xb = make_float2(__uint_as_float(b[t] << 16), __uint_as_float(b[t] & 0xFFFF0000u));

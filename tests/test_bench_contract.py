@@ -57,6 +57,27 @@ def test_algorithmic_bytes_of_one_stream_layer_step():
     assert bench.algorithmic_attn_bytes(wl, [375]) == 392256
 
 
+def test_rebase_share_of_the_step():
+    # exact step 0.336 ms, offset-only step 0.154 ms: the re-base costs 182 us per step and moves
+    # 64 streams x 36 layers x 2 kv heads x 374 retained keys x 128 x 2 bytes, read and written
+    wl = synth.workload("qwen")
+    args = types.SimpleNamespace(steps=100, warmup=20)
+    m = _fake_measurement(wl, 100, 0.336, 145.0)
+    m["plan"] = [list(range(wl.n_streams))]
+    variants = {"offset-only": {"value": 1.0, "unit": bench.UNIT, "ms_per_step": 0.154}}
+    line = bench.bench_line(wl, "exact re-base", args, 1, m, 6492.7, "measured", variants=variants)
+    rb = line["rebase_in_step"]
+    assert rb["algorithmic_bytes_per_step"] == 64 * 36 * 2 * 374 * 128 * 2 * 2
+    assert rb["us_per_step"] == pytest.approx(182.0)
+    assert rb["achieved_gbs"] == pytest.approx(64 * 36 * 2 * 374 * 128 * 4 / 182e-6 / 1e9)
+    assert rb["frac"] == pytest.approx(rb["achieved_gbs"] / 6492.7)
+    # no offset-only timing, or another scheme: no derived figure
+    assert "rebase_in_step" not in bench.bench_line(wl, "exact re-base", args, 1, m, 6492.7, "measured",
+                                                     variants={"x": {"ms_per_step": 0.1}})
+    off = synth.workload("qwen", scheme=0)
+    assert bench.rebase_in_step(off, m, variants, 100, 6492.7) is None
+
+
 def test_reference_arm_prints_one_line():
     out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--steps", "1",
                           "--warmup", "0"], cwd=ROOT, capture_output=True, text=True, timeout=600)
