@@ -947,10 +947,17 @@ AttnPlan plan_decode_attn(const DevView& v, int n_active, int n_layers, bool clu
   // the page table bounds every stream's window by max_pages * page_size
   const int max_stages = (v.max_pages * v.page_size + kKS - 1) / kKS;
   const int64_t units = static_cast<int64_t>(n_active) * v.n_kv_heads * n_layers;
-  const int64_t resident = resident_ctas(v);
+  const int64_t sms = v.num_sms > 0 ? v.num_sms : 148;
+  const int ring = v.head_dim == 128 ? stages_for<128>() : stages_for<64>();
+  // One layer of few, short windows: at most one CTA per SM, so that the next launch's CTAs
+  // find a free slot, start as soon as this launch lets them (programmatic dependent launch)
+  // and hold their descriptors and queries when it completes.  Long windows or many units
+  // keep every CTA slot streaming.
+  const bool one_per_sm = n_layers == 1 && units <= sms && max_stages <= 4 * ring;
+  const int64_t slots = one_per_sm ? sms : resident_ctas(v);
   int splits = 1;
   // fewer units than CTA slots: split every window over several CTAs
-  if (units < resident) splits = static_cast<int>(resident / units);
+  if (units < slots) splits = static_cast<int>(slots / units);
   const int cap = cluster ? 8 : 64;
   splits = splits > cap ? cap : splits;
   splits = splits > max_stages ? max_stages : splits;
@@ -961,6 +968,7 @@ AttnPlan plan_decode_attn(const DevView& v, int n_active, int n_layers, bool clu
   p.splits = splits;
   p.stages_per_split = splits > 1 ? sps : max_stages;
   p.cluster = cluster && splits > 1;
+  p.slots = slots;
   return p;
 }
 
@@ -971,7 +979,7 @@ cudaError_t launch_decode_attn(const DevView& v, int n_active, int layer0, int n
   AttnArgs args = make_args(v, n_active, layer0, n_layers, q, out, lse, q_layer_stride, lse_layer_stride, p);
   const int64_t units = static_cast<int64_t>(n_active) * v.n_kv_heads * n_layers;
   args.mode = p.cluster ? 1 : 0;
-  const int64_t grid = p.cluster ? units * p.splits : (units < resident_ctas(v) ? units : resident_ctas(v));
+  const int64_t grid = p.cluster ? units * p.splits : (units < p.slots ? units : p.slots);
   return dispatch(args, static_cast<int>(grid), st);
 }
 
@@ -981,7 +989,7 @@ cudaError_t launch_decode_attn_scratch(const DevView& v, int n_active, int layer
   AttnArgs args = make_args(v, n_active, layer, 1, q, out, lse, 0, 0, p);
   const int64_t units = static_cast<int64_t>(n_active) * v.n_kv_heads;
   args.mode = p.splits > 1 ? 2 : 0;
-  const int64_t grid = p.splits > 1 ? units * p.splits : (units < resident_ctas(v) ? units : resident_ctas(v));
+  const int64_t grid = p.splits > 1 ? units * p.splits : (units < p.slots ? units : p.slots);
   cudaError_t e = dispatch(args, static_cast<int>(grid), st);
   if (e != cudaSuccess || p.splits == 1) return e;
   const int blocks = n_active * v.q_per_step * v.n_q_heads;

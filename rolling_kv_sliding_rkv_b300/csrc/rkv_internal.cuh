@@ -167,6 +167,7 @@ struct AttnPlan {
   int splits;            // CTAs per (layer, stream, kv head)
   int stages_per_split;  // 64-slot stages each CTA streams
   bool cluster;          // splits merged through distributed shared memory
+  int64_t slots;         // CTAs the launch may keep resident (whole windows: grid <= slots)
 };
 // cluster = true: splits combine in distributed shared memory (no scratch);
 // false: every split writes (m, l, o) to part_ml / part_o and a merge kernel
