@@ -37,8 +37,8 @@ SCHEMES = {"offset": 0, "exact": 1, "on-read": 2}
 # DRAM traffic (read + write bytes) of one decode-attention launch, from the ncu launch list
 # committed under profiles/ (launch_list_qwen36x64_exact.md), valid only while the attention
 # kernel's source is the one that was profiled: a different source hash reports null.
-TRAFFIC = [{"workload": "qwen", "layers": 36, "schemes": (0, 1), "attn_src_sha256_16": "ad45a807efe036c1",
-            "bytes_per_launch": 915.6e6 + 9.1e6}]
+TRAFFIC = [{"workload": "qwen", "layers": 36, "schemes": (0, 1), "attn_src_sha256_16": "f3fca59244451734",
+            "bytes_per_launch": 915.6e6 + 9.0e6}]
 SCHEME_NAMES = {0: "offset-only", 1: "exact re-base", 2: "exact re-base applied on read"}
 
 
