@@ -131,7 +131,9 @@ __global__ void __launch_bounds__(kRebaseThreads, 4) rebase_kernel(DevView v, in
   pdl_launch_dependents();
   const int d = v.head_dim, half = d / 2, cpairs = d / 16;
   const int a = blockIdx.y;
-  const int lz = blockIdx.z;
+  // layers in reverse block order: the last keys re-based are layer 0's, which decode attention
+  // (layer-major) reads first, while they are still in L2
+  const int lz = static_cast<int>(gridDim.z) - 1 - static_cast<int>(blockIdx.z);
   const StepDesc dsc = v.desc[a];
   if (dsc.delta == 0) return;
   const int item = blockIdx.x * kRebaseThreads + threadIdx.x;
