@@ -36,8 +36,9 @@ SCHEMES = {"offset": 0, "exact": 1, "on-read": 2}
 
 # DRAM traffic (read + write bytes) of one decode-attention launch, from the ncu launch list
 # committed under profiles/ (launch_list_qwen36x64_exact.md), valid only while the attention
-# kernel's source is the one that was profiled: a different source hash reports null.
-TRAFFIC = [{"workload": "qwen", "layers": 36, "schemes": (0, 1), "attn_src_sha256_16": "f3fca59244451734",
+# source's code is the one that was profiled: a different code digest (comments and white space
+# left out) reports null.
+TRAFFIC = [{"workload": "qwen", "layers": 36, "schemes": (0, 1), "attn_code_sha256_16": "b402dd177090064a",
             "bytes_per_launch": 915.6e6 + 9.0e6}]
 SCHEME_NAMES = {0: "offset-only", 1: "exact re-base", 2: "exact re-base applied on read"}
 
@@ -157,18 +158,27 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def code_digest(path):
+    """sha256 (16 hex digits) of a C++/CUDA source with its comments and white space removed."""
+    import hashlib
+    import re
+    with open(path, encoding="utf-8") as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    text = re.sub(r"\s+", "", text)
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
+
+
 def profiled_traffic(wl):
     """ncu DRAM bytes per attention launch for this workload, or None (not profiled / kernel changed)."""
-    import hashlib
-    src = os.path.join(ROOT, "rolling_kv_sliding_rkv_b300", "csrc", "rkv_attn.cu")
     try:
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        digest = code_digest(os.path.join(ROOT, "rolling_kv_sliding_rkv_b300", "csrc", "rkv_attn.cu"))
     except OSError:
         return None
     for t in TRAFFIC:
         if (t["workload"] == wl.name and t["layers"] == wl.n_layers and wl.scheme in t["schemes"]
-                and t["attn_src_sha256_16"] == sha):
+                and t["attn_code_sha256_16"] == digest):
             return t["bytes_per_launch"]
     return None
 

@@ -11,7 +11,7 @@
 // (64 x d 16-bit values each, contiguous in the pool) land in shared memory
 // through bulk asynchronous copies (cp.async.bulk) issued by one producer
 // warp and completed on an mbarrier; 96 KB of stages are in flight per CTA
-// (three at d = 128, six at d = 64), two CTAs per SM.  The pool's chunk
+// (three at d = 128, six at d = 64), up to two CTAs per SM.  The pool's chunk
 // swizzle (rkv_internal.cuh) makes the verbatim copies conflict-free for
 // ldmatrix.
 //
@@ -332,11 +332,11 @@ __device__ __forceinline__ void rot_run(uint8_t* kblk, int r0, int pp, float4 ro
   }
 }
 
-// Two CTAs per SM.  Without a cluster the CTA walks units u = blockIdx.x,
+// Up to two CTAs per SM.  Without a cluster the CTA walks units u = blockIdx.x,
 // blockIdx.x + gridDim.x, ... (whole windows, no split), its producer warp
 // streaming the next unit's pages while the consumers finish the current
 // one.  With a cluster (few units, window split over `splits` CTAs) every
-// CTA takes exactly one (unit, split).
+// CTA takes exactly one (unit, split).  (plan_decode_attn chooses the grid.)
 //
 // Each of the four consumer warps takes 16 of a stage's 64 slots.  A warp
 // moves its K fragments into registers, runs QK^T, moves its V fragments

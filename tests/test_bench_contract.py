@@ -78,6 +78,20 @@ def test_rebase_share_of_the_step():
     assert bench.rebase_in_step(off, m, variants, 100, 6492.7) is None
 
 
+def test_code_digest_ignores_comments_and_layout_only(tmp_path):
+    a = tmp_path / "a.cu"
+    b = tmp_path / "b.cu"
+    c = tmp_path / "c.cu"
+    a.write_text("// header\nint f(int x) {\n  return x + 1;  /* one */\n}\n")
+    b.write_text("/* another\n header */ int f(int x) { return x + 1; }  // trailing\n")
+    c.write_text("int f(int x) { return x + 2; }\n")
+    assert bench.code_digest(a) == bench.code_digest(b)
+    assert bench.code_digest(a) != bench.code_digest(c)
+    # a kernel source other than the profiled one reports no traffic
+    wl = synth.workload("qwen", n_layers=8)
+    assert bench.profiled_traffic(wl) is None
+
+
 def test_reference_arm_prints_one_line():
     out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--steps", "1",
                           "--warmup", "0"], cwd=ROOT, capture_output=True, text=True, timeout=600)
