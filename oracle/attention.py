@@ -16,7 +16,10 @@ Definition (the result the rolling cache is meant to reproduce exactly):
   a causal mask inside the step (reading of voxtral.c §三: compact when
   cache length + new length exceeds the window, then encode the new
   positions against the cache).  ``per_query_window=True`` selects the
-  alternative reading t-W < j <= t for every query.
+  alternative reading t-W < j <= t for every query.  With eviction in
+  batches (a ring of capacity above W, oracle/ring.py), the shared cache
+  starts at the first retained token instead: ``first_key`` = evicted after
+  the step, which replaces n+Q-W as the lower bound.
 * q head h reads kv head floor(h / G), G = Hq / Hkv (contiguous GQA groups;
   Qwen2.5-3B has 16 query / 2 KV heads, model card "架构").
 * s_j = <R(p_t) q, R(p_j) k_j> * scale; o = sum_j softmax(s)_j v_j;
@@ -31,19 +34,23 @@ import numpy as np
 from .rope import rotate
 
 
-def visible_keys(n: int, q_per_step: int, window: int, per_query_window: bool = False):
+def visible_keys(n: int, q_per_step: int, window: int, per_query_window: bool = False,
+                 first_key: int | None = None):
     """For each query i < Q: (lo, hi) inclusive token range it attends."""
     out = []
     for i in range(q_per_step):
         t = n + i
-        lo = t - window + 1 if per_query_window else n + q_per_step - window
+        if first_key is not None:
+            lo = first_key
+        else:
+            lo = t - window + 1 if per_query_window else n + q_per_step - window
         out.append((max(0, lo), t))
     return out
 
 
 def attention_step(q_new, k_tok, v_tok, key_tokens, n: int, p0: int, window: int,
                    scale: float, theta: float, pairing: str = "half",
-                   per_query_window: bool = False):
+                   per_query_window: bool = False, first_key: int | None = None):
     """Outputs of one step.
 
     q_new   [Q][Hq][d]   raw (pre-RoPE) queries of tokens n .. n+Q-1
@@ -60,7 +67,7 @@ def attention_step(q_new, k_tok, v_tok, key_tokens, n: int, p0: int, window: int
     n_q, hq, d = q_new.shape
     hkv = k_tok.shape[1]
     group = hq // hkv
-    ranges = visible_keys(n, n_q, window, per_query_window)
+    ranges = visible_keys(n, n_q, window, per_query_window, first_key)
     lo_all = min(r[0] for r in ranges)
     hi_all = max(r[1] for r in ranges)
     keep = (key_tokens >= lo_all) & (key_tokens <= hi_all)
@@ -86,7 +93,8 @@ def attention_step(q_new, k_tok, v_tok, key_tokens, n: int, p0: int, window: int
 
 
 def attention_step_bruteforce(q_new, k_tok, v_tok, key_tokens, n: int, p0: int, window: int,
-                              scale: float, theta: float, per_query_window: bool = False):
+                              scale: float, theta: float, per_query_window: bool = False,
+                              first_key: int | None = None):
     """Second formulation: explicit loops, angles by math.cos(p * omega) (small p only).
 
     Half-split pairing.  Written without numpy linear algebra and without the
@@ -112,7 +120,10 @@ def attention_step_bruteforce(q_new, k_tok, v_tok, key_tokens, n: int, p0: int, 
     lse = [[0.0] * hq for _ in range(n_q)]
     for i in range(n_q):
         t = n + i
-        lo = max(0, t - window + 1) if per_query_window else max(0, n + n_q - window)
+        if first_key is not None:
+            lo = max(0, first_key)
+        else:
+            lo = max(0, t - window + 1) if per_query_window else max(0, n + n_q - window)
         for h in range(hq):
             g = h // (hq // hkv)
             qr = rot(q_new[i][h], p0 + t)

@@ -13,14 +13,21 @@ State fields, in the order the CUDA library reports them:
                  to `evicted` on every roll (explainer, "Rolling KV Cache
                  三步拆解", 第 2 步), or once `rebase_interval` tokens have been
                  evicted since the last re-base.  0 in the offset-only scheme.
-  head_slot      ring slot of the oldest retained token, evicted mod W
-  W              window (ring capacity)
+  head_slot      ring slot of the oldest retained token, evicted mod C
+  W              window
   P0             logical position of token 0
 
 Eviction: a step of Q tokens keeps the last W tokens (explainer 第 1 步;
 voxtral.c article §二 keeps the last VOX_DEC_WINDOW positions, §三 compacts
 when cache length + new length exceeds the window).  The ring stores token j
-in slot j mod W, so eviction moves no data.
+in slot j mod C, so eviction moves no data.
+
+Capacity C >= W (default C = W, the plain sliding window above): the window
+may grow to C tokens and is cut back to the last W only when a step would
+exceed C, i.e. eviction in batches.  This is the reading of the explainer's
+"oldest batch" (第 1 步: 最老的一批) and of voxtral.c's trigger (article §二:
+compaction only once the position reaches kv_cache_max, down to the
+window); the window length then varies in [W, C] once filled.
 """
 from __future__ import annotations
 
@@ -32,10 +39,12 @@ FIELDS = ("n", "len", "evicted", "kv_pos_offset", "rope_base", "head_slot", "W",
 
 class StreamRing:
     def __init__(self, window: int, p0: int = 0, q_per_step: int = 1,
-                 scheme: int = SCHEME_OFFSET_ONLY, rebase_interval: int = 1):
-        if window < 1 or q_per_step < 1 or q_per_step > window or rebase_interval < 1:
+                 scheme: int = SCHEME_OFFSET_ONLY, rebase_interval: int = 1, capacity: int | None = None):
+        capacity = window if capacity is None else capacity
+        if window < 1 or q_per_step < 1 or q_per_step > window or rebase_interval < 1 or capacity < window:
             raise ValueError("bad ring parameters")
         self.W = int(window)
+        self.C = int(capacity)
         self.P0 = int(p0)
         self.Q = int(q_per_step)
         self.scheme = scheme
@@ -52,20 +61,21 @@ class StreamRing:
 
     @property
     def head_slot(self) -> int:
-        return self.evicted % self.W
+        return self.evicted % self.C
 
     def step(self) -> None:
-        """Append Q tokens: advance n, evict down to W, schedule a re-base."""
+        """Append Q tokens: advance n, evict down to W once past the capacity, schedule a re-base."""
         self.n += self.Q
-        self.len = min(self.n, self.W)
-        self.evicted = self.n - self.len
+        if self.n - self.evicted > self.C:
+            self.evicted = self.n - self.W
+        self.len = self.n - self.evicted
         self.last_delta = 0
         if self.scheme == SCHEME_EXACT_REBASE and self.evicted - self.rope_base >= self.interval:
             self.last_delta = self.evicted - self.rope_base
             self.rope_base = self.evicted
 
     def slot(self, j: int) -> int:
-        return j % self.W
+        return j % self.C
 
     def physical(self, j: int) -> int:
         return j - self.evicted
@@ -90,22 +100,24 @@ class StreamRing:
 class CompactingCache:
     """The voxtral.c formulation: a growable buffer compacted by memmove.
 
-    Before appending `new_len` tokens, if length + new_len exceeds the window,
-    the oldest entries are dropped so that exactly `window` remain after the
-    append, the rest move to index 0 (memmove), and the dropped count is added
-    to kv_pos_offset (voxtral.c article §二, §三).  Kept only to pin the ring
-    model: both must agree on which tokens are retained and on their logical
-    positions.
+    Before appending `new_len` tokens, if length + new_len exceeds the
+    compaction threshold (`compact_at`, voxtral's kv_cache_max; by default the
+    window itself), the oldest entries are dropped so that exactly `window`
+    remain after the append, the rest move to index 0 (memmove), and the
+    dropped count is added to kv_pos_offset (voxtral.c article §二, §三).
+    Kept only to pin the ring model: both must agree on which tokens are
+    retained and on their logical positions.
     """
 
-    def __init__(self, window: int, p0: int = 0):
+    def __init__(self, window: int, p0: int = 0, compact_at: int | None = None):
         self.window = window
+        self.compact_at = window if compact_at is None else compact_at
         self.buf: list = []          # token ids, physical index = list index
         self.kv_pos_offset = p0
 
     def append(self, tokens: list) -> None:
         new_len = len(tokens)
-        if len(self.buf) + new_len > self.window:
+        if len(self.buf) + new_len > self.compact_at:
             drop = len(self.buf) + new_len - self.window
             self.buf = self.buf[drop:]
             self.kv_pos_offset += drop

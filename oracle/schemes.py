@@ -29,8 +29,8 @@ class StoredKeyCache:
     def __init__(self, ring: StreamRing, n_kv_heads: int, head_dim: int, theta: float):
         self.ring = ring
         self.theta = theta
-        self.k = np.zeros((ring.W, n_kv_heads, head_dim))
-        self.v = np.zeros((ring.W, n_kv_heads, head_dim))
+        self.k = np.zeros((ring.C, n_kv_heads, head_dim))
+        self.v = np.zeros((ring.C, n_kv_heads, head_dim))
 
     def step(self, q_new, k_new, v_new, scale: float):
         """Advance the ring by Q tokens and return (o [Q][Hq][d], lse [Q][Hq])."""

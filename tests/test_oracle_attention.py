@@ -79,6 +79,25 @@ def test_bruteforce_tiny(window, d):
                 assert np.abs(a[1] - b[1]).max() < 1e-12
 
 
+@pytest.mark.parametrize("first_key", [0, 2, 5])
+def test_bruteforce_first_key(first_key):
+    # eviction in batches: every query of the step attends [first_key, own token]
+    rng = np.random.default_rng(first_key)
+    for q_per_step, hq, hkv in [(1, 2, 1), (2, 4, 2), (4, 2, 1)]:
+        n = 8
+        q, k, v, toks = _rand_case(rng, n, q_per_step, hq, hkv, 4)
+        a = attention_step(q, k, v, toks, n, 5, 3, 0.7, 100.0, first_key=first_key)
+        b = attention_step_bruteforce(q, k, v, toks, n, 5, 3, 0.7, 100.0, first_key=first_key)
+        assert np.abs(a[0] - b[0]).max() < 1e-12 and np.abs(a[1] - b[1]).max() < 1e-12
+        # the window argument no longer matters; first_key = n + Q - W gives the plain window back
+        c = attention_step(q, k, v, toks, n, 5, 7, 0.7, 100.0, first_key=first_key)
+        assert np.abs(a[0] - c[0]).max() == 0.0
+        w = max(3, q_per_step)
+        d = attention_step(q, k, v, toks, n, 5, w, 0.7, 100.0, first_key=n + q_per_step - w)
+        e = attention_step(q, k, v, toks, n, 5, w, 0.7, 100.0)
+        assert np.abs(d[0] - e[0]).max() == 0.0 and np.abs(d[1] - e[1]).max() == 0.0
+
+
 def test_gqa_contiguous_groups():
     rng = np.random.default_rng(4)
     q, k, v, toks = _rand_case(rng, 20, 1, 8, 2, 16)
