@@ -1,18 +1,24 @@
 """Benchmark of the rolling-KV step: stream-steps/s (all layers) and decode-attention HBM GB/s.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload qwen] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mixed] [--impl ours|reference]
 
 One step = the whole hot path for every active stream and every layer: begin
 step (ring bookkeeping + RoPE angles), then per layer the exact re-base (exact
 scheme), RoPE + append, and split-K decode attention with its merge.  The
 timed steps replay CUDA graphs of `rkv_step` over inputs already resident in
-HBM; the window is full before timing starts (steady state).  Under torchrun
-every rank runs its own copy of the workload (streams are independent: no
-collective on the data path) and `value` sums all ranks' stream-steps over
-the slowest rank's time.
+HBM; the windows are full before timing starts (steady state).
+
+The default workload is the largest batched one: mixed-clock serving, 256
+streams with 80 / 120 / 160 ms clocks (windows 375 / 250 / 188) on a 40 ms
+scheduler tick, 36 Qwen-shaped layers, exact re-base; one step is one tick.
+The line also carries the Qwen-shaped decoder (36 layers, 64 streams) and the
+voxtral-shaped decoder (26 layers, 16 streams, window 8192) as sub-records
+with their own roofline.  Under torchrun every rank runs its own copy of the
+workload (streams are independent: no collective on the data path) and
+`value` sums all ranks' stream-steps over the slowest rank's time.
 
 The reference arm (`--impl reference`) times the fp64 CPU oracle on this
-host's cores on a bounded sample of the same workload.
+host's cores, each step a bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -34,10 +40,9 @@ METRIC = "stream-steps/sec (all layers) and decode-attn HBM GB/s as % of B300 pe
 UNIT = "stream-steps/s"
 SCHEMES = {"offset": 0, "exact": 1, "on-read": 2}
 
-# DRAM traffic (read + write bytes) of one decode-attention launch, from the ncu launch list
-# committed under profiles/ (launch_list_qwen36x64_exact.md), valid only while the attention
-# source's code is the one that was profiled: a different code digest (comments and white space
-# left out) reports null.
+# DRAM traffic (read + write bytes) of one all-layers decode-attention launch, from the committed
+# ncu launch-list summary of the same command, valid only while the attention source's code is the
+# one that was profiled: a different code digest (comments and white space left out) reports null.
 TRAFFIC = [{"workload": "qwen", "layers": 36, "schemes": (0, 1), "attn_code_sha256_16": "b402dd177090064a",
             "bytes_per_launch": 915.6e6 + 9.0e6}]
 SCHEME_NAMES = {0: "offset-only", 1: "exact re-base", 2: "exact re-base applied on read"}
@@ -48,7 +53,7 @@ def parse_args():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=20)
-    p.add_argument("--workload", default="qwen", choices=["tiny", "qwen", "voxtral", "encoder", "mixed"])
+    p.add_argument("--workload", default="mixed", choices=["tiny", "qwen", "voxtral", "encoder", "mixed"])
     p.add_argument("--scheme", default=None, choices=[None, "offset", "exact", "on-read"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
@@ -60,6 +65,10 @@ def parse_args():
                    help="skip timing the workload under the other two schemes")
     p.add_argument("--no-flatness", dest="flatness", action="store_false",
                    help="skip the per-step time at five start offsets (Qwen-shaped workload)")
+    p.add_argument("--no-sub", dest="sub", action="store_false",
+                   help="skip the Qwen- and voxtral-shaped sub-records of the default run")
+    p.add_argument("--no-per-layer", dest="per_layer", action="store_false",
+                   help="skip the step made of per-layer calls")
     return p.parse_args()
 
 
@@ -218,36 +227,61 @@ def _oracle_chunk(args):
     return done
 
 
-def oracle_timing(wl, budget_s, steps_per_chunk=4):
-    """Time the oracle on all host cores (spawned workers) on a bounded sample.
+class OracleRunner:
+    """The fp64 oracle on all host cores (spawned worker processes), timed in steps.
 
-    Each chunk is `steps_per_chunk` consecutive full-window steps of one
-    stream over a subset of layers; chunks are issued until the budget is
-    spent.  Returns stream-steps/s (all layers), extrapolated from
-    stream-layer-steps/s.
-    """
-    import multiprocessing as mp
-    cores = os.cpu_count() or 1
-    ctx = mp.get_context("spawn")
-    w = int(wl.windows().max())
-    n0 = (w // wl.q_per_step + 3) * wl.q_per_step     # steady state: window full
-    layers = list(range(0, wl.n_layers, max(1, wl.n_layers // 4)))[:4]
-    with ctx.Pool(cores) as pool:
-        pool.map(_oracle_chunk, [(wl.name, 0, n0, 1, [0])] * cores)   # import + warm caches
+    A step is a bounded sample of the workload: batches of chunks, one chunk =
+    `steps_per_chunk` consecutive full-window steps of one stream over a
+    subset of layers, issued until the step's budget is spent.  Throughput is
+    extrapolated from stream-layer-steps/s to stream-steps/s (all layers)."""
+
+    def __init__(self, wl, steps_per_chunk=4):
+        import multiprocessing as mp
+        self.wl = wl
+        self.cores = os.cpu_count() or 1
+        self.steps_per_chunk = steps_per_chunk
+        self.pool = mp.get_context("spawn").Pool(self.cores)
+        w = int(wl.windows().max())
+        self.n0 = (w // wl.q_per_step + 3) * wl.q_per_step     # steady state: window full
+        self.layers = list(range(0, wl.n_layers, max(1, wl.n_layers // 4)))[:4]
+        self.jobs = 0
+        self.pool.map(_oracle_chunk, [(wl.name, 0, self.n0, 1, [0])] * self.cores)   # import + warm caches
+
+    def step(self, budget_s):
+        """One step: chunks until `budget_s` is spent (at least one batch); returns (layer-steps, seconds)."""
+        wl = self.wl
         t0 = time.perf_counter()
         done = 0
-        jobs = 0
-        while time.perf_counter() - t0 < budget_s:
-            batch = [(wl.name, (jobs + i) % wl.n_streams, n0 + 64 * wl.q_per_step * ((jobs + i) // wl.n_streams),
-                      steps_per_chunk, layers) for i in range(cores)]
-            done += sum(pool.map(_oracle_chunk, batch))
-            jobs += cores
-        elapsed = time.perf_counter() - t0
-    rate_layer_steps = done / elapsed
-    return {"value": rate_layer_steps / wl.n_layers, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": (f"{done} full-window stream-layer-steps ({len(layers)} of {wl.n_layers} layers, "
-                       f"{steps_per_chunk} consecutive steps per stream) in {elapsed:.1f} s on {cores} spawned "
-                       f"processes; value = stream-layer-steps/s / {wl.n_layers} layers (extrapolated)")}
+        while True:
+            batch = [(wl.name, (self.jobs + i) % wl.n_streams,
+                      self.n0 + 64 * wl.q_per_step * ((self.jobs + i) // wl.n_streams),
+                      self.steps_per_chunk, self.layers) for i in range(self.cores)]
+            done += sum(self.pool.map(_oracle_chunk, batch))
+            self.jobs += self.cores
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        return done, time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+    def describe(self, done, elapsed, what=""):
+        wl = self.wl
+        return (f"{done} full-window stream-layer-steps ({len(self.layers)} of {wl.n_layers} layers, "
+                f"{self.steps_per_chunk} consecutive steps per stream){what} in {elapsed:.1f} s on {self.cores} "
+                f"spawned processes; value = stream-layer-steps/s / {wl.n_layers} layers (extrapolated)")
+
+
+def oracle_timing(wl, budget_s):
+    """The oracle's throughput on a bounded sample of about `budget_s` seconds (the cpu_baseline)."""
+    r = OracleRunner(wl)
+    try:
+        done, elapsed = r.step(budget_s)
+    finally:
+        r.close()
+    return {"value": done / elapsed / wl.n_layers, "unit": UNIT, "cores": r.cores, "kind": "oracle",
+            "sample": r.describe(done, elapsed)}
 
 
 def run_reference(args):
@@ -255,17 +289,33 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    wl = synth.workload(args.workload)
-    scheme = args.scheme or ("exact" if wl.scheme == 1 else "offset")
+    over = {"scheme": SCHEMES[args.scheme]} if args.scheme else {}
+    wl = synth.workload(args.workload, **over)
     # each step is a bounded sample: the whole run stays within about two minutes
-    per_step = max(0.02, min(1.0, 110.0 / max(1, args.steps + args.warmup)))
-    base = oracle_timing(wl, per_step * args.steps)
-    line = {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * wl.n_streams / base["value"],
+    per_step = max(0.05, min(1.0, 110.0 / max(1, args.steps + args.warmup)))
+    r = OracleRunner(wl)
+    try:
+        for _ in range(args.warmup):
+            r.step(per_step)
+        done = 0
+        elapsed = 0.0
+        for _ in range(args.steps):
+            d, t = r.step(per_step)
+            done += d
+            elapsed += t
+    finally:
+        r.close()
+    value = done / elapsed / wl.n_layers
+    base = {"value": value, "unit": UNIT, "cores": r.cores, "kind": "oracle",
+            "sample": r.describe(done, elapsed, f", {args.steps} timed steps of about {per_step:.2f} s each")}
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * elapsed / max(1, args.steps),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": describe(wl, scheme), "parallelism": "replicas"},
+            "data": "synthetic", "config": {"workload": describe(wl, SCHEME_NAMES[wl.scheme]),
+                                            "parallelism": "replicas",
+                                            "step": "a bounded sample of the workload's stream-layer-steps"},
             "cpu_baseline": base,
-            "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
@@ -300,10 +350,13 @@ def step_phases(wl):
     return [wl.active_at_tick(t).tolist() for t in range(period)]
 
 
-def measure(wl, args, dev, rank, world, timed=True, p0=None, attention=True):
+def measure(wl, args, dev, rank, world, timed=True, p0=None, attention=True, per_layer_step=False):
     """Time the step of workload `wl` on this GPU; returns the figures of one JSON line.
 
-    p0: start offset given to every stream (default: the workload's draws)."""
+    p0: start offset given to every stream (default: the workload's draws).
+    per_layer_step: also time the same steps made of per-layer calls (begin step, then for each
+    layer re-base, append and decode attention), one CUDA graph per step, as a model that runs
+    other work between its layers must call them."""
     import torch
 
     import rolling_kv_sliding_rkv_b300 as rkv
@@ -402,6 +455,50 @@ def measure(wl, args, dev, rank, world, timed=True, p0=None, attention=True):
     out.update(value=job["value"], ms=job["ms"], stream_steps=job["stream_steps"],
                launches=launches_per_step * sum(1 for i in range(args.steps) if graphs[i % R] is not None),
                free_bytes_delta=torch.cuda.mem_get_info(dev)[0] - free_before)
+
+    if per_layer_step:
+        def layer_calls(act, b):
+            A = len(act)
+            h.begin_step(act)
+            for layer in range(L):
+                if wl.scheme in (1, 2):
+                    h.rebase(layer)
+                h.append_rope(layer, b["k"][layer * A * Q * hkv * d:], b["v"][layer * A * Q * hkv * d:])
+                h.decode_attn(layer, b["q"][layer * A * Q * hq * d:], b["out"][layer * A * Q * hq * d:],
+                              b["lse"][layer * A * Q * hq:])
+        lgraphs = []
+        with torch.cuda.stream(stream):
+            for r, act in enumerate(plan):
+                if act:
+                    layer_calls(act, sets[r])
+            stream.synchronize()
+            for r, act in enumerate(plan):
+                if not act:
+                    lgraphs.append(None)
+                    continue
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    layer_calls(act, sets[r])
+                lgraphs.append(g)
+        for i in range(args.warmup + R):
+            if lgraphs[i % R] is not None:
+                lgraphs[i % R].replay()
+        barrier()
+        ev0.record(cur)
+        for i in range(args.steps):
+            if lgraphs[i % R] is not None:
+                lgraphs[i % R].replay()
+        ev1.record(cur)
+        torch.cuda.synchronize()
+        lms = ev0.elapsed_time(ev1)
+        h.sync_status()
+        ljob = aggregate(lms, sum(len(plan[i % R]) for i in range(args.steps)), world, dev)
+        per_step_launches = 1 + L * (2 + (1 if wl.scheme == 1 else 0))
+        out["per_layer_step"] = {
+            "value": ljob["value"], "unit": UNIT, "ms_per_step": ljob["ms"] / args.steps,
+            "launches_per_step": per_step_launches,
+            "how": "the same steps as one CUDA graph of per-layer calls each: begin step, then for every layer "
+                   "re-base (exact re-base scheme), RoPE + append and decode attention"}
     if not attention:
         return out
 
@@ -453,35 +550,53 @@ def measure(wl, args, dev, rank, world, timed=True, p0=None, attention=True):
     return out
 
 
-def bench_line(wl, scheme_name, args, world, m, peak, peak_kind, variants=None, flat=None, e2e=None, cpu=None):
-    """The one JSON line of a run: the driver's contract keys plus the roofline of the dominant kernel."""
+def workload_figures(wl, scheme_name, m, peak, peak_kind, steps, world):
+    """value, per-step time and the decode-attention roofline of one measured workload."""
     achieved = m["attn_bytes"] / (m["attn_all_ms"] / 1000.0) / 1e9
     achieved_layer = m["attn_bytes_layer"] / (m["attn_layer_ms"] / 1000.0) / 1e9
     A = len(step_phases(wl)[0]) if not wl.tick_ms else None
-    line = {"metric": METRIC, "value": m["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": m["ms"] / args.steps, "higher_is_better": True,
+    fig = {"value": m["value"], "unit": UNIT, "ms_per_step": m["ms"] / steps,
+           "config": {"workload": describe(wl, scheme_name),
+                      "streams_per_gpu": A if A is not None else
+                      f"{m['stream_steps'] / steps / world:.1f} active per 40 ms tick (of {wl.n_streams})",
+                      "layers": wl.n_layers},
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                        "frac": achieved / peak, "traffic": profiled_traffic(wl),
+                        "kernel": f"attn_kernel: decode attention over all {wl.n_layers} layers in one "
+                                  "launch (as inside the timed step)",
+                        "algorithmic_bytes_per_launch": m["attn_bytes"],
+                        "avg_launch_us": m["attn_all_ms"] * 1000.0,
+                        "streams_in_launch": m["attn_streams"],
+                        "peak_kind": f"{peak_kind} (hbm_gbs, STREAM-style copy, burst)"},
+           "decode_attn_gbs": achieved,
+           "decode_attn_per_layer_launch": {"achieved_gbs": achieved_layer, "frac": achieved_layer / peak,
+                                            "avg_launch_us": m["attn_layer_ms"] * 1000.0,
+                                            "algorithmic_bytes_per_launch": m["attn_bytes_layer"]}}
+    if "per_layer_step" in m:
+        fig["value_per_layer_graph"] = m["per_layer_step"]["value"]
+        fig["per_layer_step"] = m["per_layer_step"]
+    return fig
+
+
+def bench_line(wl, scheme_name, args, world, m, peak, peak_kind, variants=None, flat=None, e2e=None, cpu=None,
+               subs=None):
+    """The one JSON line of a run: the driver's contract keys plus the roofline of the dominant kernel."""
+    fig = workload_figures(wl, scheme_name, m, peak, peak_kind, args.steps, world)
+    line = {"metric": METRIC, "value": fig["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": fig["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": describe(wl, scheme_name),
-                       "streams_per_gpu": A if A is not None else
-                       f"{m['stream_steps'] / args.steps / world:.1f} active per 40 ms tick (of {wl.n_streams})",
-                       "layers": wl.n_layers,
-                       "l2": "per-step working set of KV pages > 126 MB L2; no flush between steps",
-                       "graph": "one CUDA graph per step (per tick phase for mixed clocks), replayed",
-                       "parallelism": "replicas" if world == 1 else f"replicas x{world}"},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": profiled_traffic(wl),
-                         "kernel": f"attn_kernel: decode attention over all {wl.n_layers} layers in one "
-                                   "launch (as inside the timed step)",
-                         "algorithmic_bytes_per_launch": m["attn_bytes"],
-                         "avg_launch_us": m["attn_all_ms"] * 1000.0,
-                         "streams_in_launch": m["attn_streams"],
-                         "peak_kind": f"{peak_kind} (hbm_gbs, STREAM-style copy, burst)"},
-            "decode_attn_gbs": achieved,
-            "decode_attn_per_layer_launch": {"achieved_gbs": achieved_layer, "frac": achieved_layer / peak,
-                                             "avg_launch_us": m["attn_layer_ms"] * 1000.0,
-                                             "algorithmic_bytes_per_launch": m["attn_bytes_layer"]},
+            "config": dict(fig["config"],
+                           l2="per-step working set of KV pages > 126 MB L2; no flush between steps",
+                           graph="one CUDA graph per step (per tick phase for mixed clocks), replayed",
+                           parallelism="replicas" if world == 1 else f"replicas x{world}"),
+            "roofline": fig["roofline"],
+            "decode_attn_gbs": fig["decode_attn_gbs"],
+            "decode_attn_per_layer_launch": fig["decode_attn_per_layer_launch"],
             "gpu_launches": m["launches"],
             "clocks": m.get("clocks")}
+    for key in ("value_per_layer_graph", "per_layer_step"):
+        if key in fig:
+            line[key] = fig[key]
     if variants:
         line["schemes"] = variants
         rb = rebase_in_step(wl, m, variants, args.steps, peak)
@@ -489,6 +604,8 @@ def bench_line(wl, scheme_name, args, world, m, peak, peak_kind, variants=None, 
             line["rebase_in_step"] = rb
     if flat is not None:
         line["flatness"] = flat
+    if subs:
+        line["workloads"] = subs
     if e2e is not None:
         line["e2e"] = e2e
     if cpu is not None:
@@ -514,7 +631,7 @@ def run_ours(args):
         over["n_layers"] = args.layers
     wl = synth.workload(args.workload, **over)
     scheme_name = SCHEME_NAMES[wl.scheme]
-    m = measure(wl, args, dev, rank, world)
+    m = measure(wl, args, dev, rank, world, per_layer_step=args.per_layer)
     h = m.pop("h")
     peak, peak_kind = measured_peak()
 
@@ -530,31 +647,49 @@ def run_ours(args):
             todo.append(("exact re-base every 8 rolls", dict(over, rebase_interval=8)))
         for label, vover in todo:
             vw = synth.workload(args.workload, **vover)
-            vm = measure(vw, args, dev, rank, 1, timed=False)
+            vm = measure(vw, args, dev, rank, 1, timed=False, per_layer_step=args.per_layer)
             vm.pop("h").close()
             variants[label] = {
                 "value": vm["value"], "unit": UNIT, "ms_per_step": vm["ms"] / args.steps,
                 "decode_attn_gbs": vm["attn_bytes"] / (vm["attn_all_ms"] / 1000.0) / 1e9,
                 "decode_attn_frac": vm["attn_bytes"] / (vm["attn_all_ms"] / 1000.0) / 1e9 / peak}
+            if "per_layer_step" in vm:
+                variants[label]["value_per_layer_graph"] = vm["per_layer_step"]["value"]
 
-    flat = None
-    if args.flatness and rank == 0 and wl.name == "qwen" and not args.layers:
+    def flatness(fw, free_delta):
         # cost per step must not depend on how far the streams are into their logical timelines
         offsets = [0, 540_000, 1_080_000, 2_000_000, 2 ** 31 + 5]
         per = []
         for p0 in offsets:
-            fm = measure(wl, args, dev, rank, 1, timed=False, p0=p0, attention=False)
+            fm = measure(fw, args, dev, rank, 1, timed=False, p0=p0, attention=False)
             fm.pop("h").close()
             per.append(fm["ms"] / args.steps)
-        flat = {"p0": offsets, "ms_per_step": per, "spread": max(per) / min(per) - 1.0,
-                "free_bytes_delta_over_timed_steps": m["free_bytes_delta"]}
+        return {"p0": offsets, "ms_per_step": per, "spread": max(per) / min(per) - 1.0,
+                "free_bytes_delta_over_timed_steps": free_delta}
+
+    flat = None
+    if args.flatness and rank == 0 and wl.name == "qwen" and not args.layers:
+        flat = flatness(wl, m["free_bytes_delta"])
+
+    # the other two batched decoder workloads, each with its own roofline (default run only)
+    subs = {}
+    if args.sub and rank == 0 and args.workload == "mixed" and not args.layers and not args.scheme:
+        for name in ("qwen", "voxtral"):
+            sw = synth.workload(name)
+            sm = measure(sw, args, dev, rank, 1, timed=False, per_layer_step=args.per_layer)
+            sm.pop("h").close()
+            subs[name] = workload_figures(sw, SCHEME_NAMES[sw.scheme], sm, peak, peak_kind, args.steps, 1)
+            subs[name]["free_bytes_delta_over_timed_steps"] = sm["free_bytes_delta"]
+            if name == "qwen" and args.flatness:
+                subs[name]["flatness"] = flatness(sw, sm["free_bytes_delta"])
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = oracle_timing(wl, args.cpu_seconds)
 
     if rank == 0:
-        line = bench_line(wl, scheme_name, args, world, m, peak, peak_kind, variants, flat, e2e, cpu)
+        line = bench_line(wl, scheme_name, args, world, m, peak, peak_kind, variants, flat, e2e, cpu, subs)
+        line["free_bytes_delta_over_timed_steps"] = m["free_bytes_delta"]
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -200,7 +200,11 @@ RKV_API int rkv_rebase(rkv_handle* h, int32_t layer, void* stream);
  *   lse   device [A][Q][Hq] fp32: natural log of sum exp(scaled scores); may
  *         be NULL
  * Query token n_old + i of a stream attends its tokens j with
- * max(0, n_new - W) <= j <= n_old + i. */
+ * max(0, n_new - W) <= j <= n_old + i.  q may be written by the kernel
+ * launched immediately before this call on `stream`: the kernel reads q only
+ * after that kernel has completed (programmatic dependent launch lets this
+ * kernel start early, but it waits for its predecessor before touching q,
+ * the pages or out). */
 RKV_API int rkv_decode_attn(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv_bf16* out,
                             float* lse, void* stream);
 
@@ -228,20 +232,24 @@ RKV_API int rkv_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active,
  * inside its 80 ms clock step, or a plug-in inside a serving engine whose
  * caching allocator already holds the free HBM.
  *
- * Same arguments, call-order rules and results as rkv_decode_attn, but the
- * split-K partial results go to a fixed array compiled into the library
- * (8 MiB per device, held by every GPU that loads the library until the
- * process exits) instead of the handle's state buffer.  A call that needs
- * more than 8 MiB of partials ((2 + head_dim) floats per active stream,
- * query row and split) returns RKV_ERR_CAPACITY with the sizes in the
- * message.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current, so make that first call
- * before any stream capture.  Every call on a device shares the one array,
- * and the array keeps the last call's contents; nothing in it needs to start
- * at zero, because every partial the merge reads is written earlier in the
- * same call.  Calls that overlap on the GPU (other streams, other handles,
- * other threads) race on the array: the caller must serialise them.  No
- * cudaMalloc, cudaFree or allocating library routine is called. */
+ * Same arguments and call-order rules as rkv_decode_attn.  When the windows
+ * are split over several CTAs, the per-split partial results go to a fixed
+ * array compiled into the library (8 MiB per device, held by every GPU that
+ * loads the library until the process exits) and a second kernel merges
+ * them; rkv_decode_attn merges its splits in distributed shared memory
+ * instead and may split differently, so the two agree to fp32 rounding of
+ * the merge, not bit for bit.  A call whose windows are not split uses no
+ * part of the array.  A call that needs more than 8 MiB of partials
+ * ((2 + head_dim) floats per active stream, query row and split) returns
+ * RKV_ERR_CAPACITY with the sizes in the message.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current, so make that first call before any stream capture.
+ * Every call on a device shares the one array, and the array keeps the last
+ * call's contents; nothing in it needs to start at zero, because every
+ * partial the merge reads is written earlier in the same call.  Calls that
+ * overlap on the GPU (other streams, other handles, other threads) race on
+ * the array: the caller must serialise them.  No cudaMalloc, cudaFree or
+ * allocating library routine is called. */
 RKV_API int rkv_decode_attn_static(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv_bf16* out,
                                    float* lse, void* stream);
 
@@ -272,6 +280,16 @@ RKV_API int rkv_reset_stream(rkv_handle* h, int32_t stream_id, int64_t start_off
 RKV_API int rkv_stream_snapshot_bytes(const rkv_handle* h, int32_t stream_id, size_t* bytes);
 RKV_API int rkv_save_stream(rkv_handle* h, int32_t stream_id, void* dst, size_t bytes, void* stream);
 RKV_API int rkv_load_stream(rkv_handle* h, int32_t stream_id, const void* src, size_t bytes, void* stream);
+
+/* Check a stream state record (RKV_STATE_FIELDS int64, the order of
+ * rkv_get_stream_state) against the rules every step keeps under `cfg`:
+ * W_s in [q_per_step, RKV_MAX_WINDOW], 0 <= P0 < 2^52, n >= 0 a multiple of
+ * q_per_step with P0 + n < 2^52, len = min(n, W), evicted = n - len,
+ * kv_pos_offset = P0 + evicted, head_slot = evicted mod W, and rope_base in
+ * (evicted - rebase_interval, evicted] for the exact schemes, 0 otherwise.
+ * rkv_load_stream applies it to a snapshot before restoring it.  Host only:
+ * RKV_OK, else RKV_ERR_CONFIG with the broken rule in rkv_last_error(NULL). */
+RKV_API int rkv_check_stream_state(const rkv_config* cfg, const int64_t* state);
 
 /* Copy one stream's device state to host `out` (RKV_STATE_FIELDS int64):
  * n, len, evicted, kv_pos_offset, rope_base, head_slot, W, P0.  Waits for
@@ -310,6 +328,14 @@ RKV_API int rkv_gen_tokens(uint64_t seed, uint32_t tag, int32_t stream_id, int32
  * (tags 2, 3); token index = the stream's own token count. */
 RKV_API int rkv_gen_step_inputs(rkv_handle* h, uint64_t seed, int32_t layer, float scale, rkv_bf16* q,
                         rkv_bf16* k, rkv_bf16* v, void* stream);
+
+/* The same draws for the next step of the listed streams, every layer, in
+ * the layout rkv_step takes: q [L][A][Q][Hq][d], k and v [L][A][Q][Hkv][d]
+ * (tags 1, 2, 3; rows in active_ids order).  The token index of a stream's
+ * row t is its device token count n (as it stands when the kernel runs) plus
+ * t, i.e. the tokens the next rkv_begin_step or rkv_step will append. */
+RKV_API int rkv_gen_next_inputs(rkv_handle* h, uint64_t seed, const int32_t* active_ids, int32_t n_active,
+                                float scale, rkv_bf16* q, rkv_bf16* k, rkv_bf16* v, void* stream);
 
 #ifdef __cplusplus
 }

@@ -12,8 +12,8 @@ from . import _abi
 from ._abi import (  # noqa: F401
     RKV_ERR_CAPACITY, RKV_ERR_CONFIG, RKV_ERR_CUDA, RKV_ERR_DEVICE_BOUNDS, RKV_ERR_DEVICE_RANGE, RKV_ERR_INVALID_ARG,
     RKV_ERR_STATE, RKV_ERR_TIMEOUT, RKV_OK, RKV_SCHEME_EXACT_ON_READ, RKV_SCHEME_EXACT_REBASE, RKV_SCHEME_OFFSET_ONLY,
-    STATE_FIELDS, RkvError, make_config, rkv_append_rope, rkv_begin_step, rkv_clock_resolve,
-    rkv_create, rkv_decode_attn, rkv_decode_attn_layers, rkv_decode_attn_static, rkv_destroy, rkv_gen_step_inputs, rkv_gen_tokens,
+    STATE_FIELDS, RkvError, make_config, rkv_append_rope, rkv_begin_step, rkv_check_stream_state, rkv_clock_resolve,
+    rkv_create, rkv_decode_attn, rkv_decode_attn_layers, rkv_decode_attn_static, rkv_destroy, rkv_gen_next_inputs, rkv_gen_step_inputs, rkv_gen_tokens,
     rkv_get_stream_state, rkv_last_error, rkv_load_stream, rkv_rebase, rkv_required_bytes, rkv_reset_stream,
     rkv_rope_cossin, rkv_save_stream, rkv_stream_snapshot_bytes,
     rkv_step, rkv_sync_status,
@@ -59,6 +59,9 @@ class RollingKV:
 
     def gen_step_inputs(self, seed, layer, scale, q, k, v, stream=None):
         rkv_gen_step_inputs(self.handle, seed, layer, scale, q, k, v, stream)
+
+    def gen_next_inputs(self, seed, active_ids, scale, q, k, v, stream=None):
+        rkv_gen_next_inputs(self.handle, seed, active_ids, scale, q, k, v, stream)
 
     def reset_stream(self, stream_id, start_offset=0, stream=None):
         rkv_reset_stream(self.handle, stream_id, start_offset, stream)

@@ -68,6 +68,7 @@ _SIGS = {
     "rkv_decode_attn_layers": [_vp, _i32, _i32, _vp, _vp, _vp, _vp],
     "rkv_step": [_vp, C.POINTER(_i32), _i32, _vp, _vp, _vp, _vp, _vp, _vp],
     "rkv_get_stream_state": [_vp, _i32, C.POINTER(_i64), _vp],
+    "rkv_check_stream_state": [C.POINTER(rkv_config), C.POINTER(_i64)],
     "rkv_reset_stream": [_vp, _i32, _i64, _vp],
     "rkv_stream_snapshot_bytes": [_vp, _i32, C.POINTER(_sz)],
     "rkv_save_stream": [_vp, _i32, _vp, _sz, _vp],
@@ -77,6 +78,7 @@ _SIGS = {
     "rkv_rope_cossin": [_vp, _i32, _i32, _f64, _vp, _vp],
     "rkv_gen_tokens": [_u64, _u32, _i32, _i32, _i64, _i32, _i32, _f32, _vp, _vp],
     "rkv_gen_step_inputs": [_vp, _u64, _i32, _f32, _vp, _vp, _vp, _vp],
+    "rkv_gen_next_inputs": [_vp, _u64, C.POINTER(_i32), _i32, _f32, _vp, _vp, _vp, _vp],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -215,6 +217,13 @@ def rkv_get_stream_state(h: int, stream_id: int, stream=None) -> list:
     return list(out)
 
 
+def rkv_check_stream_state(cfg: rkv_config, state) -> None:
+    vals = [int(x) for x in state]
+    if len(vals) != RKV_STATE_FIELDS:
+        raise ValueError(f"{RKV_STATE_FIELDS} state fields expected")
+    _check(_lib.rkv_check_stream_state(C.byref(cfg), (_i64 * RKV_STATE_FIELDS)(*vals)))
+
+
 def rkv_sync_status(h: int, stream=None) -> None:
     _check(_lib.rkv_sync_status(h, _stream(stream)), h)
 
@@ -235,3 +244,8 @@ def rkv_gen_tokens(seed: int, tag: int, stream_id: int, layer: int, token0: int,
 
 def rkv_gen_step_inputs(h: int, seed: int, layer: int, scale: float, q, k, v, stream=None) -> None:
     _check(_lib.rkv_gen_step_inputs(h, seed, layer, scale, _ptr(q), _ptr(k), _ptr(v), _stream(stream)), h)
+
+
+def rkv_gen_next_inputs(h: int, seed: int, active_ids, scale: float, q, k, v, stream=None) -> None:
+    ids, n = _i32_array(active_ids)
+    _check(_lib.rkv_gen_next_inputs(h, seed, ids, n, scale, _ptr(q), _ptr(k), _ptr(v), _stream(stream)), h)

@@ -359,7 +359,7 @@ int rkv_decode_attn(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv_bf16* o
   if (!h->appended[layer]) return fail(h, RKV_ERR_STATE, "rkv_decode_attn before rkv_append_rope for this layer");
   if (rkv::exact_scheme(h->cfg.scheme) && !h->rebased[layer])
     return fail(h, RKV_ERR_STATE, "rkv_decode_attn before rkv_rebase for this layer");
-  cudaError_t e = rkv::launch_decode_attn(h->view, h->n_active, layer, 1, q, out, lse, 0, 0,
+  cudaError_t e = rkv::launch_decode_attn(h->view, h->n_active, layer, 1, q, out, lse, 0, 0, false,
                                           static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(h, e, "decode_attn launch");
   return RKV_OK;
@@ -381,7 +381,7 @@ int rkv_decode_attn_layers(rkv_handle* h, int32_t layer0, int32_t n_layers, cons
   const rkv_config& c = h->cfg;
   const int64_t rows = static_cast<int64_t>(h->n_active) * c.q_per_step;
   cudaError_t e = rkv::launch_decode_attn(h->view, h->n_active, layer0, n_layers, q, out, lse,
-                                          rows * c.n_q_heads * c.head_dim, rows * c.n_q_heads,
+                                          rows * c.n_q_heads * c.head_dim, rows * c.n_q_heads, false,
                                           static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(h, e, "decode_attn launch");
   return RKV_OK;
@@ -408,7 +408,8 @@ int rkv_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active, const r
   e = rkv::launch_append_rope(h->view, n_active, 0, c.n_layers, k, v, kv_stride, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "append_rope launch");
   std::fill(h->appended.begin(), h->appended.end(), 1);
-  e = rkv::launch_decode_attn(h->view, n_active, 0, c.n_layers, q, out, lse, q_stride, lse_stride, st);
+  // q was written before this call, three launches back: the kernel may read it before its wait
+  e = rkv::launch_decode_attn(h->view, n_active, 0, c.n_layers, q, out, lse, q_stride, lse_stride, true, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "decode_attn launch");
   return RKV_OK;
 }
@@ -511,9 +512,8 @@ int rkv_load_stream(rkv_handle* h, int32_t stream_id, const void* src, size_t by
   snap_header(h, stream_id, want);
   if (std::memcmp(hdr, want, sizeof hdr) != 0)
     return fail(h, RKV_ERR_CONFIG, "snapshot taken under another configuration, window or scheme");
-  if (state[rkv::F_N] < 0 ||
-      state[rkv::F_LEN] < 0 || state[rkv::F_LEN] > state[rkv::F_W])
-    return fail(h, RKV_ERR_CONFIG, "snapshot state is inconsistent");
+  if (rkv_check_stream_state(&h->cfg, state) != RKV_OK)
+    return fail(h, RKV_ERR_CONFIG, std::string("snapshot state is inconsistent: ") + g_last_error);
   // the window is part of the stream's layout: it must be the slot's own
   int64_t w_dev = 0;
   e = cudaMemcpyAsync(&w_dev, h->view.state + static_cast<int64_t>(stream_id) * rkv::kStateFields + rkv::F_W,
@@ -530,6 +530,30 @@ int rkv_load_stream(rkv_handle* h, int32_t stream_id, const void* src, size_t by
       e = cudaMemcpyAsync(snap_run(h, stream_id, r, l), sp + off, run, cudaMemcpyDefault, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   return e == cudaSuccess ? RKV_OK : cuda_fail(h, e, "loading a stream");
+}
+
+int rkv_check_stream_state(const rkv_config* cfg, const int64_t* st) {
+  std::string why;
+  if (!cfg || !st) return fail(nullptr, RKV_ERR_INVALID_ARG, "config or state is NULL");
+  if (!validate_config(cfg, &why)) return fail(nullptr, RKV_ERR_CONFIG, why);
+  const int64_t n = st[rkv::F_N], len = st[rkv::F_LEN], ev = st[rkv::F_EVICTED], off = st[rkv::F_KV_POS_OFFSET];
+  const int64_t rb = st[rkv::F_ROPE_BASE], head = st[rkv::F_HEAD_SLOT], w = st[rkv::F_W], p0 = st[rkv::F_P0];
+  const int64_t kMaxPos = int64_t(1) << 52;
+  auto bad = [&](const char* m) { return fail(nullptr, RKV_ERR_CONFIG, m); };
+  if (w < cfg->q_per_step || w > RKV_MAX_WINDOW) return bad("window outside [q_per_step, RKV_MAX_WINDOW]");
+  if (p0 < 0 || p0 >= kMaxPos) return bad("P0 outside [0, 2^52)");
+  if (n < 0 || n % cfg->q_per_step != 0 || n >= kMaxPos - p0) return bad("token count n negative, not a multiple of q_per_step, or past 2^52");
+  if (len != (n < w ? n : w)) return bad("len differs from min(n, W)");
+  if (ev != n - len) return bad("evicted differs from n - len");
+  if (off != p0 + ev) return bad("kv_pos_offset differs from P0 + evicted");
+  if (head != ev % w) return bad("head_slot differs from evicted mod W");
+  if (rkv::exact_scheme(cfg->scheme)) {
+    if (rb < 0 || rb > ev || ev - rb >= cfg->rebase_interval)
+      return bad("rope_base outside (evicted - rebase_interval, evicted]");
+  } else if (rb != 0) {
+    return bad("rope_base must be 0 in the offset-only scheme");
+  }
+  return RKV_OK;
 }
 
 int rkv_get_stream_state(rkv_handle* h, int32_t stream_id, int64_t* out, void* stream) {
@@ -598,6 +622,22 @@ int rkv_gen_step_inputs(rkv_handle* h, uint64_t seed, int32_t layer, float scale
   cudaError_t e = rkv::launch_gen_step_inputs(h->view, h->n_active, seed, layer, scale, q, k, v,
                                               static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? RKV_OK : cuda_fail(h, e, "gen_step_inputs launch");
+}
+
+int rkv_gen_next_inputs(rkv_handle* h, uint64_t seed, const int32_t* active_ids, int32_t n_active, float scale,
+                        rkv_bf16* q, rkv_bf16* k, rkv_bf16* v, void* stream) {
+  if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
+  if (!q || !k || !v) return fail(h, RKV_ERR_INVALID_ARG, "q, k, v must be non-NULL");
+  if (!active_ids || n_active < 1 || n_active > h->cfg.n_streams)
+    return fail(h, RKV_ERR_INVALID_ARG, "active_ids must list 1 .. n_streams streams");
+  rkv::ActiveIds ids;
+  ids.n = n_active;
+  for (int i = 0; i < n_active; ++i) {
+    if (active_ids[i] < 0 || active_ids[i] >= h->cfg.n_streams) return fail(h, RKV_ERR_INVALID_ARG, "stream id out of range");
+    ids.id[i] = active_ids[i];
+  }
+  cudaError_t e = rkv::launch_gen_next_inputs(h->view, ids, seed, scale, q, k, v, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RKV_OK : cuda_fail(h, e, "gen_next_inputs launch");
 }
 
 int rkv_decode_attn_static(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv_bf16* out, float* lse,

@@ -64,6 +64,9 @@ struct AttnArgs {
   int layer0, n_layers, n_active;
   int splits, stages_per_split;
   int mode;            // 0: whole windows; 1: split, cluster merge; 2: split, partials to part_ml / part_o
+  int q_early;         // 1: q was written two or more launches back and may be read before the
+                       // dependency wait (rkv_step); 0: q is read after it, since the caller's
+                       // kernel that wrote q may be this launch's immediate predecessor
 };
 
 // 2^x with the hardware approximation (relative error about 2^-22; subnormal
@@ -481,12 +484,15 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
     }
     QPrefetch<D> pf;
     StepDesc dnext;
-    if (u_first < n_units) {  // queries and descriptors: written two or more launches back
+    // descriptors and angles come from the begin-step kernel, two or more launches back; the
+    // queries only when the launcher says so (args.q_early), else after the wait
+    if (u_first < n_units) {
       const Unit un0 = unit_of(u_first, n_active, hkv);
-      q_prefetch<D>(args, un0, tid, pf);
+      if (args.q_early) q_prefetch<D>(args, un0, tid, pf);
       dnext = v.desc[un0.a];
     }
     pdl_wait();
+    if (u_first < n_units && !args.q_early) q_prefetch<D>(args, unit_of(u_first, n_active, hkv), tid, pf);
     int k0 = 0;  // ring position of the unit's first stage
     for (int u = u_first; u < n_units; u += u_step) {
       const Unit un = unit_of(u, n_active, hkv);
@@ -938,6 +944,8 @@ AttnArgs make_args(const DevView& v, int n_active, int layer0, int n_layers, con
   args.n_active = n_active;
   args.splits = p.splits;
   args.stages_per_split = p.stages_per_split;
+  args.mode = 0;
+  args.q_early = 0;
   return args;
 }
 
@@ -974,9 +982,10 @@ AttnPlan plan_decode_attn(const DevView& v, int n_active, int n_layers, bool clu
 
 cudaError_t launch_decode_attn(const DevView& v, int n_active, int layer0, int n_layers, const uint16_t* q,
                                uint16_t* out, float* lse, int64_t q_layer_stride, int64_t lse_layer_stride,
-                               cudaStream_t st) {
+                               bool q_early, cudaStream_t st) {
   const AttnPlan p = plan_decode_attn(v, n_active, n_layers, true);
   AttnArgs args = make_args(v, n_active, layer0, n_layers, q, out, lse, q_layer_stride, lse_layer_stride, p);
+  args.q_early = q_early ? 1 : 0;
   const int64_t units = static_cast<int64_t>(n_active) * v.n_kv_heads * n_layers;
   args.mode = p.cluster ? 1 : 0;
   const int64_t grid = p.cluster ? units * p.splits : (units < p.slots ? units : p.slots);
@@ -989,6 +998,7 @@ cudaError_t launch_decode_attn_scratch(const DevView& v, int n_active, int layer
   AttnArgs args = make_args(v, n_active, layer, 1, q, out, lse, 0, 0, p);
   const int64_t units = static_cast<int64_t>(n_active) * v.n_kv_heads;
   args.mode = p.splits > 1 ? 2 : 0;
+  args.q_early = 0;
   const int64_t grid = p.splits > 1 ? units * p.splits : (units < p.slots ? units : p.slots);
   cudaError_t e = dispatch(args, static_cast<int>(grid), st);
   if (e != cudaSuccess || p.splits == 1) return e;

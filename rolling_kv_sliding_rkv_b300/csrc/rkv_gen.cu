@@ -50,9 +50,13 @@ __global__ void gen_tokens_kernel(uint64_t seed, uint32_t tag, int32_t stream, i
     out[static_cast<int64_t>(t) * width + e] = draw(key, e, scale);
 }
 
-// grid (A * Q, 3): tensor 0 = q [A][Q][Hq][d], 1 = k, 2 = v [A][Q][Hkv][d]
+// grid (A * Q, 3): tensor 0 = q [A][Q][Hq][d], 1 = k, 2 = v [A][Q][Hkv][d].  Launched with
+// programmatic dependent launch and letting its dependents start before it writes, as a
+// caller's own kernel that produces the queries of a layer may be.
 __global__ void gen_step_kernel(DevView v, uint64_t seed, int32_t layer, float scale, uint16_t* __restrict__ q,
                                 uint16_t* __restrict__ k, uint16_t* __restrict__ vv) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int row = blockIdx.x;
   const int a = row / v.q_per_step, t = row % v.q_per_step;
   const int which = blockIdx.y;
@@ -64,7 +68,30 @@ __global__ void gen_step_kernel(DevView v, uint64_t seed, int32_t layer, float s
   for (int e = threadIdx.x; e < width; e += blockDim.x) dst[e] = draw(key, e, scale);
 }
 
+// The inputs of the next step of the listed streams, all layers: grid (A * Q, 3, L), token
+// index = the stream's token count before that step (read from the device state).
+__global__ void gen_next_kernel(DevView v, ActiveIds ids, uint64_t seed, float scale, uint16_t* __restrict__ q,
+                                uint16_t* __restrict__ k, uint16_t* __restrict__ vv) {
+  const int row = blockIdx.x;
+  const int a = row / v.q_per_step, t = row % v.q_per_step;
+  const int which = blockIdx.y, layer = blockIdx.z;
+  const int s = ids.id[a];
+  const int64_t n = v.state[static_cast<int64_t>(s) * kStateFields + F_N];
+  const int heads = which == 0 ? v.n_q_heads : v.n_kv_heads;
+  const int width = heads * v.head_dim;
+  const int64_t rows = static_cast<int64_t>(ids.n) * v.q_per_step;
+  uint16_t* dst = (which == 0 ? q : which == 1 ? k : vv) + (layer * rows + row) * width;
+  const uint64_t key = token_key(seed, static_cast<uint32_t>(which + 1), s, layer, n + t);
+  for (int e = threadIdx.x; e < width; e += blockDim.x) dst[e] = draw(key, e, scale);
+}
+
 }  // namespace
+
+cudaError_t launch_gen_next_inputs(const DevView& v, const ActiveIds& ids, uint64_t seed, float scale, uint16_t* q,
+                                   uint16_t* k, uint16_t* vv, cudaStream_t st) {
+  gen_next_kernel<<<dim3(ids.n * v.q_per_step, 3, v.n_layers), 256, 0, st>>>(v, ids, seed, scale, q, k, vv);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gen_tokens(uint64_t seed, uint32_t tag, int32_t stream_id, int32_t layer, int64_t token0,
                               int32_t n_tokens, int32_t width, float scale, uint16_t* out, cudaStream_t st) {
@@ -76,8 +103,8 @@ cudaError_t launch_gen_tokens(uint64_t seed, uint32_t tag, int32_t stream_id, in
 
 cudaError_t launch_gen_step_inputs(const DevView& v, int n_active, uint64_t seed, int32_t layer, float scale,
                                    uint16_t* q, uint16_t* k, uint16_t* vv, cudaStream_t st) {
-  gen_step_kernel<<<dim3(n_active * v.q_per_step, 3), 256, 0, st>>>(v, seed, layer, scale, q, k, vv);
-  return cudaGetLastError();
+  return launch_pdl(gen_step_kernel, dim3(n_active * v.q_per_step, 3), dim3(256), 0, st, v, seed, layer, scale, q, k,
+                    vv);
 }
 
 }  // namespace rkv

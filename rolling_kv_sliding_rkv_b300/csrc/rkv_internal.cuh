@@ -78,7 +78,9 @@ struct ActiveIds {
 // its own dependents launch, so when any of them starts, every kernel two
 // launches back has completed: a kernel may read, before its own wait, data
 // that only those earlier kernels write (the step descriptors, the page table,
-// the caller's queries), never data its immediate predecessor may write.  A
+// the caller's queries inside rkv_step, which were written before the call),
+// never data its immediate predecessor may write (a caller's kernel that
+// writes the queries just before rkv_decode_attn, for instance).  A
 // dependent grid launches only after every CTA of its predecessor has
 // started, so waiting CTAs never hold resources the predecessor still needs.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -175,7 +177,7 @@ struct AttnPlan {
 AttnPlan plan_decode_attn(const DevView& v, int n_active, int n_layers, bool cluster);
 cudaError_t launch_decode_attn(const DevView& v, int n_active, int layer0, int n_layers, const uint16_t* q,
                                uint16_t* out, float* lse, int64_t q_layer_stride, int64_t lse_layer_stride,
-                               cudaStream_t st);
+                               bool q_early, cudaStream_t st);
 // the split-K form with partials in v.part_ml / v.part_o (one layer)
 cudaError_t launch_decode_attn_scratch(const DevView& v, int n_active, int layer, const uint16_t* q, uint16_t* out,
                                        float* lse, cudaStream_t st);
@@ -188,6 +190,8 @@ cudaError_t launch_rope_cossin(const int64_t* pos, int n, int head_dim, const Om
                                cudaStream_t st);
 cudaError_t launch_gen_tokens(uint64_t seed, uint32_t tag, int32_t stream_id, int32_t layer, int64_t token0,
                               int32_t n_tokens, int32_t width, float scale, uint16_t* out, cudaStream_t st);
+cudaError_t launch_gen_next_inputs(const DevView& v, const ActiveIds& ids, uint64_t seed, float scale, uint16_t* q,
+                                   uint16_t* k, uint16_t* vv, cudaStream_t st);
 cudaError_t launch_gen_step_inputs(const DevView& v, int n_active, uint64_t seed, int32_t layer, float scale,
                                    uint16_t* q, uint16_t* k, uint16_t* vv, cudaStream_t st);
 

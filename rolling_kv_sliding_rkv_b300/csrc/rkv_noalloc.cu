@@ -1,14 +1,15 @@
-// rkv_decode_attn_static: decode attention whose split-K scratch lives in a
-// fixed array inside the library instead of the handle's state buffer.
+// rkv_decode_attn_static: decode attention whose split-K partials live in a
+// fixed array inside the library, so the call allocates nothing.
 //
 // Who needs it: code that may not allocate device memory at the point where
 // it runs attention.  A real-time audio callback has a clock-step budget of
 // 80 ms and cannot afford an allocator call that may synchronise the device;
 // a plug-in hosted by a serving engine whose caching allocator has already
 // reserved the free HBM has no memory of its own to ask for.  Such callers
-// pass only inputs and outputs here; the partial results go to the array
-// below, which every process that loads the library holds on every device it
-// uses until exit.
+// pass only inputs and outputs here; the partial results of a window split
+// over several CTAs go to the array below, which every process that loads the
+// library holds on every device it uses until exit.  A call whose windows are
+// not split writes its outputs directly and touches the array not at all.
 #include <mutex>
 
 #include "rkv_internal.cuh"
@@ -43,13 +44,15 @@ cudaError_t scratch_address(float** out) {
   return cudaSuccess;
 }
 
-size_t partial_rows(const DevView& v, int n_active) {
-  const AttnPlan p = plan_decode_attn(v, n_active, 1, false);
+// Partial rows of one call: one per (active stream, query row, split), none when the plan
+// does not split the windows (the kernel then writes out and lse itself).
+size_t partial_rows(const AttnPlan& p, const DevView& v, int n_active) {
+  if (p.splits <= 1) return 0;
   return static_cast<size_t>(n_active) * v.q_per_step * v.n_q_heads * p.splits;
 }
 
-size_t ml_floats(const DevView& v, int n_active) {
-  return (partial_rows(v, n_active) * 2 + 63) / 64 * 64;  // keeps the outputs that follow 256-byte aligned
+size_t ml_floats(size_t rows) {
+  return (rows * 2 + 63) / 64 * 64;  // keeps the outputs that follow 256-byte aligned
 }
 
 }  // namespace
@@ -57,7 +60,8 @@ size_t ml_floats(const DevView& v, int n_active) {
 size_t static_scratch_floats() { return kStaticScratchFloats; }
 
 size_t static_scratch_need(const DevView& v, int n_active) {
-  return ml_floats(v, n_active) + partial_rows(v, n_active) * v.head_dim;
+  const size_t rows = partial_rows(plan_decode_attn(v, n_active, 1, false), v, n_active);
+  return rows == 0 ? 0 : ml_floats(rows) + rows * v.head_dim;
 }
 
 cudaError_t launch_decode_attn_static(const DevView& v, int n_active, int layer, const uint16_t* q, uint16_t* out,
@@ -65,9 +69,10 @@ cudaError_t launch_decode_attn_static(const DevView& v, int n_active, int layer,
   float* base = nullptr;
   cudaError_t e = scratch_address(&base);
   if (e != cudaSuccess) return e;
+  const size_t rows = partial_rows(plan_decode_attn(v, n_active, 1, false), v, n_active);
   DevView w = v;
   w.part_ml = base;
-  w.part_o = base + ml_floats(v, n_active);
+  w.part_o = base + ml_floats(rows);
   return launch_decode_attn_scratch(w, n_active, layer, q, out, lse, st);
 }
 

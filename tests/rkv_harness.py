@@ -27,14 +27,18 @@ class Run:
     ring: dict = field(default_factory=dict)      # stream -> oracle StreamRing after the run
 
 
-def run_gpu(wl: synth.Workload, n_ticks: int, want: set, streams_of_interest=None, whole_step=False):
+def run_gpu(wl: synth.Workload, n_ticks: int, want: set, streams_of_interest=None, whole_step=False,
+            attn="regular"):
     """Run `n_ticks` steps (ticks for the mixed-clock workload) and copy sampled outputs.
 
     want: set of (stream, layer, n_old) to record, n_old = the stream's token
     count before the step.  A mixed-clock workload first brings every stream
     to its initial fill with extra steps of the lagging streams.
     whole_step: drive rkv_step (all layers per launch) instead of the
-    per-layer calls; the inputs are the same generator draws.
+    per-layer calls; the inputs are the same generator draws
+    (rkv_gen_next_inputs, every layer of the step in one launch).
+    attn: "regular" (rkv_decode_attn) or "static" (rkv_decode_attn_static) for
+    the per-layer calls.
     """
     import torch
 
@@ -80,13 +84,7 @@ def run_gpu(wl: synth.Workload, n_ticks: int, want: set, streams_of_interest=Non
         for s in active:
             rings[s].step()
         nqe, nke = a * Q * hq * d, a * Q * hkv * d
-        for layer in range(L):
-            for idx, s in enumerate(active):
-                for tag, buf, width in ((synth.TAG_Q, qa, hq * d), (synth.TAG_K, ka, hkv * d),
-                                        (synth.TAG_V, va, hkv * d)):
-                    base = layer * (nqe if tag == synth.TAG_Q else nke) + idx * Q * width
-                    rkv.rkv_gen_tokens(wl.seed, tag, s, layer, n_old[s], Q, width, wl.input_scale,
-                                       buf[base:base + Q * width])
+        h.gen_next_inputs(wl.seed, active, wl.input_scale, qa, ka, va)
         h.step(active, qa[: L * nqe], ka[: L * nke], va[: L * nke], outa[: L * nqe], lsea[: L * a * Q * hq])
         for layer in range(L):
             record(active, n_old, layer, outa[layer * nqe:], lsea[layer * a * Q * hq:])
@@ -104,7 +102,10 @@ def run_gpu(wl: synth.Workload, n_ticks: int, want: set, streams_of_interest=Non
             if exact:
                 h.rebase(layer)
             h.append_rope(layer, k, v)
-            h.decode_attn(layer, q, out, lse)
+            if attn == "static":
+                rkv.rkv_decode_attn_static(h.handle, layer, q, out, lse)
+            else:
+                h.decode_attn(layer, q, out, lse)
             record(active, n_old, layer, out, lse)
 
     # initial fill (ragged), one extra step at a time for the streams still short of it

@@ -108,3 +108,34 @@ def test_null_handle_is_rejected():
         with pytest.raises(rkv.RkvError) as e:
             call()
         assert e.value.code == rkv.RKV_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("scheme,interval,q", [(0, 1, 1), (1, 1, 1), (1, 5, 1), (2, 3, 1), (0, 1, 4)])
+def test_stream_state_check(scheme, interval, q):
+    """States the integer ring model reaches are accepted; one field off by one is rejected."""
+    from oracle.ring import StreamRing
+    cfg = _cfg(n_streams=1, scheme=scheme, rebase_interval=interval, q_per_step=q,
+               n_q_heads=4 if q > 1 else 16, n_kv_heads=4 if q > 1 else 2)
+    w, p0 = 12, 2 ** 40 + 3
+    ring = StreamRing(w, p0, q, 1 if scheme else 0, interval)
+    checked = 0
+    for _ in range(40):
+        st = ring.state()
+        rkv.rkv_check_stream_state(cfg, st)
+        for i in range(len(st)):
+            for dlt in (-1, 1):
+                bad = list(st)
+                bad[i] += dlt
+                if i == 4 and scheme and 0 <= bad[4] <= bad[2] and bad[2] - bad[4] < interval:
+                    continue        # rope_base has slack of its own between re-bases
+                if i == 6 and st[0] <= w:
+                    continue        # before the window fills, W is fixed only by the stream's pages
+                with pytest.raises(rkv.RkvError) as e:
+                    rkv.rkv_check_stream_state(cfg, bad)
+                assert e.value.code == rkv.RKV_ERR_CONFIG
+                checked += 1
+        ring.step()
+    assert checked > 400
+    for bad in ([0, 0, 0, -1, 0, 0, w, -1], [0, 0, 0, 2 ** 52, 0, 0, w, 2 ** 52]):   # P0 outside [0, 2^52)
+        with pytest.raises(rkv.RkvError):
+            rkv.rkv_check_stream_state(cfg, bad)

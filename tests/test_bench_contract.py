@@ -99,3 +99,7 @@ def test_reference_arm_prints_one_line():
     line = json.loads(out.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "stream-steps/s"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    # the same workload description as the GPU arm's line, and a per-step time of the steps it ran
+    wl = synth.workload("tiny")
+    assert line["config"]["workload"] == bench.describe(wl, bench.SCHEME_NAMES[wl.scheme])
+    assert 0 < line["ms_per_step"] * line["steps"] < 600e3

@@ -43,3 +43,36 @@ def test_rope_cos_sin_exact_at_large_positions(rkv, head_dim):
     # fp32 rounding of an fp64 value accurate to ~1e-15: within 2^-24 relative plus a hair
     assert np.abs(got[..., 0] - c).max() < 1.2e-7
     assert np.abs(got[..., 1] - s).max() < 1.2e-7
+
+
+def test_next_step_generator_bit_identical(rkv):
+    """rkv_gen_next_inputs: every layer of the next step of a subset of streams, in rkv_step's layout,
+    with each stream's token index read from the device state (streams at different counts)."""
+    import torch
+    L, S, hq, hkv, d, Q = 3, 5, 8, 2, 64, 2
+    h = rkv.RollingKV([16] * S, [0] * S, n_layers=L, n_streams=S, n_q_heads=hq, n_kv_heads=hkv, head_dim=d,
+                      q_per_step=Q, scheme=0, page_size=16)
+    zq = torch.zeros(S, Q, hq, d, dtype=torch.bfloat16, device="cuda")
+    zk = torch.zeros(S, Q, hkv, d, dtype=torch.bfloat16, device="cuda")
+    counts = [0] * S
+    for active in ([0, 1, 2, 3, 4], [1, 3], [3]):     # streams 0..4 at 2, 4, 2, 6, 2 tokens
+        h.begin_step(active)
+        for layer in range(L):
+            h.append_rope(layer, zk, zk)
+        for s in active:
+            counts[s] += Q
+    h.sync_status()
+    active = [3, 0, 1]
+    seed, scale = 99, 0.5
+    q = torch.empty(L, len(active), Q, hq, d, dtype=torch.bfloat16, device="cuda")
+    k = torch.empty(L, len(active), Q, hkv, d, dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    h.gen_next_inputs(seed, active, scale, q, k, v)
+    torch.cuda.synchronize()
+    for tag, buf, heads in ((synth.TAG_Q, q, hq), (synth.TAG_K, k, hkv), (synth.TAG_V, v, hkv)):
+        got = buf.view(torch.int16).cpu().numpy().view(np.uint16)
+        for layer in range(L):
+            for a, s in enumerate(active):
+                want = synth.token_tensor(seed, tag, s, layer, range(counts[s], counts[s] + Q), heads, d, scale)
+                assert np.array_equal(got[layer, a], np.asarray(want).reshape(Q, heads, d)), (tag, layer, s)
+    h.close()

@@ -80,6 +80,14 @@ def test_small_every_output(case):
     print(case, "max out err", e_o, "max lse err", e_l)
 
 
+def final_counts(wl, n_ticks):
+    """Token count of every stream after the harness's initial fill and `n_ticks` ticks."""
+    counts = wl.initial_fill().copy()
+    for t in range(n_ticks):
+        counts[wl.active_at_tick(t)] += 1
+    return counts * wl.q_per_step
+
+
 FULL = {
     "tiny": ("tiny", dict(), 1000, [0, 1, 374, 375, 376, 998, 999], [0]),
     "qwen": ("qwen", dict(), 1000, [0, 1, 374, 375, 376, 999], [0, 17, 40, 63]),
@@ -92,24 +100,44 @@ FULL = {
     # the most streams a handle takes (RKV_MAX_STREAMS)
     "max_streams": ("qwen", dict(n_layers=1, n_streams=1024, extra={"window": 40}), 50, [0, 39, 40, 49],
                     [0, 511, 1023]),
+    # the timed path itself: rkv_step over every layer (the persistent all-layers launches after the
+    # re-base in reverse layer order), at the benchmark's shapes
+    "qwen_step": ("qwen", dict(), 1000, [0, 374, 375, 376, 999], [0, 17, 40, 63], True),
+    "qwen_step_on_read": ("qwen", dict(scheme=2), 1000, [0, 374, 375, 376, 999], [0, 17, 40, 63], True),
+    # mixed clocks: windows of 375 / 250 / 188 filled from ragged starts, then two 12-tick schedule
+    # periods more; one stream of each clock and one more 80 ms stream
+    "mixed_step": ("mixed", dict(), 510, "schedule", [0, 1, 2, 3], True),
+    "encoder_step": ("encoder", dict(), 200, [0, 4, 744, 748, 752, 796], [0, 31], True),
 }
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("case", sorted(FULL))
 def test_full_size_sampled(case):
-    name, over, ticks, steps, streams = FULL[case]
+    name, over, ticks, steps, streams, *opt = FULL[case]
+    whole_step = bool(opt and opt[0])
     wl = synth.workload(name, **over)
     layers = sorted({0, wl.n_layers // 2, wl.n_layers - 1})
+    final = final_counts(wl, ticks)
+    fill = wl.initial_fill() * wl.q_per_step
+    w = wl.windows()
     want = set()
-    if steps is None:   # mixed clocks: sample every 37th token of the chosen streams
-        steps = list(range(0, 500, 37))
     for s in streams:
+        if steps is None:        # mixed clocks: every 37th token of the chosen streams
+            mine = range(0, 500, 37)
+        elif steps == "schedule":  # the fill, the window's edge and the last two steps the run reaches
+            mine = {0, int(fill[s]) - 1, int(fill[s]), int(w[s]) - 1, int(w[s]), int(w[s]) + 1,
+                    int(final[s]) - 2, int(final[s]) - 1}
+        else:
+            mine = steps
         for layer in layers:
-            for n_old in steps:
-                want.add((s, layer, n_old))
-    run = run_gpu(wl, ticks, want, streams_of_interest=streams)
-    assert len(run.samples) >= len(want) // 2
+            for n_old in mine:
+                if 0 <= n_old < final[s] and n_old % wl.q_per_step == 0:
+                    want.add((s, layer, n_old))
+    if steps == "schedule":
+        assert all(final[s] >= w[s] + 2 for s in streams)   # every chosen window filled and rolled
+    run = run_gpu(wl, ticks, want, streams_of_interest=streams, whole_step=whole_step)
+    assert set(run.samples) == want
     e_o, e_l = compare(run, wl)
     for s in streams:
         assert list(run.states[s].values()) == run.ring[s].state()
