@@ -350,13 +350,15 @@ def step_phases(wl):
     return [wl.active_at_tick(t).tolist() for t in range(period)]
 
 
-def measure(wl, args, dev, rank, world, timed=True, p0=None, attention=True, per_layer_step=False):
+def measure(wl, args, dev, rank, world, timed=True, p0=None, attention=True, per_layer_step=False, churn=0):
     """Time the step of workload `wl` on this GPU; returns the figures of one JSON line.
 
     p0: start offset given to every stream (default: the workload's draws).
     per_layer_step: also time the same steps made of per-layer calls (begin step, then for each
     layer re-base, append and decode attention), one CUDA graph per step, as a model that runs
-    other work between its layers must call them."""
+    other work between its layers must call them.
+    churn: streams that leave per step, their slots taken at once by new streams with new start
+    offsets (rkv_reset_streams from a device-side schedule the graphs walk through)."""
     import torch
 
     import rolling_kv_sliding_rkv_b300 as rkv
@@ -387,25 +389,46 @@ def measure(wl, args, dev, rank, world, timed=True, p0=None, attention=True, per
         sets.append(bufs)
     torch.cuda.synchronize()
 
+    churn_state = None
+    if churn:
+        # a schedule of leave/join events: row t lists `churn` distinct slots and their new start
+        # offsets; every step takes the next row (a device-side counter), so a replayed graph
+        # resets different slots each time
+        T = 4096
+        t_idx = torch.arange(T * churn, dtype=torch.int64).view(T, churn)
+        churn_state = {"ids": ((t_idx * 97 + 13) % S).to(torch.int32).to(dev),
+                       "p0": ((t_idx * 1_000_003 + 7) % (2 ** 40)).to(dev),
+                       "ctr": torch.zeros(1, dtype=torch.int64, device=dev),
+                       "cur_ids": torch.empty(churn, dtype=torch.int32, device=dev),
+                       "cur_p0": torch.empty(churn, dtype=torch.int64, device=dev), "T": T}
+
+    def whole_step(act, b):
+        if churn_state is not None:
+            c = churn_state
+            torch.index_select(c["ids"], 0, c["ctr"], out=c["cur_ids"].view(1, -1))
+            torch.index_select(c["p0"], 0, c["ctr"], out=c["cur_p0"].view(1, -1))
+            c["ctr"].add_(1).remainder_(c["T"])
+            h.reset_streams(c["cur_ids"], c["cur_p0"])
+        h.step(act, b["q"], b["k"], b["v"], b["out"], b["lse"])
+
     stream = torch.cuda.Stream()
     graphs = []
     with torch.cuda.stream(stream):
         for r, act in enumerate(plan):   # eager warm-up of the capture stream
             if act:
-                b = sets[r]
-                h.step(act, b["q"], b["k"], b["v"], b["out"], b["lse"])
+                whole_step(act, sets[r])
         stream.synchronize()
         for r, act in enumerate(plan):
             if not act:
                 graphs.append(None)
                 continue
-            b = sets[r]
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                h.step(act, b["q"], b["k"], b["v"], b["out"], b["lse"])
+                whole_step(act, sets[r])
             graphs.append(g)
-    # begin step, re-base (exact re-base scheme), append, decode attention: each one launch over all layers
-    launches_per_step = 1 + (1 if wl.scheme == 1 else 0) + 1 + 1
+    # begin step, re-base (materialised exact re-base), RoPE + append, decode attention: each one
+    # launch over all layers
+    launches_per_step = 1 + (1 if wl.scheme == 1 else 0) + 1 + 1 + (1 if churn else 0)
 
     # fill every window, then warm up: steady state before timing
     slowest = max(int(c) // max(wl.tick_ms, 1) for c in wl.stream_clocks()) if wl.tick_ms else 1
@@ -463,9 +486,9 @@ def measure(wl, args, dev, rank, world, timed=True, p0=None, attention=True, per
             for layer in range(L):
                 if wl.scheme in (1, 2):
                     h.rebase(layer)
-                h.append_rope(layer, b["k"][layer * A * Q * hkv * d:], b["v"][layer * A * Q * hkv * d:])
-                h.decode_attn(layer, b["q"][layer * A * Q * hq * d:], b["out"][layer * A * Q * hq * d:],
-                              b["lse"][layer * A * Q * hq:])
+                h.append_decode_attn(layer, b["q"][layer * A * Q * hq * d:], b["k"][layer * A * Q * hkv * d:],
+                                     b["v"][layer * A * Q * hkv * d:], b["out"][layer * A * Q * hq * d:],
+                                     b["lse"][layer * A * Q * hq:])
         lgraphs = []
         with torch.cuda.stream(stream):
             for r, act in enumerate(plan):
@@ -493,12 +516,13 @@ def measure(wl, args, dev, rank, world, timed=True, p0=None, attention=True, per
         lms = ev0.elapsed_time(ev1)
         h.sync_status()
         ljob = aggregate(lms, sum(len(plan[i % R]) for i in range(args.steps)), world, dev)
-        per_step_launches = 1 + L * (2 + (1 if wl.scheme == 1 else 0))
+        per_step_launches = 1 + L * (1 + (1 if wl.scheme == 1 else 0))
         out["per_layer_step"] = {
             "value": ljob["value"], "unit": UNIT, "ms_per_step": ljob["ms"] / args.steps,
             "launches_per_step": per_step_launches,
             "how": "the same steps as one CUDA graph of per-layer calls each: begin step, then for every layer "
-                   "re-base (exact re-base scheme), RoPE + append and decode attention"}
+                   "re-base (materialised exact re-base) and decode attention with the append fused "
+                   "(rkv_append_decode_attn)"}
     if not attention:
         return out
 
@@ -655,6 +679,15 @@ def run_ours(args):
                 "decode_attn_frac": vm["attn_bytes"] / (vm["attn_all_ms"] / 1000.0) / 1e9 / peak}
             if "per_layer_step" in vm:
                 variants[label]["value_per_layer_graph"] = vm["per_layer_step"]["value"]
+        if wl.tick_ms:
+            # serving churn: two streams leave and two new ones join in their slots on every tick
+            cm = measure(wl, args, dev, rank, 1, timed=False, attention=False, churn=2)
+            cm.pop("h").close()
+            variants[f"{SCHEME_NAMES[wl.scheme]}, 2 streams leaving and joining per tick"] = {
+                "value": cm["value"], "unit": UNIT, "ms_per_step": cm["ms"] / args.steps,
+                "how": "each step first resets 2 stream slots to new start offsets (rkv_reset_streams, "
+                       "a device-side schedule walked by the replayed graphs); the new streams start "
+                       "empty windows"}
 
     def flatness(fw, free_delta):
         # cost per step must not depend on how far the streams are into their logical timelines

@@ -45,8 +45,8 @@
  * layer lacks them returns RKV_ERR_STATE.
  *
  * Memory in HBM (pool_dev).  Regions of [L][pages][Hkv][page_size][d]
- * 16-bit elements: rotated keys (fp16; not in RKV_SCHEME_EXACT_ON_READ),
- * values (bf16), and in the exact schemes pre-RoPE keys (bf16).  Stream s
+ * 16-bit elements: rotated keys (fp16), values (bf16), and in
+ * RKV_SCHEME_EXACT_REBASE pre-RoPE keys (bf16).  Stream s
  * owns ceil(W_s / page_size) pages; token j lives in ring slot j mod W_s, so
  * eviction moves no data.  Within a row of d elements the 16-byte chunk c
  * sits at chunk position c ^ (row offset in the page & 7), which makes a
@@ -86,9 +86,12 @@ typedef enum {
 typedef enum {
   RKV_SCHEME_OFFSET_ONLY = 0,  /* K rotated once at P0 + j; kv_pos_offset bookkeeping only */
   RKV_SCHEME_EXACT_REBASE = 1, /* K kept at window-relative positions, re-based on every roll */
-  RKV_SCHEME_EXACT_ON_READ = 2 /* the same window-relative positions and re-base bookkeeping, but the
-                                * rotation R(j - rope_base) is applied to the pre-RoPE key as attention
-                                * reads it, so no re-based key is ever stored (re-base moves no bytes) */
+  RKV_SCHEME_EXACT_ON_READ = 2 /* the same exact positions and re-base bookkeeping, but the re-base is
+                                * applied as attention reads: a key is stored once, rotated by its
+                                * ring slot index j mod W (positions stay below W however long the
+                                * stream runs), and the query is rotated by its offset from the ring
+                                * lap of each key, so no stored key is ever re-rotated (re-base moves
+                                * no bytes) */
 } rkv_scheme;
 
 /* Shape and policy of one handle.  All layers share it. */
@@ -102,7 +105,11 @@ typedef struct {
   int32_t page_size;       /* ring slots per page: 16, 32, 64 or 128 */
   int32_t scheme;          /* rkv_scheme */
   int32_t rebase_interval; /* exact scheme: re-base once this many tokens left (>= 1) */
-  int32_t reserved;        /* must be 0 */
+  int32_t window_slack;    /* ring capacity beyond the window, >= 0: a stream keeps up to C_s =
+                            * W_s + window_slack tokens and, at the step that would exceed C_s,
+                            * evicts down to the last W_s in one batch (the oldest batch leaves
+                            * together); 0 evicts exactly enough on every step (a plain sliding
+                            * window of W_s) */
   double rope_theta;       /* RoPE base theta > 1 (1e6 for the Qwen2.5 decoder) */
   double softmax_scale;    /* score scale; 0 selects 1/sqrt(head_dim) */
 } rkv_config;
@@ -168,11 +175,12 @@ RKV_API int rkv_begin_step(rkv_handle* h, const int32_t* active_ids, int32_t n_a
  *   k  device [A][Q][Hkv][d] bf16, pre-RoPE keys of the new tokens (A =
  *      n_active, rows in active_ids order)
  *   v  device [A][Q][Hkv][d] bf16
- * Writes the key rotated to its position (logical P0 + j, or j - rope_base
- * in the exact scheme) into ring slot (token mod W) of each stream, stored
- * as fp16 (round to nearest even; eleven significant bits, so a stored key
- * adds ~2e-4 to a unit-scale score, where bf16 would add ~1.6e-3), and v as
- * given (bf16), plus the pre-RoPE k in the exact scheme.  A rotated key of
+ * Writes the key rotated to its position (logical P0 + j; j - rope_base in
+ * RKV_SCHEME_EXACT_REBASE; its ring slot j mod W in RKV_SCHEME_EXACT_ON_READ)
+ * into ring slot (token mod W) of each stream, stored as fp16 (round to
+ * nearest even; eleven significant bits, so a stored key adds ~2e-4 to a
+ * unit-scale score, where bf16 would add ~1.6e-3), and v as given (bf16),
+ * plus the pre-RoPE k in RKV_SCHEME_EXACT_REBASE.  A rotated key of
  * magnitude >= 65520 is reported as RKV_ERR_DEVICE_RANGE by rkv_sync_status.
  * Once per layer per step. */
 RKV_API int rkv_append_rope(rkv_handle* h, int32_t layer, const rkv_bf16* k, const rkv_bf16* v,
@@ -186,16 +194,18 @@ RKV_API int rkv_append_rope(rkv_handle* h, int32_t layer, const rkv_bf16* k, con
  * schemes only (RKV_ERR_STATE otherwise); must be called once per layer per
  * step, before rkv_decode_attn of that layer (a no-op on the device for
  * streams that do not re-base this step).  In RKV_SCHEME_EXACT_ON_READ it
- * enqueues nothing: rkv_decode_attn applies the same rotation to every key
- * it reads. */
+ * enqueues nothing: rkv_decode_attn rotates the query by each key's offset
+ * from its ring lap instead, which gives every score the same position
+ * difference. */
 RKV_API int rkv_rebase(rkv_handle* h, int32_t layer, void* stream);
 
 /* Windowed GQA attention for one layer (explainer 第 3 步), split-K over the
  * window with a log-sum-exp merge of the splits in distributed shared memory
  * (no scratch memory).
  *   q     device [A][Q][Hq][d] bf16, pre-RoPE queries of the new tokens;
- *         rotated inside the kernel in fp32 at the same positions as the
- *         step's keys (never rounded back to 16 bits), not modified
+ *         rotated inside the kernel in fp32 to the positions the scheme's
+ *         stored keys are measured from (never rounded back to 16 bits), not
+ *         modified
  *   out   device [A][Q][Hq][d] bf16: softmax(q k^T * scale) v over the window
  *   lse   device [A][Q][Hq] fp32: natural log of sum exp(scaled scores); may
  *         be NULL
@@ -208,6 +218,19 @@ RKV_API int rkv_rebase(rkv_handle* h, int32_t layer, void* stream);
 RKV_API int rkv_decode_attn(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv_bf16* out,
                             float* lse, void* stream);
 
+/* rkv_append_rope and rkv_decode_attn of one layer in one launch: the
+ * attention kernel writes the step's new keys (rotated as rkv_append_rope
+ * rotates them) and values into the pool itself, just before it streams
+ * the ring stage that holds them, and attends over them in the same pass.
+ * Arguments as the two calls take them (q [A][Q][Hq][d], k and v
+ * [A][Q][Hkv][d], out, lse); results as rkv_append_rope followed by
+ * rkv_decode_attn.  In the exact schemes rkv_rebase of the layer must come
+ * first.  Counts as the layer's append (RKV_ERR_STATE if the layer's tokens
+ * were appended already).  q, k and v may be written by the kernel launched
+ * just before. */
+RKV_API int rkv_append_decode_attn(rkv_handle* h, int32_t layer, const rkv_bf16* q, const rkv_bf16* k,
+                                   const rkv_bf16* v, rkv_bf16* out, float* lse, void* stream);
+
 /* rkv_decode_attn for layers layer0 .. layer0 + n_layers - 1 of the open
  * step in one launch (the layers' queries must all be known, as in
  * rkv_step).  q and out are [n_layers][A][Q][Hq][d], lse [n_layers][A][Q][Hq]
@@ -217,9 +240,9 @@ RKV_API int rkv_decode_attn_layers(rkv_handle* h, int32_t layer0, int32_t n_laye
                                    rkv_bf16* out, float* lse, void* stream);
 
 /* The whole step for all layers: rkv_begin_step, then rkv_rebase (exact
- * scheme), rkv_append_rope and rkv_decode_attn for every layer, each as one
- * launch over all layers (the layers' inputs are all given, so their work is
- * independent).  Same results as the per-layer calls.
+ * re-base scheme), rkv_append_rope and rkv_decode_attn for every layer, each
+ * as one launch over all layers (the layers' inputs are all given, so their
+ * work is independent).  Same results as the per-layer calls.
  *   q     device [L][A][Q][Hq][d], k, v [L][A][Q][Hkv][d], all pre-RoPE bf16
  *   out   device [L][A][Q][Hq][d], lse [L][A][Q][Hq] (may be NULL) */
 RKV_API int rkv_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active, const rkv_bf16* q,
@@ -265,6 +288,18 @@ RKV_API int rkv_decode_attn_static(rkv_handle* h, int32_t layer, const rkv_bf16*
  * new history has written it. */
 RKV_API int rkv_reset_stream(rkv_handle* h, int32_t stream_id, int64_t start_offset, void* stream);
 
+/* rkv_reset_stream for a list of stream slots held in device memory, one
+ * launch for all of them: a serving loop whose streams leave and join
+ * between steps writes the list (and the new start offsets) on the device,
+ * so a captured graph of the step takes a new list on every replay.
+ *   ids_dev  device [n] int32: stream ids, distinct; a negative id is skipped
+ *   p0_dev   device [n] int64: their new start offsets
+ * An entry with an id >= n_streams or a start offset outside [0, 2^52) is
+ * skipped and reported as RKV_ERR_DEVICE_BOUNDS by rkv_sync_status.  Takes
+ * effect for the next rkv_begin_step, as rkv_reset_stream does. */
+RKV_API int rkv_reset_streams(rkv_handle* h, const int32_t* ids_dev, const int64_t* p0_dev, int32_t n,
+                              void* stream);
+
 /* Snapshot of one stream for resume: its ring state and the contents of its
  * pages in every layer (no page describes this; it is how a 24/7 serving
  * loop moves or checkpoints a live stream).  rkv_stream_snapshot_bytes gives
@@ -299,6 +334,19 @@ RKV_API int rkv_get_stream_state(rkv_handle* h, int32_t stream_id, int64_t* out,
 /* Wait for `stream`, read and clear the device status word: RKV_OK,
  * RKV_ERR_DEVICE_BOUNDS, RKV_ERR_DEVICE_RANGE or RKV_ERR_TIMEOUT. */
 RKV_API int rkv_sync_status(rkv_handle* h, void* stream);
+
+/* Failure-detection test hook (no page describes it).  The attention
+ * kernel's waits on its shared-memory stages are bounded: a wait gives up
+ * after one second, records RKV_ERR_TIMEOUT in the status word, drains the
+ * CTA's own copies in flight and returns, and later launches of the handle
+ * skip their copies until rkv_sync_status has read the status.  This hook
+ * lets a test drive that path without any fault: wait_ns shortens the limit
+ * (1 us .. 1 s; 0 restores one second), and withhold_stage >= 0 makes each
+ * attention CTA's producer skip the copy of its stage with that number
+ * (counted from 0 along the CTA's walk), so the consumers' wait for it runs
+ * out; -1 turns that off.  Affects launches enqueued after the call.  Host
+ * only. */
+RKV_API int rkv_set_wait_test(rkv_handle* h, int32_t withhold_stage, uint64_t wait_ns);
 
 /* Message of the last failure on this handle (NULL: of the calling thread's
  * last failure without a handle).  Valid until the next call. */

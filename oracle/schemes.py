@@ -1,4 +1,4 @@
-"""fp64 mirrors of the two storage schemes (invariance checks only).
+"""fp64 mirrors of the storage schemes (invariance checks only).
 
 Offset-only (voxtral.c rolling-KV article, §二): RoPE is applied once, when a
 key is written, at its logical position P0 + j; keys are never re-encoded.
@@ -9,7 +9,10 @@ number of positions evicted since the last re-base, so the stored positions
 restart inside the window; the new query and key use window-relative
 positions too.
 
-Both are evaluated in fp64 against a stored-key cache and must equal
+The exact re-base applied on read (RingSlotKeyCache below) stores each key
+once at its ring slot and rotates the query instead.
+
+All are evaluated in fp64 against a stored-key cache and must equal
 ``oracle.attention.attention_step`` (absolute positions) up to rounding,
 because RoPE scores depend only on position differences.
 """
@@ -64,4 +67,57 @@ class StoredKeyCache:
         return o, lse
 
 
-__all__ = ["StoredKeyCache", "SCHEME_OFFSET_ONLY", "SCHEME_EXACT_REBASE"]
+class RingSlotKeyCache:
+    """One stream, one layer: keys stored rotated by their ring slot, the exact re-base on read.
+
+    The stored key of token j is R(j mod C) k_j, written once; nothing is
+    re-rotated when the window rolls.  Window positions then stay below C
+    however long the stream runs, like the exact re-base's window-relative
+    positions (explainer, "Rolling KV Cache 三步拆解", 第 2 步), and the
+    re-base moves to the query: with E = floor(evicted / C), the retained
+    tokens j in [evicted, n) have floor(j / C) = E in ring slots >= evicted
+    mod C and E + 1 below, so query token t is rotated to t - C*E against the
+    first group and to t - C*(E + 1) against the second.  Each score is then
+    <R(t - j) q, k_j>, the definition's.
+    """
+
+    def __init__(self, ring: StreamRing, n_kv_heads: int, head_dim: int, theta: float):
+        self.ring = ring
+        self.theta = theta
+        self.k = np.zeros((ring.C, n_kv_heads, head_dim))
+        self.v = np.zeros((ring.C, n_kv_heads, head_dim))
+
+    def step(self, q_new, k_new, v_new, scale: float):
+        """Advance the ring by Q tokens and return (o [Q][Hq][d], lse [Q][Hq])."""
+        r = self.ring
+        n_old = r.n
+        r.step()
+        C = r.C
+        toks = list(range(n_old, r.n))
+        k_rot = rotate(np.asarray(k_new, dtype=np.float64), [r.slot(j) for j in toks], self.theta)
+        for i, j in enumerate(toks):
+            self.k[r.slot(j)] = k_rot[i]
+            self.v[r.slot(j)] = np.asarray(v_new[i], dtype=np.float64)
+        lap = r.evicted // C
+        first_slot = r.evicted % C
+        q_new = np.asarray(q_new, dtype=np.float64)
+        n_q, hq, d = q_new.shape
+        group = hq // self.k.shape[1]
+        o = np.zeros((n_q, hq, d))
+        lse = np.zeros((n_q, hq))
+        for i, t in enumerate(toks):
+            q_cur = rotate(q_new[i][None], [t - C * lap], self.theta)[0]         # slots >= first_slot
+            q_next = rotate(q_new[i][None], [t - C * (lap + 1)], self.theta)[0]  # slots < first_slot
+            keys = [j for j in r.retained() if j <= t]
+            slots = [r.slot(j) for j in keys]
+            for h in range(hq):
+                s = np.array([self.k[sl, h // group, :] @ (q_cur[h] if sl >= first_slot else q_next[h])
+                              for sl in slots]) * scale
+                m = s.max()
+                e = np.exp(s - m)
+                o[i, h] = e @ self.v[slots, h // group, :] / e.sum()
+                lse[i, h] = m + math.log(e.sum())
+        return o, lse
+
+
+__all__ = ["StoredKeyCache", "RingSlotKeyCache", "SCHEME_OFFSET_ONLY", "SCHEME_EXACT_REBASE"]

@@ -12,10 +12,10 @@ from . import _abi
 from ._abi import (  # noqa: F401
     RKV_ERR_CAPACITY, RKV_ERR_CONFIG, RKV_ERR_CUDA, RKV_ERR_DEVICE_BOUNDS, RKV_ERR_DEVICE_RANGE, RKV_ERR_INVALID_ARG,
     RKV_ERR_STATE, RKV_ERR_TIMEOUT, RKV_OK, RKV_SCHEME_EXACT_ON_READ, RKV_SCHEME_EXACT_REBASE, RKV_SCHEME_OFFSET_ONLY,
-    STATE_FIELDS, RkvError, make_config, rkv_append_rope, rkv_begin_step, rkv_check_stream_state, rkv_clock_resolve,
+    STATE_FIELDS, RkvError, make_config, rkv_append_decode_attn, rkv_append_rope, rkv_begin_step, rkv_check_stream_state, rkv_clock_resolve,
     rkv_create, rkv_decode_attn, rkv_decode_attn_layers, rkv_decode_attn_static, rkv_destroy, rkv_gen_next_inputs, rkv_gen_step_inputs, rkv_gen_tokens,
-    rkv_get_stream_state, rkv_last_error, rkv_load_stream, rkv_rebase, rkv_required_bytes, rkv_reset_stream,
-    rkv_rope_cossin, rkv_save_stream, rkv_stream_snapshot_bytes,
+    rkv_get_stream_state, rkv_last_error, rkv_load_stream, rkv_rebase, rkv_required_bytes, rkv_reset_stream, rkv_reset_streams,
+    rkv_rope_cossin, rkv_save_stream, rkv_set_wait_test, rkv_stream_snapshot_bytes,
     rkv_step, rkv_sync_status,
 )
 
@@ -51,6 +51,9 @@ class RollingKV:
     def decode_attn(self, layer, q, out, lse=None, stream=None):
         rkv_decode_attn(self.handle, layer, q, out, lse, stream)
 
+    def append_decode_attn(self, layer, q, k, v, out, lse=None, stream=None):
+        rkv_append_decode_attn(self.handle, layer, q, k, v, out, lse, stream)
+
     def decode_attn_layers(self, layer0, n_layers, q, out, lse=None, stream=None):
         rkv_decode_attn_layers(self.handle, layer0, n_layers, q, out, lse, stream)
 
@@ -65,6 +68,9 @@ class RollingKV:
 
     def reset_stream(self, stream_id, start_offset=0, stream=None):
         rkv_reset_stream(self.handle, stream_id, start_offset, stream)
+
+    def reset_streams(self, ids_dev, p0_dev, stream=None):
+        rkv_reset_streams(self.handle, ids_dev, p0_dev, ids_dev.numel(), stream)
 
     def save_stream(self, stream_id, stream=None):
         """The stream's snapshot as a uint8 tensor on the handle's device."""

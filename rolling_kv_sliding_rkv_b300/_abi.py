@@ -40,7 +40,7 @@ class rkv_config(C.Structure):
     _fields_ = [("n_layers", C.c_int32), ("n_streams", C.c_int32), ("n_q_heads", C.c_int32),
                 ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("q_per_step", C.c_int32),
                 ("page_size", C.c_int32), ("scheme", C.c_int32), ("rebase_interval", C.c_int32),
-                ("reserved", C.c_int32), ("rope_theta", C.c_double), ("softmax_scale", C.c_double)]
+                ("window_slack", C.c_int32), ("rope_theta", C.c_double), ("softmax_scale", C.c_double)]
 
 
 class rkv_clock(C.Structure):
@@ -65,15 +65,18 @@ _SIGS = {
     "rkv_rebase": [_vp, _i32, _vp],
     "rkv_decode_attn": [_vp, _i32, _vp, _vp, _vp, _vp],
     "rkv_decode_attn_static": [_vp, _i32, _vp, _vp, _vp, _vp],
+    "rkv_append_decode_attn": [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp],
     "rkv_decode_attn_layers": [_vp, _i32, _i32, _vp, _vp, _vp, _vp],
     "rkv_step": [_vp, C.POINTER(_i32), _i32, _vp, _vp, _vp, _vp, _vp, _vp],
     "rkv_get_stream_state": [_vp, _i32, C.POINTER(_i64), _vp],
     "rkv_check_stream_state": [C.POINTER(rkv_config), C.POINTER(_i64)],
     "rkv_reset_stream": [_vp, _i32, _i64, _vp],
+    "rkv_reset_streams": [_vp, _vp, _vp, _i32, _vp],
     "rkv_stream_snapshot_bytes": [_vp, _i32, C.POINTER(_sz)],
     "rkv_save_stream": [_vp, _i32, _vp, _sz, _vp],
     "rkv_load_stream": [_vp, _i32, _vp, _sz, _vp],
     "rkv_sync_status": [_vp, _vp],
+    "rkv_set_wait_test": [_vp, _i32, _u64],
     "rkv_destroy": [_vp],
     "rkv_rope_cossin": [_vp, _i32, _i32, _f64, _vp, _vp],
     "rkv_gen_tokens": [_u64, _u32, _i32, _i32, _i64, _i32, _i32, _f32, _vp, _vp],
@@ -180,6 +183,10 @@ def rkv_decode_attn(h: int, layer: int, q, out, lse=None, stream=None) -> None:
     _check(_lib.rkv_decode_attn(h, layer, _ptr(q), _ptr(out), _ptr(lse), _stream(stream)), h)
 
 
+def rkv_append_decode_attn(h: int, layer: int, q, k, v, out, lse=None, stream=None) -> None:
+    _check(_lib.rkv_append_decode_attn(h, layer, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _stream(stream)), h)
+
+
 def rkv_decode_attn_static(h: int, layer: int, q, out, lse=None, stream=None) -> None:
     _check(_lib.rkv_decode_attn_static(h, layer, _ptr(q), _ptr(out), _ptr(lse), _stream(stream)), h)
 
@@ -195,6 +202,10 @@ def rkv_step(h: int, active_ids, q, k, v, out, lse=None, stream=None) -> None:
 
 def rkv_reset_stream(h: int, stream_id: int, start_offset: int, stream=None) -> None:
     _check(_lib.rkv_reset_stream(h, stream_id, start_offset, _stream(stream)), h)
+
+
+def rkv_reset_streams(h: int, ids_dev, p0_dev, n: int, stream=None) -> None:
+    _check(_lib.rkv_reset_streams(h, _ptr(ids_dev), _ptr(p0_dev), n, _stream(stream)), h)
 
 
 def rkv_stream_snapshot_bytes(h: int, stream_id: int) -> int:
@@ -226,6 +237,10 @@ def rkv_check_stream_state(cfg: rkv_config, state) -> None:
 
 def rkv_sync_status(h: int, stream=None) -> None:
     _check(_lib.rkv_sync_status(h, _stream(stream)), h)
+
+
+def rkv_set_wait_test(h: int, withhold_stage: int, wait_ns: int) -> None:
+    _check(_lib.rkv_set_wait_test(h, withhold_stage, wait_ns), h)
 
 
 def rkv_destroy(h: int) -> None:

@@ -27,6 +27,7 @@ struct rkv_handle {
   int device = 0;
   int num_sms = 0;
   bool step_open = false;
+  bool launched_since_begin = false;  // a kernel of this library followed the begin-step kernel
   int32_t n_active = 0;
   std::vector<uint8_t> appended, rebased;
   std::vector<int32_t> first_page, n_pages_of;  // per stream: its contiguous run of pages
@@ -55,7 +56,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Layout {
-  size_t state, page_table, desc, cs_new, omega, rope_table, status, total;
+  size_t state, page_table, desc, cs_new, cs_q, cs_lap, omega, rope_table, status, total;
   size_t pool_region_elems;  // elements of one pool region (all layers)
   int32_t max_pages, n_pages, t_rows, w_max, regions;
 };
@@ -76,7 +77,7 @@ bool validate_config(const rkv_config* c, std::string* why) {
     return bad("page_size must be 16, 32, 64 or 128");
   if (c->scheme != RKV_SCHEME_OFFSET_ONLY && !rkv::exact_scheme(c->scheme)) return bad("unknown scheme");
   if (c->rebase_interval < 1) return bad("rebase_interval must be >= 1");
-  if (c->reserved != 0) return bad("reserved must be 0");
+  if (c->window_slack < 0 || c->window_slack > RKV_MAX_WINDOW) return bad("window_slack must be in [0, RKV_MAX_WINDOW]");
   if (!(c->rope_theta > 1.0) || !std::isfinite(c->rope_theta)) return bad("rope_theta must be finite and > 1");
   if (!(c->softmax_scale >= 0.0) || !std::isfinite(c->softmax_scale)) return bad("softmax_scale must be finite and >= 0");
   (void)buf;
@@ -94,14 +95,15 @@ bool compute_layout(const rkv_config* c, const int32_t* window, Layout* L, std::
   int64_t n_pages = 0;
   for (int s = 0; s < S; ++s) {
     const int32_t w = window[s];
-    if (w < c->q_per_step || w > RKV_MAX_WINDOW) {
+    if (w < c->q_per_step || w > RKV_MAX_WINDOW - c->window_slack) {
       char buf[160];
-      snprintf(buf, sizeof buf, "window[%d] = %d outside [q_per_step, RKV_MAX_WINDOW]", s, w);
+      snprintf(buf, sizeof buf, "window[%d] = %d outside [q_per_step, RKV_MAX_WINDOW - window_slack]", s, w);
       *why = buf;
       return false;
     }
-    w_max = w > w_max ? w : w_max;
-    n_pages += (w + c->page_size - 1) / c->page_size;
+    const int32_t ring = w + c->window_slack;  // the stream's ring capacity
+    w_max = ring > w_max ? ring : w_max;
+    n_pages += (ring + c->page_size - 1) / c->page_size;
   }
   if (n_pages > (1 << 30)) {
     *why = "too many pages";
@@ -110,15 +112,16 @@ bool compute_layout(const rkv_config* c, const int32_t* window, Layout* L, std::
   L->w_max = w_max;
   L->max_pages = (w_max + c->page_size - 1) / c->page_size;
   L->n_pages = static_cast<int32_t>(n_pages);
-  const bool exact = rkv::exact_scheme(c->scheme);
-  // window-relative positions of the exact scheme stay below W + interval - 1
-  const int64_t t_rows = exact ? static_cast<int64_t>(w_max) + c->rebase_interval - 1 : 0;
+  const bool on_read = c->scheme == RKV_SCHEME_EXACT_ON_READ;
+  // window-relative positions of the materialised exact re-base stay below C + interval - 1
+  const int64_t t_rows =
+      c->scheme == RKV_SCHEME_EXACT_REBASE ? static_cast<int64_t>(w_max) + c->rebase_interval - 1 : 0;
   if (t_rows > (1 << 24)) {
     *why = "window + rebase_interval too large";
     return false;
   }
   L->t_rows = static_cast<int32_t>(t_rows);
-  // rotated keys, values, pre-RoPE keys (exact re-base); rotate-on-read keeps no rotated copy
+  // rotated keys, values, and pre-RoPE keys for the materialised exact re-base
   L->regions = c->scheme == RKV_SCHEME_EXACT_REBASE ? 3 : 2;
   const int half = c->head_dim / 2;
   size_t off = 0;
@@ -131,6 +134,8 @@ bool compute_layout(const rkv_config* c, const int32_t* window, Layout* L, std::
   L->page_table = take(static_cast<size_t>(S) * L->max_pages * sizeof(int32_t));
   L->desc = take(static_cast<size_t>(S) * sizeof(rkv::StepDesc));
   L->cs_new = take(static_cast<size_t>(S) * c->q_per_step * half * 2 * sizeof(float));
+  L->cs_q = on_read ? take(static_cast<size_t>(S) * c->q_per_step * half * 2 * sizeof(float)) : L->cs_new;
+  L->cs_lap = on_read ? take(static_cast<size_t>(S) * half * 2 * sizeof(float)) : 0;
   L->omega = take(static_cast<size_t>(half) * sizeof(double));
   L->rope_table = take(static_cast<size_t>(t_rows) * half * 2 * sizeof(float));
   L->status = take(4 * sizeof(int32_t));
@@ -139,7 +144,24 @@ bool compute_layout(const rkv_config* c, const int32_t* window, Layout* L, std::
   return true;
 }
 
+bool step_in_progress(const rkv_handle* h) {
+  if (!h->step_open) return false;
+  const bool exact = rkv::exact_scheme(h->cfg.scheme);
+  for (int l = 0; l < h->cfg.n_layers; ++l)
+    if (!h->appended[l] || (exact && !h->rebased[l])) return true;
+  return false;
+}
+
 bool check_layer(rkv_handle* h, int32_t layer) { return layer >= 0 && layer < h->cfg.n_layers; }
+
+// What the next decode-attention launch may read before its dependency wait: the begin-step
+// kernel's outputs once another kernel of this library followed it (it is then two or more
+// launches back), and the caller's queries only when they were written before the call
+// (rkv_step) and the descriptors may be read as well.
+int early_bits(const rkv_handle* h, bool q_before_call) {
+  if (!h->launched_since_begin) return 0;
+  return rkv::kEarlyDesc | (q_before_call ? rkv::kEarlyQ : 0);
+}
 
 }  // namespace
 
@@ -217,21 +239,17 @@ int rkv_create(const rkv_config* cfg, const int32_t* window, const int64_t* star
   v.page_table = reinterpret_cast<int32_t*>(sb + L.page_table);
   v.desc = reinterpret_cast<rkv::StepDesc*>(sb + L.desc);
   v.cs_new = reinterpret_cast<float*>(sb + L.cs_new);
+  v.cs_q = reinterpret_cast<float*>(sb + L.cs_q);
+  v.cs_lap = cfg->scheme == RKV_SCHEME_EXACT_ON_READ ? reinterpret_cast<float*>(sb + L.cs_lap) : nullptr;
   v.omega = reinterpret_cast<double*>(sb + L.omega);
   v.rope_table = L.t_rows ? reinterpret_cast<float*>(sb + L.rope_table) : nullptr;
   v.part_ml = nullptr;  // split-K partials: only the scratch form of decode attention has them
   v.part_o = nullptr;
   v.status = reinterpret_cast<int32_t*>(sb + L.status);
   uint16_t* pool = static_cast<uint16_t*>(pool_dev);
-  if (cfg->scheme == RKV_SCHEME_EXACT_ON_READ) {
-    v.k_rot = nullptr;
-    v.k_raw = pool;
-    v.v = pool + L.pool_region_elems;
-  } else {
-    v.k_rot = pool;
-    v.v = pool + L.pool_region_elems;
-    v.k_raw = L.regions == 3 ? pool + 2 * L.pool_region_elems : nullptr;
-  }
+  v.k_rot = pool;
+  v.v = pool + L.pool_region_elems;
+  v.k_raw = L.regions == 3 ? pool + 2 * L.pool_region_elems : nullptr;
   v.layer_stride = static_cast<int64_t>(L.n_pages) * cfg->n_kv_heads * cfg->page_size * cfg->head_dim;
   v.n_streams = cfg->n_streams;
   v.n_layers = cfg->n_layers;
@@ -245,9 +263,12 @@ int rkv_create(const rkv_config* cfg, const int32_t* window, const int64_t* star
   v.t_rows = L.t_rows;
   v.scheme = cfg->scheme;
   v.rebase_interval = cfg->rebase_interval;
+  v.window_slack = cfg->window_slack;
   const double scale = cfg->softmax_scale > 0.0 ? cfg->softmax_scale : 1.0 / std::sqrt(static_cast<double>(cfg->head_dim));
   v.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
   v.num_sms = h->num_sms;
+  v.wait_ns = rkv::kDefaultWaitNs;
+  v.withhold_stage = -1;
 
   // host images of the stream state, page tables and RoPE frequencies
   const int S = cfg->n_streams, half = cfg->head_dim / 2;
@@ -259,7 +280,7 @@ int rkv_create(const rkv_config* cfg, const int32_t* window, const int64_t* star
     st[rkv::F_KV_POS_OFFSET] = start_offset[s];
     st[rkv::F_W] = window[s];
     st[rkv::F_P0] = start_offset[s];
-    const int pages = (window[s] + cfg->page_size - 1) / cfg->page_size;
+    const int pages = (window[s] + cfg->window_slack + cfg->page_size - 1) / cfg->page_size;
     h->first_page.push_back(next_page);
     h->n_pages_of.push_back(pages);
     for (int p = 0; p < pages; ++p) table[static_cast<size_t>(s) * L.max_pages + p] = next_page++;
@@ -316,6 +337,7 @@ int rkv_begin_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active, v
   cudaError_t e = rkv::launch_begin_step(h->view, ids, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(h, e, "begin_step launch");
   h->step_open = true;
+  h->launched_since_begin = false;
   h->n_active = n_active;
   std::fill(h->appended.begin(), h->appended.end(), 0);
   std::fill(h->rebased.begin(), h->rebased.end(), 0);
@@ -333,6 +355,7 @@ int rkv_append_rope(rkv_handle* h, int32_t layer, const rkv_bf16* k, const rkv_b
   cudaError_t e = rkv::launch_append_rope(h->view, h->n_active, layer, 1, k, v, 0, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(h, e, "append_rope launch");
   h->appended[layer] = 1;
+  h->launched_since_begin = true;
   return RKV_OK;
 }
 
@@ -346,6 +369,7 @@ int rkv_rebase(rkv_handle* h, int32_t layer, void* stream) {
   cudaError_t e = rkv::launch_rebase(h->view, h->n_active, layer, 1, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(h, e, "rebase launch");
   h->rebased[layer] = 1;
+  if (h->cfg.scheme == RKV_SCHEME_EXACT_REBASE) h->launched_since_begin = true;
   return RKV_OK;
 }
 
@@ -359,9 +383,36 @@ int rkv_decode_attn(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv_bf16* o
   if (!h->appended[layer]) return fail(h, RKV_ERR_STATE, "rkv_decode_attn before rkv_append_rope for this layer");
   if (rkv::exact_scheme(h->cfg.scheme) && !h->rebased[layer])
     return fail(h, RKV_ERR_STATE, "rkv_decode_attn before rkv_rebase for this layer");
-  cudaError_t e = rkv::launch_decode_attn(h->view, h->n_active, layer, 1, q, out, lse, 0, 0, false,
+  rkv::AttnExtras x;
+  x.early = early_bits(h, false);
+  cudaError_t e = rkv::launch_decode_attn(h->view, h->n_active, layer, 1, q, out, lse, 0, 0, x,
                                           static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(h, e, "decode_attn launch");
+  h->launched_since_begin = true;
+  return RKV_OK;
+}
+
+int rkv_append_decode_attn(rkv_handle* h, int32_t layer, const rkv_bf16* q, const rkv_bf16* k, const rkv_bf16* v,
+                           rkv_bf16* out, float* lse, void* stream) {
+  NvtxRange nvtx_range("rkv:append_decode_attn");
+  if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
+  if (!h->step_open) return fail(h, RKV_ERR_STATE, "no open step (call rkv_begin_step)");
+  if (!check_layer(h, layer)) return fail(h, RKV_ERR_INVALID_ARG, "layer out of range");
+  if (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return fail(h, RKV_ERR_INVALID_ARG, "q, k, v and out must be non-NULL and 16-byte aligned");
+  if (h->appended[layer]) return fail(h, RKV_ERR_STATE, "this layer's tokens were already appended in this step");
+  if (rkv::exact_scheme(h->cfg.scheme) && !h->rebased[layer])
+    return fail(h, RKV_ERR_STATE, "rkv_append_decode_attn before rkv_rebase for this layer");
+  rkv::AttnExtras x;
+  x.early = early_bits(h, false);
+  x.k_new = k;
+  x.v_new = v;
+  cudaError_t e = rkv::launch_decode_attn(h->view, h->n_active, layer, 1, q, out, lse, 0, 0, x,
+                                          static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "append_decode_attn launch");
+  h->appended[layer] = 1;
+  h->launched_since_begin = true;
   return RKV_OK;
 }
 
@@ -380,10 +431,13 @@ int rkv_decode_attn_layers(rkv_handle* h, int32_t layer0, int32_t n_layers, cons
       return fail(h, RKV_ERR_STATE, "rkv_decode_attn_layers before rkv_append_rope (or rkv_rebase) of a layer");
   const rkv_config& c = h->cfg;
   const int64_t rows = static_cast<int64_t>(h->n_active) * c.q_per_step;
+  rkv::AttnExtras x;
+  x.early = early_bits(h, false);
   cudaError_t e = rkv::launch_decode_attn(h->view, h->n_active, layer0, n_layers, q, out, lse,
-                                          rows * c.n_q_heads * c.head_dim, rows * c.n_q_heads, false,
+                                          rows * c.n_q_heads * c.head_dim, rows * c.n_q_heads, x,
                                           static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(h, e, "decode_attn launch");
+  h->launched_since_begin = true;
   return RKV_OK;
 }
 
@@ -402,15 +456,23 @@ int rkv_step(rkv_handle* h, const int32_t* active_ids, int32_t n_active, const r
   const int64_t lse_stride = rows * c.n_q_heads;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
-  if (rkv::exact_scheme(c.scheme)) e = rkv::launch_rebase(h->view, n_active, 0, c.n_layers, st);
-  if (e != cudaSuccess) return cuda_fail(h, e, "rebase launch");
+  if (c.scheme == RKV_SCHEME_EXACT_REBASE) {
+    e = rkv::launch_rebase(h->view, n_active, 0, c.n_layers, st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "rebase launch");
+    h->launched_since_begin = true;
+  }
   std::fill(h->rebased.begin(), h->rebased.end(), 1);
   e = rkv::launch_append_rope(h->view, n_active, 0, c.n_layers, k, v, kv_stride, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "append_rope launch");
-  std::fill(h->appended.begin(), h->appended.end(), 1);
-  // q was written before this call, three launches back: the kernel may read it before its wait
-  e = rkv::launch_decode_attn(h->view, n_active, 0, c.n_layers, q, out, lse, q_stride, lse_stride, true, st);
+  h->launched_since_begin = true;
+  // q was written before this call, two or more launches back, so the attention kernel may read
+  // it before its dependency wait
+  rkv::AttnExtras x;
+  x.early = early_bits(h, true);
+  e = rkv::launch_decode_attn(h->view, n_active, 0, c.n_layers, q, out, lse, q_stride, lse_stride, x, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "decode_attn launch");
+  std::fill(h->appended.begin(), h->appended.end(), 1);
+  h->launched_since_begin = true;
   return RKV_OK;
 }
 
@@ -424,6 +486,15 @@ int rkv_reset_stream(rkv_handle* h, int32_t stream_id, int64_t start_offset, voi
   return e == cudaSuccess ? RKV_OK : cuda_fail(h, e, "reset_stream launch");
 }
 
+int rkv_reset_streams(rkv_handle* h, const int32_t* ids_dev, const int64_t* p0_dev, int32_t n, void* stream) {
+  NvtxRange nvtx_range("rkv:reset_streams");
+  if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
+  if (n < 0 || n > RKV_MAX_STREAMS || (n > 0 && (!ids_dev || !p0_dev)))
+    return fail(h, RKV_ERR_INVALID_ARG, "n must be in [0, RKV_MAX_STREAMS] with non-NULL lists");
+  cudaError_t e = rkv::launch_reset_streams(h->view, ids_dev, p0_dev, n, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RKV_OK : cuda_fail(h, e, "reset_streams launch");
+}
+
 namespace {
 
 constexpr int64_t kSnapMagic = 0x31504e5356524bLL;  // "KRVSNP1" little-endian tag
@@ -434,7 +505,7 @@ void snap_header(const rkv_handle* h, int32_t s, int64_t* hdr) {
   const rkv_config& c = h->cfg;
   const int64_t fields[kSnapHeader] = {kSnapMagic, 1, c.n_layers, c.n_kv_heads, c.head_dim, c.page_size,
                                        c.scheme, c.q_per_step, c.rebase_interval,
-                                       static_cast<int64_t>(h->n_pages_of[s]), h->regions, 0, 0, 0, 0, 0};
+                                       static_cast<int64_t>(h->n_pages_of[s]), h->regions, c.window_slack, 0, 0, 0, 0};
   std::memcpy(hdr, fields, sizeof fields);
 }
 
@@ -449,13 +520,6 @@ size_t snap_bytes(const rkv_handle* h, int32_t s) {
          static_cast<size_t>(h->regions) * h->cfg.n_layers * snap_run_elems(h, s) * sizeof(uint16_t);
 }
 
-bool step_in_progress(const rkv_handle* h) {
-  if (!h->step_open) return false;
-  const bool exact = rkv::exact_scheme(h->cfg.scheme);
-  for (int l = 0; l < h->cfg.n_layers; ++l)
-    if (!h->appended[l] || (exact && !h->rebased[l])) return true;
-  return false;
-}
 
 // pointer to (region r, layer l) of stream s's pages
 uint16_t* snap_run(const rkv_handle* h, int32_t s, int r, int l) {
@@ -543,10 +607,16 @@ int rkv_check_stream_state(const rkv_config* cfg, const int64_t* st) {
   if (w < cfg->q_per_step || w > RKV_MAX_WINDOW) return bad("window outside [q_per_step, RKV_MAX_WINDOW]");
   if (p0 < 0 || p0 >= kMaxPos) return bad("P0 outside [0, 2^52)");
   if (n < 0 || n % cfg->q_per_step != 0 || n >= kMaxPos - p0) return bad("token count n negative, not a multiple of q_per_step, or past 2^52");
-  if (len != (n < w ? n : w)) return bad("len differs from min(n, W)");
+  // len as the steps leave it: n until the first step past the ring capacity C = W + slack
+  // (which takes n to n1, the first multiple of Q above C, and len to W), then W + k Q with k
+  // counting the steps since the last batch, k <= K = floor((C - W) / Q)
+  const int64_t q = cfg->q_per_step, ring = w + cfg->window_slack;
+  const int64_t n1 = (ring / q + 1) * q;
+  const int64_t want_len = n < n1 ? n : w + ((n - n1) / q % ((ring - w) / q + 1)) * q;
+  if (len != want_len) return bad("len differs from the eviction rule (min(n, W) without window slack)");
   if (ev != n - len) return bad("evicted differs from n - len");
   if (off != p0 + ev) return bad("kv_pos_offset differs from P0 + evicted");
-  if (head != ev % w) return bad("head_slot differs from evicted mod W");
+  if (head != ev % ring) return bad("head_slot differs from evicted mod (W + window_slack)");
   if (rkv::exact_scheme(cfg->scheme)) {
     if (rb < 0 || rb > ev || ev - rb >= cfg->rebase_interval)
       return bad("rope_base outside (evicted - rebase_interval, evicted]");
@@ -622,6 +692,16 @@ int rkv_gen_step_inputs(rkv_handle* h, uint64_t seed, int32_t layer, float scale
   cudaError_t e = rkv::launch_gen_step_inputs(h->view, h->n_active, seed, layer, scale, q, k, v,
                                               static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? RKV_OK : cuda_fail(h, e, "gen_step_inputs launch");
+}
+
+int rkv_set_wait_test(rkv_handle* h, int32_t withhold_stage, uint64_t wait_ns) {
+  if (!h) return fail(nullptr, RKV_ERR_INVALID_ARG, "handle is NULL");
+  if (withhold_stage < -1) return fail(h, RKV_ERR_INVALID_ARG, "withhold_stage must be -1 or a stage number");
+  if (wait_ns != 0 && (wait_ns < 1000 || wait_ns > rkv::kDefaultWaitNs))
+    return fail(h, RKV_ERR_INVALID_ARG, "wait_ns must be 0 (default) or in [1 us, 1 s]");
+  h->view.wait_ns = wait_ns ? wait_ns : rkv::kDefaultWaitNs;
+  h->view.withhold_stage = withhold_stage;
+  return RKV_OK;
 }
 
 int rkv_gen_next_inputs(rkv_handle* h, uint64_t seed, const int32_t* active_ids, int32_t n_active, float scale,

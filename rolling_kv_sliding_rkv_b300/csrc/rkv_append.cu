@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(128) append_rope_kernel(DevView v, int layer0,
   const int a = row / v.q_per_step, t = row % v.q_per_step;
   const StepDesc dsc = v.desc[a];
   const int64_t tok = dsc.n_old + t;
-  const int slot = static_cast<int>(tok % dsc.window);
+  const int slot = static_cast<int>(tok % dsc.ring);
   const int ring_page = slot / v.page_size;
   if (ring_page >= v.max_pages) {
     record_error(v.status, DEV_BOUNDS, 1, ring_page);
@@ -91,21 +91,13 @@ __global__ void __launch_bounds__(128) append_rope_kernel(DevView v, int layer0,
   float xa[8], xb[8];
   unpack8(ka, xa);
   unpack8(kb, xb);
-  if (v.k_rot) {
-    const float* cs = v.cs_new + (static_cast<int64_t>(row) * half + cp * 8) * 2;
-    uint4 ya, yb;
-    bool fits;
-    rotate8(xa, xb, cs, &ya, &yb, &fits);
-    if (!fits) record_error(v.status, DEV_RANGE, 1, cp);
-    *reinterpret_cast<uint4*>(v.k_rot + dst + pa) = ya;
-    *reinterpret_cast<uint4*>(v.k_rot + dst + pb) = yb;
-  } else {
-    // rotate-on-read: the rotation happens in attention; |R x| <= sqrt(2) max(|a|, |b|) must fit fp16
-    bool ok = true;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) ok = ok && fmaxf(fabsf(xa[j]), fabsf(xb[j])) < 46000.0f;
-    if (!ok) record_error(v.status, DEV_RANGE, 2, cp);
-  }
+  const float* cs = v.cs_new + (static_cast<int64_t>(row) * half + cp * 8) * 2;
+  uint4 ya, yb;
+  bool fits;
+  rotate8(xa, xb, cs, &ya, &yb, &fits);
+  if (!fits) record_error(v.status, DEV_RANGE, 1, cp);
+  *reinterpret_cast<uint4*>(v.k_rot + dst + pa) = ya;
+  *reinterpret_cast<uint4*>(v.k_rot + dst + pb) = yb;
 }
 
 // A thread re-bases one chunk pair (elements 8c .. 8c+7 and their partners
@@ -140,7 +132,7 @@ __global__ void __launch_bounds__(kRebaseThreads, 4) rebase_kernel(DevView v, in
   const int cp = item % cpairs;
   const int kvh = (item / cpairs) % v.n_kv_heads;
   const int slot0 = (item / (cpairs * v.n_kv_heads)) * kRebaseRun;
-  const int W = dsc.window;
+  const int W = dsc.ring;  // the ring's modulus
   if (slot0 >= W) return;
   const int ev_mod = static_cast<int>(dsc.evicted % W);
   const int old_len = static_cast<int>(dsc.n_old - dsc.evicted);  // window index of the first new token
@@ -240,7 +232,7 @@ cudaError_t launch_append_rope(const DevView& v, int n_active, int layer0, int n
 }
 
 cudaError_t launch_rebase(const DevView& v, int n_active, int layer0, int n_layers, cudaStream_t st) {
-  if (v.k_rot == nullptr) return cudaSuccess;  // rotate-on-read: nothing is stored re-based
+  if (v.scheme != RKV_SCHEME_EXACT_REBASE) return cudaSuccess;  // on read: nothing is stored re-based
   const int64_t per_stream =
       static_cast<int64_t>(v.max_pages) * v.page_size / kRebaseRun * v.n_kv_heads * (v.head_dim / 16);
   dim3 grid(static_cast<unsigned>((per_stream + kRebaseThreads - 1) / kRebaseThreads), n_active, n_layers);

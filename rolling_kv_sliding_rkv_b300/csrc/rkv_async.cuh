@@ -1,13 +1,12 @@
 // mbarrier, bulk asynchronous copy (cp.async.bulk) and timer helpers shared by
-// the streaming kernels.  Every wait is bounded: it gives up after kWaitNs of
-// %globaltimer and the caller records RKV_ERR_TIMEOUT in the status word.
+// the streaming kernels.  Every wait is bounded: it gives up after a limit of
+// %globaltimer nanoseconds (one second unless the handle's failure-detection
+// test hook shortened it) and the caller records RKV_ERR_TIMEOUT in the status word.
 #pragma once
 
 #include <stdint.h>
 
 namespace rkv {
-
-constexpr unsigned long long kWaitNs = 1000000000ull;  // give up on a barrier after 1 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -43,14 +42,14 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
-// Wait for the phase with the given parity to complete; false after kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
   if (mbar_test(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (;;) {
     for (int i = 0; i < 32; ++i)
       if (mbar_test(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -24,11 +24,14 @@
 //   P^T = exp2(S^T - m) (rows' running max m), rounded to bf16 and turned
 //       into the B operand by an 8x8 transpose (movmatrix);
 //   O^T[d][8 rows] += V^T[d][16 keys] . P^T  (V read with ldmatrix.trans).
-// Stored keys are fp16 (offset-only and exact re-base schemes).  In the
-// rotate-on-read scheme the pool holds pre-RoPE bf16 keys and each consumer
-// warp turns its slots of a landed K stage, in shared memory, into the keys
-// rotated by R(j - rope_base) in fp32 (cos/sin from the window-relative
-// table), rounded once to fp16: the exact re-base with no stored copy.
+// Stored keys are fp16.  In the exact re-base applied on read, a key is
+// stored rotated by its ring slot index (j mod C, C the ring's capacity) and
+// never touched again; the query carries the rest of the rotation: for ring
+// slots at or above evicted mod C it is rotated to j_q - C * floor(evicted /
+// C), for the slots below (tokens of the ring's next lap) C less, so every
+// score sees the exact position difference of its tokens.  The second query
+// is R(-C) applied to the first, in the registers of the MMA fragments
+// (lap_shift).
 //
 // Splits of one (layer, stream, kv head) form a thread-block cluster and
 // combine their (m, l, O) through distributed shared memory; the scratch
@@ -64,10 +67,19 @@ struct AttnArgs {
   int layer0, n_layers, n_active;
   int splits, stages_per_split;
   int mode;            // 0: whole windows; 1: split, cluster merge; 2: split, partials to part_ml / part_o
-  int q_early;         // 1: q was written two or more launches back and may be read before the
-                       // dependency wait (rkv_step); 0: q is read after it, since the caller's
-                       // kernel that wrote q may be this launch's immediate predecessor
+  // What may be read before the dependency wait (programmatic dependent launch; see
+  // rkv_internal.cuh): bit 0 the step descriptors, angles and pages (the begin-step kernel ran two
+  // or more launches back), bit 1 the queries (written before the call, rkv_step).  A cleared bit
+  // means the data may come from this launch's immediate predecessor and is read after the wait.
+  int early;
+  // fused append (rkv_append_decode_attn, rkv_step): the step's new keys and values, pre-RoPE,
+  // [layer][A][Q][Hkv][d], written rotated into the pool by the producer before it copies their
+  // stage; NULL when rkv_append_rope did it
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  int64_t kv_layer_stride;
 };
+
 
 // 2^x with the hardware approximation (relative error about 2^-22; subnormal
 // results flush to zero, which softmax weights below 2^-126 can afford)
@@ -189,14 +201,16 @@ __device__ __forceinline__ Unit unit_of(int u, int n_active, int hkv) {
   return r;
 }
 
-// Ring slots holding tokens: all W once anything was evicted, else 0 .. len-1.
-__device__ __forceinline__ int slots_in_use(const StepDesc& d) { return d.evicted > 0 ? d.window : d.len; }
+// Ring slots written so far: all C once anything was evicted, else 0 .. len-1.  With a ring
+// capacity above the window (window_slack > 0) some of them hold evicted tokens: masked.
+__device__ __forceinline__ int slots_in_use(const StepDesc& d) { return d.evicted > 0 ? d.ring : d.len; }
 
 // Query prefetch of one consumer thread: pair cp of row r (chunks cp and cp + D/16).
 template <int D>
 struct QPrefetch {
   uint4 xa, xb;
   float4 cs[4];
+  float lap;  // on read: element tid of the unit's (cos, sin)(-C omega) row
 };
 
 template <int D>
@@ -211,7 +225,7 @@ __device__ __forceinline__ void q_prefetch(const AttnArgs& args, const Unit& un,
         args.q + un.lz * args.q_layer_stride + ((static_cast<int64_t>(un.a) * nq + t) * v.n_q_heads + h) * D;
     pf.xa = *reinterpret_cast<const uint4*>(x + cp * 8);
     pf.xb = *reinterpret_cast<const uint4*>(x + H + cp * 8);
-    const float4* cs = reinterpret_cast<const float4*>(v.cs_new + ((static_cast<int64_t>(un.a) * nq + t) * H + cp * 8) * 2);
+    const float4* cs = reinterpret_cast<const float4*>(v.cs_q + ((static_cast<int64_t>(un.a) * nq + t) * H + cp * 8) * 2);
 #pragma unroll
     for (int j = 0; j < 4; ++j) pf.cs[j] = cs[j];
   } else {
@@ -219,6 +233,7 @@ __device__ __forceinline__ void q_prefetch(const AttnArgs& args, const Unit& un,
 #pragma unroll
     for (int j = 0; j < 4; ++j) pf.cs[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  pf.lap = v.cs_lap && tid < D ? v.cs_lap[static_cast<int64_t>(un.a) * D + tid] : 0.f;
 }
 
 // Rotate, scale to log2 units and split into fp16 hi + lo; write the tiles.
@@ -255,84 +270,133 @@ __device__ __forceinline__ void q_build(const QPrefetch<D>& pf, float scale_log2
   *reinterpret_cast<uint4*>(ql_s + r * QSTR + H + cp * 8) = make_uint4(lb[0], lb[1], lb[2], lb[3]);
 }
 
-// ---------------- rotate-on-read
+// ---------------- exact re-base applied on read: the query of the ring's next lap
 //
-// In the rotate-on-read scheme the pool holds pre-RoPE bf16 keys.  Each
-// consumer warp turns its 16 slots of a landed K stage, in place in shared
-// memory, into the keys rotated by R(j - rope_base) (window-relative
-// positions, the exact scheme's table) and rounded once to fp16, then runs
-// exactly as over stored rotated keys.
-//
-// Lane layout: a lane owns the frequency pair (2p, 2p + 1) of one key row,
-// i.e. one 32-bit word in each half of the row (D/4 lanes per row, 128/D rows
-// at a time); at D = 128 the 32 words of one half are one conflict-free
-// 128-byte access.  Ring slots hold consecutive window positions except where
-// the ring wraps, so along a run of 8 slots the (cos, sin) of the following
-// slots come from the run's first row by a recurrence: one complex
-// multiplication with (cos, sin)(omega) for the second slot, then the
-// three-term form y(n+1) = 2 cos(omega) y(n) - y(n-1) (one paired FMA for the
-// cosines, one for the sines).  An error made k positions before the end of a
-// run grows at most k-fold (|sin(k w) / sin(w)| <= k), so after at most 7 steps
-// the pair is within ~2e-6 of the table's, far below the fp16 rounding of the
-// rotated key.  The table row of each run's first slot is loaded before the
-// stage is awaited; the row of the wrap slot (window index 0) once per unit.
-
-// table row (window index + rel_shift) of ring slot `slot`; clamped, since slots
-// past the window hold nothing the consumers use
-__device__ __forceinline__ int rot_row(int slot, int ev_mod, int W, int rel_shift, int t_rows) {
-  int w = slot - ev_mod;
-  if (w < 0) w += W;
-  return min(max(w + rel_shift, 0), t_rows - 1);
+// The query fragments of one k-step hold, per thread, elements 16 ks + 2 tq
+// (+1) and 16 ks + 2 tq + 8 (+1) of query row g; element i < d/2 and its RoPE
+// partner i + d/2 sit in k-steps ks and ks + KSTEPS/2 at the same register,
+// so R(-C) applies to the fragments in place.  Each element is rebuilt in
+// fp32 from its hi + lo parts, rotated with (cos, sin)(-C omega_i), and split
+// into fp16 hi + lo again (a relative error of a few 2^-24, far below the
+// fp16 rounding of the stored key).
+template <int D, int NT>
+__device__ __forceinline__ void lap_shift(uint32_t (&qh)[NT][D / 16][2], uint32_t (&ql)[NT][D / 16][2],
+                                          const float* lap, int tq) {
+  constexpr int HK = D / 32;  // k-steps of the first half of the row
+#pragma unroll
+  for (int ks = 0; ks < HK; ++ks)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      // (cos, sin) of frequencies i, i + 1 with i = 16 ks + 2 tq + 8 r
+      const float4 cs = reinterpret_cast<const float4*>(lap)[(16 * ks + 2 * tq + 8 * r) / 2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float2 ah = __half22float2(*reinterpret_cast<const __half2*>(&qh[nt][ks][r]));
+        const float2 al = __half22float2(*reinterpret_cast<const __half2*>(&ql[nt][ks][r]));
+        const float2 bh = __half22float2(*reinterpret_cast<const __half2*>(&qh[nt][ks + HK][r]));
+        const float2 bl = __half22float2(*reinterpret_cast<const __half2*>(&ql[nt][ks + HK][r]));
+        const float a0 = ah.x + al.x, a1 = ah.y + al.y, b0 = bh.x + bl.x, b1 = bh.y + bl.y;
+        const float ra0 = a0 * cs.x - b0 * cs.y, rb0 = a0 * cs.y + b0 * cs.x;
+        const float ra1 = a1 * cs.z - b1 * cs.w, rb1 = a1 * cs.w + b1 * cs.z;
+        const __half2 ha = __floats2half2_rn(ra0, ra1), hb = __floats2half2_rn(rb0, rb1);
+        const float2 fa = __half22float2(ha), fb = __half22float2(hb);
+        qh[nt][ks][r] = *reinterpret_cast<const uint32_t*>(&ha);
+        qh[nt][ks + HK][r] = *reinterpret_cast<const uint32_t*>(&hb);
+        ql[nt][ks][r] = pack_f16(ra0 - fa.x, ra1 - fa.y);
+        ql[nt][ks + HK][r] = pack_f16(rb0 - fb.x, rb1 - fb.y);
+      }
+    }
 }
 
-// Rotate this lane's words of the 8 rows r0 .. r0+7 of a K block (r0 % 8 == 0, so row r0 + t
-// has swizzle t).  WRAP: the ring wraps at row r0 + t_wrap, whose (cos, sin) is `wrap`.
-template <int D, bool WRAP>
-__device__ __forceinline__ void rot_run(uint8_t* kblk, int r0, int pp, float4 row, float4 wrap, int t_wrap,
-                                        float2 c1, float2 s1, float2 ns1) {
-  uint8_t* p = kblk + r0 * D * 2;
-  uint32_t a[8], b[8];
-#pragma unroll
-  for (int t = 0; t < 8; ++t) {
-    // element 2p of the row sits in chunk p/4 (swizzled to p/4 ^ t), word p%4; its partner
-    // d/2 later in chunk p/4 + d/16
-    const int oa = ((pp * 4) ^ (t << 4)) + t * D * 2;
-    const int ob = oa + (D == 128 ? 128 : ((t & 4) ? -64 : 64));
-    a[t] = *reinterpret_cast<const uint32_t*>(p + oa);
-    b[t] = *reinterpret_cast<const uint32_t*>(p + ob);
+// The order a CTA walks its stages st0 .. st1-1: starting after the stage of the stream's newest
+// ring slot, so that the stage holding the step's new tokens comes last (the producer writes
+// them into the pool just before copying that stage, while the earlier stages stream).
+__device__ __forceinline__ int stage_rot(const StepDesc& d, int nq, int st0, int cnt) {
+  const int newest = static_cast<int>((d.n_old + nq - 1) % d.ring);
+  const int rel = newest / 64 - st0;
+  return rel >= 0 && rel < cnt ? rel + 1 : 0;
+}
+__device__ __forceinline__ int stage_at(int i, int st0, int cnt, int rot) {
+  const int j = i + rot;
+  return st0 + (j >= cnt ? j - cnt : j);
+}
+
+// Fused append (rkv_append_decode_attn, rkv_step): the step's new tokens of (layer, stream, kv
+// head) that fall in stage `st` are written by the producer warp, as rkv_append_rope would write
+// them (key rotated by its cos/sin row and rounded to fp16, the pre-RoPE key for the materialised
+// re-base, the value as given): into the pool for the steps to come and, unless `kstage` is NULL,
+// into their rows of the stage's shared-memory buffer, which the stage's bulk copies then skip.
+// Lane c < D/16 rotates chunk pair (c, c + D/16) of a key, lanes D/16 .. D/16 + D/8 - 1 copy one
+// 16-byte chunk of a value.  Returns the rows written into the stage (bit r: row r).
+__device__ __forceinline__ uint64_t new_rows(const StepDesc& dsc, int nq, int st) {
+  uint64_t m = 0;
+  for (int t = 0; t < nq; ++t) {
+    const int slot = static_cast<int>((dsc.n_old + t) % dsc.ring);
+    if (slot / 64 == st) m |= uint64_t(1) << (slot % 64);
   }
-  float2 c = make_float2(row.x, row.z), s = make_float2(row.y, row.w);
-  float2 cp = c, sp = s;                                   // one position back
-  const float2 tc1 = make_float2(2.f * c1.x, 2.f * c1.y);  // 2 cos(omega), exact
-#pragma unroll
-  for (int t = 0; t < 8; ++t) {
-    if (t > 0) {
-      float2 cn, sn;
-      if (WRAP && t == t_wrap) {
-        cn = make_float2(wrap.x, wrap.z);
-        sn = make_float2(wrap.y, wrap.w);
-      } else if (t == 1 || (WRAP && t == t_wrap + 1)) {  // (c, s) * (cos, sin)(omega)
-        cn = __ffma2_rn(c, c1, __fmul2_rn(s, ns1));
-        sn = __ffma2_rn(s, c1, __fmul2_rn(c, s1));
-      } else {  // 2 cos(omega) y(n) - y(n-1)
-        cn = __ffma2_rn(tc1, c, make_float2(-cp.x, -cp.y));
-        sn = __ffma2_rn(tc1, s, make_float2(-sp.x, -sp.y));
-      }
-      cp = c;
-      sp = s;
-      c = cn;
-      s = sn;
+  return m;
+}
+
+template <int D>
+__device__ __noinline__ void write_new(const AttnArgs& args, const StepDesc& dsc, const Unit& un, int st,
+                                       uint16_t* kstage, int lane) {
+  const DevView& v = args.v;
+  const int nq = v.q_per_step, hkv = v.n_kv_heads, ps = v.page_size;
+  const int layer = args.layer0 + un.lz;
+  constexpr int CP = D / 16, H = D / 2;
+  for (int t = 0; t < nq; ++t) {
+    const int slot = static_cast<int>((dsc.n_old + t) % dsc.ring);
+    if (slot / 64 != st) continue;
+    const int rp = slot / ps, off = slot % ps, r = slot % 64;  // r & 7 == off & 7: the same swizzle
+    const int page = rp < v.max_pages ? v.page_table[static_cast<int64_t>(dsc.stream) * v.max_pages + rp] : -1;
+    if (page < 0 || page >= v.n_pages) {
+      if (lane == 0) record_error(v.status, DEV_BOUNDS, 24, page);
+      continue;
     }
-    const float2 xa = make_float2(__uint_as_float(a[t] << 16), __uint_as_float(a[t] & 0xFFFF0000u));
-    const float2 xb = make_float2(__uint_as_float(b[t] << 16), __uint_as_float(b[t] & 0xFFFF0000u));
-    const float2 nxb = make_float2(-xb.x, -xb.y);
-    const float2 ra = __ffma2_rn(nxb, s, __fmul2_rn(xa, c));  // a cos - b sin
-    const float2 rb = __ffma2_rn(xa, s, __fmul2_rn(xb, c));   // a sin + b cos
-    const int oa = ((pp * 4) ^ (t << 4)) + t * D * 2;
-    const int ob = oa + (D == 128 ? 128 : ((t & 4) ? -64 : 64));
-    *reinterpret_cast<uint32_t*>(p + oa) = pack_f16(ra.x, ra.y);
-    *reinterpret_cast<uint32_t*>(p + ob) = pack_f16(rb.x, rb.y);
+    const int64_t dst = pool_offset(v, layer, page, un.kvh, off);
+    const int64_t row = static_cast<int64_t>(un.a) * nq + t;
+    const int64_t src = un.lz * args.kv_layer_stride + (row * hkv + un.kvh) * D;
+    if (lane < CP) {
+      const int c = lane;
+      const uint4 ka = *reinterpret_cast<const uint4*>(args.k_new + src + c * 8);
+      const uint4 kb = *reinterpret_cast<const uint4*>(args.k_new + src + H + c * 8);
+      const float4* cs = reinterpret_cast<const float4*>(v.cs_new + (row * H + c * 8) * 2);
+      const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kb.x, kb.y, kb.z, kb.w};
+      uint32_t ya[4], yb[4];
+      bool ok = true;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 rc = cs[j];  // (cos, sin) of elements 2j, 2j + 1 of the chunk
+        const float a0 = __uint_as_float(wa[j] << 16), a1 = __uint_as_float(wa[j] & 0xFFFF0000u);
+        const float b0 = __uint_as_float(wb[j] << 16), b1 = __uint_as_float(wb[j] & 0xFFFF0000u);
+        const float ra0 = a0 * rc.x - b0 * rc.y, rb0 = a0 * rc.y + b0 * rc.x;
+        const float ra1 = a1 * rc.z - b1 * rc.w, rb1 = a1 * rc.w + b1 * rc.z;
+        ok = ok && fits_f16(ra0) && fits_f16(ra1) && fits_f16(rb0) && fits_f16(rb1);
+        ya[j] = pack_f16(ra0, ra1);
+        yb[j] = pack_f16(rb0, rb1);
+      }
+      if (!ok) record_error(v.status, DEV_RANGE, 3, c);
+      const int pa = swizzle_chunk(c, off) * 8, pb = swizzle_chunk(c + CP, off) * 8;
+      const uint4 A = make_uint4(ya[0], ya[1], ya[2], ya[3]), B = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+      *reinterpret_cast<uint4*>(v.k_rot + dst + pa) = A;
+      *reinterpret_cast<uint4*>(v.k_rot + dst + pb) = B;
+      if (v.k_raw) {
+        *reinterpret_cast<uint4*>(v.k_raw + dst + pa) = ka;
+        *reinterpret_cast<uint4*>(v.k_raw + dst + pb) = kb;
+      }
+      if (kstage) {
+        *reinterpret_cast<uint4*>(kstage + r * D + pa) = A;
+        *reinterpret_cast<uint4*>(kstage + r * D + pb) = B;
+      }
+    } else if (lane < CP + D / 8) {
+      const int c = lane - CP;
+      const uint4 x = *reinterpret_cast<const uint4*>(args.v_new + src + c * 8);
+      *reinterpret_cast<uint4*>(v.v + dst + swizzle_chunk(c, off) * 8) = x;
+      if (kstage) *reinterpret_cast<uint4*>(kstage + (64 + r) * D + swizzle_chunk(c, off) * 8) = x;
+    }
   }
+  if (kstage) fence_proxy_async_smem();  // the rows written above precede the buffer's next bulk copies
+  __syncwarp();
 }
 
 // Up to two CTAs per SM.  Without a cluster the CTA walks units u = blockIdx.x,
@@ -345,7 +409,7 @@ __device__ __forceinline__ void rot_run(uint8_t* kblk, int r0, int pp, float4 ro
 // moves its K fragments into registers, runs QK^T, moves its V fragments
 // into registers and frees the ring slot before the softmax and PV, so the
 // slot refills while the warp computes.
-template <int D, int NT, bool ON_READ>
+template <int D, int NT, bool ON_READ, bool FUSE>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const __grid_constant__ AttnArgs args) {
   constexpr int KSTEPS = D / 16;  // k-steps of QK^T, m-tiles of PV
   constexpr int QSTR = D + 8;     // padded fp16 row stride of the query tiles
@@ -362,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
   __shared__ float red_m[kCW][ROWS], red_l[kCW][ROWS];
   __shared__ float row_m[ROWS], row_l[ROWS];
   __shared__ int abort_flag, poisoned_s;
+  __shared__ __align__(16) float lap_s[ON_READ ? D : 4];  // (cos, sin)(-C omega_i) of the unit's stream
 
   const DevView& v = args.v;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -392,49 +457,64 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
   if (warp == kCW) {
     // ---------------- producer: the warp walks every stage of every unit in the order the
     // consumers take them; lane 0 issues the bulk copies, the lanes hold 32 page-table
-    // entries at a time, the next unit's descriptor is loaded a unit ahead
-    if (!poisoned) {
+    // entries at a time, the next unit's descriptor is loaded a unit ahead.  With the append
+    // fused, the walk always completes: after a timed-out wait (or in a launch that starts
+    // after one) it still writes every new token into the pool, only the copies stop.
+    if (!poisoned || FUSE) {
       const int ps = v.page_size;
-      const uint16_t* kreg = ON_READ ? v.k_raw : v.k_rot;
+      const uint16_t* kreg = v.k_rot;
       const int copies = ps >= kKS ? 1 : kKS / ps;
       const int rows_per_copy = ps >= kKS ? kKS : ps;
       const uint32_t bytes = static_cast<uint32_t>(rows_per_copy) * D * 2;
-      int k = 0;  // stages issued so far (ring position)
-      bool stop = false;
+      int k = 0;  // stages walked so far (ring position)
+      int k_issued = 0;  // stages walked up to the last one whose copies were issued
+      bool stop = poisoned;
       StepDesc dnext;
-      // the descriptors and the page table come from kernels at least two launches back (see
-      // pdl_wait); the pages may come from the immediate predecessor: copies start after the wait
-      if (u_first < n_units) dnext = v.desc[unit_of(u_first, n_active, hkv).a];
+      // the page table comes from rkv_create; the descriptors from the begin-step kernel, read
+      // before the wait only when it ran two or more launches back (args.early); the pages may
+      // come from the immediate predecessor: the bulk copies start after the wait
+      const bool desc_early = (args.early & kEarlyDesc) != 0;
+      if (u_first < n_units && desc_early && !stop) dnext = v.desc[unit_of(u_first, n_active, hkv).a];
       pdl_wait();
       pdl_launch_dependents();
-      for (int u = u_first; u < n_units && !stop; u += u_step) {
+      if (u_first < n_units && !(desc_early && !poisoned)) dnext = v.desc[unit_of(u_first, n_active, hkv).a];
+      for (int u = u_first; u < n_units; u += u_step) {
         const Unit un = unit_of(u, n_active, hkv);
         const StepDesc dsc = dnext;
         if (u + u_step < n_units) dnext = v.desc[unit_of(u + u_step, n_active, hkv).a];  // lands during this unit
         const int layer = args.layer0 + un.lz;
         const int n_st = (slots_in_use(dsc) + kKS - 1) / kKS;
         const int st0 = split * args.stages_per_split;
-        const int st1 = min(st0 + args.stages_per_split, n_st);
-        const int stream_pages = (dsc.window + ps - 1) / ps;
+        const int cnt = max(0, min(st0 + args.stages_per_split, n_st) - st0);
+        const int rot = stage_rot(dsc, v.q_per_step, st0, cnt);
+        const int stream_pages = (dsc.ring + ps - 1) / ps;
         const int32_t* ptab = v.page_table + static_cast<int64_t>(dsc.stream) * v.max_pages;
         int pbase = -64, pt_lane = 0;
-        for (int st = st0; st < st1; ++st, ++k) {
+        for (int i = 0; i < cnt; ++i, ++k) {
+          const int st = stage_at(i, st0, cnt, rot);
           const int buf = k % kStages;
-          if (k >= kStages &&
-              !__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty_bar[buf]), ((k / kStages) - 1) & 1))) {
+          if (!stop && k >= kStages &&
+              !__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty_bar[buf]), ((k / kStages) - 1) & 1, v.wait_ns))) {
             if (lane == 0) {
               record_error(v.status, DEV_TIMEOUT, 20, k);
               atomicExch(&abort_flag, 1);
             }
             stop = true;
-            break;
           }
-          if (__any_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&abort_flag) != 0)) {
-            stop = true;
-            break;
+          if (!stop && __any_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&abort_flag) != 0)) stop = true;
+          if (!stop) k_issued = k + 1;
+          // fused append: the stage's new rows go into the pool and, when the stage is copied,
+          // into its buffer, which the copies below then skip
+          const uint64_t patched = FUSE ? new_rows(dsc, v.q_per_step, st) : 0;
+          // the failure-detection test hook: this stage's copy never starts, so its consumers'
+          // bounded wait runs out
+          if (stop || k == v.withhold_stage) {
+            if (FUSE && patched) write_new<D>(args, dsc, un, st, nullptr, lane);
+            continue;
           }
+          if (FUSE && patched) write_new<D>(args, dsc, un, st, kv_s + buf * 2 * STAGE_ELEMS, lane);
           const uint32_t fb = smem_u32(&full_bar[buf]);
-          if (lane == 0) mbar_arrive_expect_tx(fb, 2u * kKS * D * 2);
+          if (lane == 0) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(kKS - __popcll(patched)) * D * 2 * 2);
           for (int c = 0; c < copies; ++c) {
             const int slot = st * kKS + c * rows_per_copy;
             int rp = slot / ps;
@@ -452,16 +532,33 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
             if (lane == 0) {
               const int64_t src = pool_offset(v, layer, page, un.kvh, off);
               const uint32_t dk = smem_u32(kv_s + buf * 2 * STAGE_ELEMS + c * rows_per_copy * D);
-              bulk_copy_g2s(dk, kreg + src, bytes, fb);
-              bulk_copy_g2s(dk + STAGE_ELEMS * 2, v.v + src, bytes, fb);
+              const int r0 = c * rows_per_copy;
+              if (!FUSE || ((patched >> r0) & ((uint64_t(2) << (rows_per_copy - 1)) - 1)) == 0) {
+                bulk_copy_g2s(dk, kreg + src, bytes, fb);
+                bulk_copy_g2s(dk + STAGE_ELEMS * 2, v.v + src, bytes, fb);
+              } else {  // runs of rows around the ones written above
+                for (int a = 0; a < rows_per_copy;) {
+                  if ((patched >> (r0 + a)) & 1) {
+                    ++a;
+                    continue;
+                  }
+                  int b = a;
+                  while (b < rows_per_copy && !((patched >> (r0 + b)) & 1)) ++b;
+                  const uint32_t nb = static_cast<uint32_t>(b - a) * D * 2;
+                  bulk_copy_g2s(dk + a * D * 2, kreg + src + a * D, nb, fb);
+                  bulk_copy_g2s(dk + STAGE_ELEMS * 2 + a * D * 2, v.v + src + a * D, nb, fb);
+                  a = b;
+                }
+              }
             }
           }
         }
       }
-      // never leave with copies in flight (only reachable on an aborted run)
+      // never leave with copies in flight (only reachable on an aborted run): the last kStages
+      // stages whose copies were issued
       if (lane == 0)
-        for (int i = max(0, k - kStages); i < k; ++i)
-          if (!mbar_wait(smem_u32(&full_bar[i % kStages]), (i / kStages) & 1))
+        for (int i = max(0, k_issued - kStages); i < k_issued; ++i)
+          if (i != v.withhold_stage && !mbar_wait(smem_u32(&full_bar[i % kStages]), (i / kStages) & 1, v.wait_ns))
             record_error(v.status, DEV_TIMEOUT, 22, i);
     }
   } else if (!poisoned) {
@@ -473,49 +570,55 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
     const int mi = lane >> 3, ri = lane & 7;
     const int krow = wt * 16 + ri + (mi & 1) * 8, kchunk = mi >> 1;  // K as the A operand
     const int vrow = wt * 16 + ri + (mi >> 1) * 8, vchunk = mi & 1;  // V^T as the A operand
-    // rotating on read: this lane's frequency pair (lane % (d/4)) in the table; (cos, sin)(omega)
-    const float4* rtab = reinterpret_cast<const float4*>(v.rope_table) + lane % (D / 4);
-    float2 rc1 = make_float2(1.f, 1.f), rs1 = make_float2(0.f, 0.f), rns1 = rs1;
-    if (ON_READ && v.t_rows > 1) {
-      const float4 t = __ldg(rtab + D / 4);
-      rc1 = make_float2(t.x, t.z);
-      rs1 = make_float2(t.y, t.w);
-      rns1 = make_float2(-t.y, -t.w);
-    }
     QPrefetch<D> pf;
     StepDesc dnext;
-    // descriptors and angles come from the begin-step kernel, two or more launches back; the
-    // queries only when the launcher says so (args.q_early), else after the wait
+    // descriptors, angles and queries before the wait only as args.early allows
+    const bool desc_early = (args.early & kEarlyDesc) != 0, q_early = (args.early & kEarlyQ) != 0;
     if (u_first < n_units) {
       const Unit un0 = unit_of(u_first, n_active, hkv);
-      if (args.q_early) q_prefetch<D>(args, un0, tid, pf);
-      dnext = v.desc[un0.a];
+      if (desc_early) dnext = v.desc[un0.a];
+      if (desc_early && q_early) q_prefetch<D>(args, un0, tid, pf);
     }
     pdl_wait();
-    if (u_first < n_units && !args.q_early) q_prefetch<D>(args, unit_of(u_first, n_active, hkv), tid, pf);
+    if (u_first < n_units) {
+      const Unit un0 = unit_of(u_first, n_active, hkv);
+      if (!desc_early) dnext = v.desc[un0.a];
+      if (!(desc_early && q_early)) q_prefetch<D>(args, un0, tid, pf);
+    }
     int k0 = 0;  // ring position of the unit's first stage
     for (int u = u_first; u < n_units; u += u_step) {
       const Unit un = unit_of(u, n_active, hkv);
       const StepDesc dsc = dnext;
-      const int W = dsc.window, len = dsc.len;
+      const int W = dsc.ring, len = dsc.len;  // W: the ring's modulus
       const int nslots = slots_in_use(dsc);
       const int n_st = (nslots + kKS - 1) / kKS;
       const int st0 = split * args.stages_per_split;
       const int my_st = max(0, min(st0 + args.stages_per_split, n_st) - st0);
+      const int rot = stage_rot(dsc, nq, st0, my_st);
 
       q_build<D, NT>(pf, v.scale_log2, tid, qh_s, ql_s);
+      if constexpr (ON_READ) {
+        if (tid < D) lap_s[tid] = pf.lap;
+      }
       consumer_sync();  // S1: query tiles ready; the previous unit's output pass is over
       uint32_t qh[NT][KSTEPS][2], ql[NT][KSTEPS][2];
+      auto load_q = [&]() {  // the query fragments (B operand) from the tiles
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int ks = 0; ks < KSTEPS; ++ks) {
-          const int base = (nt * 8 + g) * QSTR + ks * 16 + 2 * tq;
-          qh[nt][ks][0] = *reinterpret_cast<const uint32_t*>(qh_s + base);
-          qh[nt][ks][1] = *reinterpret_cast<const uint32_t*>(qh_s + base + 8);
-          ql[nt][ks][0] = *reinterpret_cast<const uint32_t*>(ql_s + base);
-          ql[nt][ks][1] = *reinterpret_cast<const uint32_t*>(ql_s + base + 8);
-        }
+          for (int ks = 0; ks < KSTEPS; ++ks) {
+            const int base = (nt * 8 + g) * QSTR + ks * 16 + 2 * tq;
+            qh[nt][ks][0] = *reinterpret_cast<const uint32_t*>(qh_s + base);
+            qh[nt][ks][1] = *reinterpret_cast<const uint32_t*>(qh_s + base + 8);
+            ql[nt][ks][0] = *reinterpret_cast<const uint32_t*>(ql_s + base);
+            ql[nt][ks][1] = *reinterpret_cast<const uint32_t*>(ql_s + base + 8);
+          }
+      };
+      load_q();
+      // on read: whether the fragments hold the next lap's query (R(-C) applied), for the ring
+      // slots below evicted mod C
+      bool lap_b = false;
+      const float* lap = lap_s;
       if (u + u_step < n_units) {  // the next unit's query and descriptor land during this unit
         const Unit un1 = unit_of(u + u_step, n_active, hkv);
         q_prefetch<D>(args, un1, tid, pf);
@@ -537,24 +640,12 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
 
       const int ev_mod = static_cast<int>(dsc.evicted % W);
       const int first_new = len - nq;  // window index of the step's first new token
-      const int rel_shift = static_cast<int>(dsc.evicted - dsc.rope_base);
-      float4 rwrap = make_float4(1.f, 0.f, 1.f, 0.f);  // (cos, sin) at window index 0
-      if constexpr (ON_READ) rwrap = __ldg(rtab + static_cast<int64_t>(min(max(rel_shift, 0), v.t_rows - 1)) * (D / 4));
       bool aborted = false;
       for (int i = 0; i < my_st; ++i) {
         const int k = k0 + i;
         const int buf = k % kStages;
         // warp-uniform decision: every lane leaves together if any lane gave up
-        // rotating on read: the table rows of this warp's runs, loaded while the stage lands
-        float4 rrow[ON_READ ? 2 / (128 / D) : 1];
-        if constexpr (ON_READ) {
-#pragma unroll
-          for (int j = 0; j < 2 / (128 / D); ++j) {
-            const int run = 2 * wt + (D == 128 ? j : lane / 16);
-            rrow[j] = __ldg(rtab + static_cast<int64_t>(rot_row((st0 + i) * kKS + run * 8, ev_mod, W, rel_shift, v.t_rows)) * (D / 4));
-          }
-        }
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[buf]), (k / kStages) & 1))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[buf]), (k / kStages) & 1, v.wait_ns))) {
           if (lane == 0) {
             record_error(v.status, DEV_TIMEOUT, 23, k);
             atomicExch(&abort_flag, 1);
@@ -562,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
           aborted = true;
           break;
         }
-        const int slot_base = (st0 + i) * kKS + wt * 16;
+        const int slot_base = stage_at(i, st0, my_st, rot) * kKS + wt * 16;
         const uint32_t kb = smem_u32(kv_s + buf * 2 * STAGE_ELEMS);
         const uint32_t vb = kb + STAGE_ELEMS * 2;
         if (slot_base >= nslots) {  // none of this warp's slots holds a token
@@ -579,21 +670,6 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
           if (w < 0) w += W;
           widx[hk] = slot < nslots ? w : -1;
         }
-        if constexpr (ON_READ) {
-          // rotate this warp's 16 pre-RoPE keys in place (two runs of 8 slots), then let the
-          // warp's lanes see each other's words
-          uint8_t* kblk = reinterpret_cast<uint8_t*>(kv_s + buf * 2 * STAGE_ELEMS);
-#pragma unroll
-          for (int j = 0; j < 2 / (128 / D); ++j) {
-            const int run = 2 * wt + (D == 128 ? j : lane / 16);
-            const int tw = ev_mod - ((st0 + i) * kKS + run * 8);
-            if (tw > 0 && tw < 8)
-              rot_run<D, true>(kblk, run * 8, lane % (D / 4), rrow[j], rwrap, tw, rc1, rs1, rns1);
-            else
-              rot_run<D, false>(kblk, run * 8, lane % (D / 4), rrow[j], rwrap, 0, rc1, rs1, rns1);
-          }
-          __syncwarp();
-        }
         // K fragments of this warp's 16 slots (the A operand, one per k-step)
         uint32_t kf[KSTEPS][4];
 #pragma unroll
@@ -603,24 +679,60 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sh[nt][e] = sl[nt][e] = 0.f;
+        auto qk = [&](float (&ah)[NT][4], float (&al)[NT][4]) {
 #pragma unroll
-        for (int ks = 0; ks < KSTEPS; ++ks)
+          for (int ks = 0; ks < KSTEPS; ++ks)
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mma_f16(sh[nt], kf[ks], qh[nt][ks][0], qh[nt][ks][1]);
-            mma_f16(sl[nt], kf[ks], ql[nt][ks][0], ql[nt][ks][1]);
+            for (int nt = 0; nt < NT; ++nt) {
+              mma_f16(ah[nt], kf[ks], qh[nt][ks][0], qh[nt][ks][1]);
+              mma_f16(al[nt], kf[ks], ql[nt][ks][0], ql[nt][ks][1]);
+            }
+        };
+        if constexpr (ON_READ) {
+          // warp-uniform: slots [slot_base, slot_base + 16) against ev_mod
+          if (slot_base + 16 <= ev_mod) {         // all of the next lap
+            if (!lap_b) lap_shift<D, NT>(qh, ql, lap, tq);
+            lap_b = true;
+            qk(sh, sl);
+          } else if (slot_base >= ev_mod) {       // all of the current lap
+            if (lap_b) load_q();
+            lap_b = false;
+            qk(sh, sl);
+          } else {                                // the chunk where the two laps meet
+            float bh[NT][4], bl[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) bh[nt][e] = bl[nt][e] = 0.f;
+            if (!lap_b) lap_shift<D, NT>(qh, ql, lap, tq);
+            qk(bh, bl);
+            load_q();
+            lap_b = false;
+            qk(sh, sl);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (slot_base + g + 8 * (e >> 1) < ev_mod) {
+                  sh[nt][e] = bh[nt][e];
+                  sl[nt][e] = bl[nt][e];
+                }
           }
+        } else {
+          qk(sh, sl);
+        }
         // V fragments (V^T as the A operand, one per m-tile), then the slot refills while we compute
         uint32_t vf[KSTEPS][4];
 #pragma unroll
         for (int mt = 0; mt < KSTEPS; ++mt) ldsm_x4_t(vb + vrow * D * 2 + (swizzle_chunk(2 * mt + vchunk, ri) << 4), vf[mt]);
-        if constexpr (ON_READ) fence_proxy_async_smem();  // the rotated keys precede the slot's next bulk copy
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty_bar[buf]));
         // online softmax; C layout: e = 0,1 key g rows 2tq, 2tq+1; e = 2,3 key g+8.  A chunk
-        // whose slots all hold tokens that every query of the step sees needs no mask.
+        // whose slots all hold tokens that every query of the step sees needs no mask (one query
+        // and every written slot in the window: no test needed).
         const bool full_chunk = slot_base + 16 <= nslots &&
-                                (nq == 1 || __all_sync(0xffffffffu, widx[0] <= first_new && widx[1] <= first_new));
+                                ((nq == 1 && len == nslots) ||
+                                 __all_sync(0xffffffffu, widx[0] <= first_new && widx[1] <= first_new));
         uint32_t pb[NT][2];
         float alpha[NT][2];
 #pragma unroll
@@ -856,7 +968,7 @@ __global__ void __launch_bounds__(128) merge_kernel(DevView v, int splits, uint1
   if (lse && threadIdx.x == 0) lse[blockIdx.x] = (mx + log2f(lsum)) * 0.69314718055994531f;
 }
 
-template <int D, int NT, bool ON_READ>
+template <int D, int NT, bool ON_READ, bool FUSE>
 struct Kernel {
   // The dynamic shared-memory opt-in is per device, so it and the occupancy it gives are
   // set up once for every device the process uses.
@@ -868,10 +980,10 @@ struct Kernel {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
     std::lock_guard<std::mutex> lock(mu);
     if (occ[dev] == 0) {
-      cudaFuncSetAttribute(attn_kernel<D, NT, ON_READ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(attn_kernel<D, NT, ON_READ, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem_bytes<D, NT>());
       int o = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, attn_kernel<D, NT, ON_READ>, kThreads,
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, attn_kernel<D, NT, ON_READ, FUSE>, kThreads,
                                                         smem_bytes<D, NT>()) != cudaSuccess)
         o = 1;
       occ[dev] = o < 1 ? 1 : o;
@@ -897,13 +1009,13 @@ struct Kernel {
       attr[1].val.clusterDim.z = 1;
       cfg.numAttrs = 2;
     }
-    return cudaLaunchKernelEx(&cfg, attn_kernel<D, NT, ON_READ>, args);
+    return cudaLaunchKernelEx(&cfg, attn_kernel<D, NT, ON_READ, FUSE>, args);
   }
 };
 
 template <int D, int NT>
 int occupancy_of(bool on_read) {
-  return on_read ? Kernel<D, NT, true>::occupancy() : Kernel<D, NT, false>::occupancy();
+  return on_read ? Kernel<D, NT, true, false>::occupancy() : Kernel<D, NT, false, false>::occupancy();
 }
 
 int occupancy_for(const DevView& v) {
@@ -915,8 +1027,10 @@ int occupancy_for(const DevView& v) {
 
 template <int D, int NT>
 cudaError_t dispatch_on_read(const AttnArgs& args, int grid, cudaStream_t st) {
-  if (args.v.scheme == RKV_SCHEME_EXACT_ON_READ) return Kernel<D, NT, true>::launch(args, grid, st);
-  return Kernel<D, NT, false>::launch(args, grid, st);
+  const bool fuse = args.k_new != nullptr;
+  if (args.v.scheme == RKV_SCHEME_EXACT_ON_READ)
+    return fuse ? Kernel<D, NT, true, true>::launch(args, grid, st) : Kernel<D, NT, true, false>::launch(args, grid, st);
+  return fuse ? Kernel<D, NT, false, true>::launch(args, grid, st) : Kernel<D, NT, false, false>::launch(args, grid, st);
 }
 
 cudaError_t dispatch(const AttnArgs& args, int grid, cudaStream_t st) {
@@ -945,7 +1059,10 @@ AttnArgs make_args(const DevView& v, int n_active, int layer0, int n_layers, con
   args.splits = p.splits;
   args.stages_per_split = p.stages_per_split;
   args.mode = 0;
-  args.q_early = 0;
+  args.early = 0;
+  args.k_new = nullptr;
+  args.v_new = nullptr;
+  args.kv_layer_stride = 0;
   return args;
 }
 
@@ -982,10 +1099,13 @@ AttnPlan plan_decode_attn(const DevView& v, int n_active, int n_layers, bool clu
 
 cudaError_t launch_decode_attn(const DevView& v, int n_active, int layer0, int n_layers, const uint16_t* q,
                                uint16_t* out, float* lse, int64_t q_layer_stride, int64_t lse_layer_stride,
-                               bool q_early, cudaStream_t st) {
+                               const AttnExtras& x, cudaStream_t st) {
   const AttnPlan p = plan_decode_attn(v, n_active, n_layers, true);
   AttnArgs args = make_args(v, n_active, layer0, n_layers, q, out, lse, q_layer_stride, lse_layer_stride, p);
-  args.q_early = q_early ? 1 : 0;
+  args.early = x.early;
+  args.k_new = x.k_new;
+  args.v_new = x.v_new;
+  args.kv_layer_stride = x.kv_layer_stride;
   const int64_t units = static_cast<int64_t>(n_active) * v.n_kv_heads * n_layers;
   args.mode = p.cluster ? 1 : 0;
   const int64_t grid = p.cluster ? units * p.splits : (units < p.slots ? units : p.slots);
@@ -998,7 +1118,7 @@ cudaError_t launch_decode_attn_scratch(const DevView& v, int n_active, int layer
   AttnArgs args = make_args(v, n_active, layer, 1, q, out, lse, 0, 0, p);
   const int64_t units = static_cast<int64_t>(n_active) * v.n_kv_heads;
   args.mode = p.splits > 1 ? 2 : 0;
-  args.q_early = 0;
+  args.early = kEarlyDesc;  // rkv_append_rope ran after the begin-step kernel
   const int64_t grid = p.splits > 1 ? units * p.splits : (units < p.slots ? units : p.slots);
   cudaError_t e = dispatch(args, static_cast<int>(grid), st);
   if (e != cudaSuccess || p.splits == 1) return e;

@@ -11,6 +11,7 @@
 namespace rkv {
 
 constexpr int kStateFields = RKV_STATE_FIELDS;
+constexpr unsigned long long kDefaultWaitNs = 1000000000ull;  // a bounded device wait gives up after 1 s
 // state field indices (order reported by rkv_get_stream_state)
 enum { F_N = 0, F_LEN, F_EVICTED, F_KV_POS_OFFSET, F_ROPE_BASE, F_HEAD_SLOT, F_W, F_P0 };
 
@@ -25,7 +26,7 @@ struct StepDesc {
   int64_t delta;      // exact scheme: re-base amount this step (0: none)
   int32_t stream;     // stream id
   int32_t len;        // window length after this step
-  int32_t window;     // W
+  int32_t ring;       // ring capacity C = W + window_slack: token j lives in ring slot j mod C
   int32_t pad;
 };
 
@@ -34,21 +35,27 @@ struct DevView {
   int64_t* state;        // [S][8]
   int32_t* page_table;   // [S][max_pages] -> physical page
   StepDesc* desc;        // [S] by active index
-  float* cs_new;         // [S][Q][d/2][2] cos/sin of the new tokens' positions
-  float* rope_table;     // [t_rows][d/2][2] cos/sin of r * omega, r < t_rows (exact scheme)
+  float* cs_new;         // [S][Q][d/2][2] cos/sin of the new keys' stored positions
+  float* cs_q;           // [S][Q][d/2][2] cos/sin of the queries' positions (= cs_new except on read)
+  float* cs_lap;         // [S][d/2][2] cos/sin of -W * omega (rotate-on-read scheme only)
+  float* rope_table;     // [t_rows][d/2][2] cos/sin of r * omega, r < t_rows (materialised exact re-base)
   double* omega;         // [d/2]
   float* part_ml;        // [S][Q*Hq][splits][2] (running max in log2 units, sum)
   float* part_o;         // [S][Q*Hq][splits][d] normalised partial outputs
   int32_t* status;       // [4]: code, detail, detail2, unused
-  uint16_t* k_rot;       // pool: [L][n_pages][Hkv][ps][d] rotated keys, fp16 bits (NULL: rotate-on-read scheme)
+  uint16_t* k_rot;       // pool: [L][n_pages][Hkv][ps][d] rotated keys, fp16 bits
   uint16_t* v;           // pool: values (bf16 bits), same layout
-  uint16_t* k_raw;       // pool: pre-RoPE keys (bf16 bits; exact schemes), same layout
+  uint16_t* k_raw;       // pool: pre-RoPE keys (bf16 bits; materialised exact re-base only), same layout
   int64_t layer_stride;  // elements of one layer in one pool region
   int32_t n_streams, n_layers, n_q_heads, n_kv_heads, head_dim, q_per_step;
   int32_t page_size, n_pages, max_pages, t_rows;
-  int32_t scheme, rebase_interval;
+  int32_t scheme, rebase_interval, window_slack;
   int32_t num_sms;       // host-side launch planning only
   float scale_log2;      // softmax scale * log2(e)
+  // failure-detection test hook (rkv_set_wait_test): bounded waits give up after wait_ns; the
+  // attention producer skips the copy of its stage number withhold_stage (-1: none)
+  unsigned long long wait_ns;
+  int32_t withhold_stage;
 };
 
 // Both exact schemes keep window-relative key positions and a rope_base.
@@ -158,6 +165,7 @@ __device__ __forceinline__ int64_t pool_offset(const DevView& v, int layer, int 
 cudaError_t launch_init_tables(const DevView& v, cudaStream_t st);
 cudaError_t launch_begin_step(const DevView& v, const ActiveIds& ids, cudaStream_t st);
 cudaError_t launch_reset_stream(const DevView& v, int s, int64_t p0, cudaStream_t st);
+cudaError_t launch_reset_streams(const DevView& v, const int32_t* ids, const int64_t* p0, int n, cudaStream_t st);
 // Layers [layer0, layer0 + n_layers) in one launch; per-layer tensors of the
 // step's inputs/outputs are `*_layer_stride` elements apart.
 cudaError_t launch_append_rope(const DevView& v, int n_active, int layer0, int n_layers, const uint16_t* k,
@@ -175,9 +183,18 @@ struct AttnPlan {
 // false: every split writes (m, l, o) to part_ml / part_o and a merge kernel
 // combines them (single layer only).
 AttnPlan plan_decode_attn(const DevView& v, int n_active, int n_layers, bool cluster);
+// What a decode-attention launch may read before its dependency wait, and the fused append.
+constexpr int kEarlyDesc = 1;  // step descriptors and angles: the begin-step kernel ran two or more launches back
+constexpr int kEarlyQ = 2;     // the queries: written before the call that launches (rkv_step)
+struct AttnExtras {
+  int early = 0;
+  const uint16_t* k_new = nullptr;  // fused append: pre-RoPE keys [layer][A][Q][Hkv][d]
+  const uint16_t* v_new = nullptr;  // and values, written into the pool by the attention launch
+  int64_t kv_layer_stride = 0;
+};
 cudaError_t launch_decode_attn(const DevView& v, int n_active, int layer0, int n_layers, const uint16_t* q,
                                uint16_t* out, float* lse, int64_t q_layer_stride, int64_t lse_layer_stride,
-                               bool q_early, cudaStream_t st);
+                               const AttnExtras& x, cudaStream_t st);
 // the split-K form with partials in v.part_ml / v.part_o (one layer)
 cudaError_t launch_decode_attn_scratch(const DevView& v, int n_active, int layer, const uint16_t* q, uint16_t* out,
                                        float* lse, cudaStream_t st);

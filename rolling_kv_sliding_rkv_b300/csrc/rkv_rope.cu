@@ -40,21 +40,35 @@ __global__ void init_tables_kernel(DevView v) {
 // One block per active stream: advance the ring state (host-side rules in
 // rkv.h, rkv_begin_step), record the step descriptor, then cos/sin of the
 // positions of the step's new tokens.
+//
+// Positions per scheme, for new token j = n_old + t:
+//   offset-only         keys and queries at P0 + j;
+//   exact re-base       keys and queries at j - rope_base (window-relative);
+//   exact, on read      key stored at its ring slot j mod C (C = W +
+//                       window_slack, the ring's capacity); the query at
+//                       j - C * floor(evicted / C) against the keys of ring
+//                       slots >= evicted mod C, and C less against the slots
+//                       below (tokens of the ring's next lap), the second by
+//                       the rotation R(-C) the kernel applies to the first.
+//   Every score then sees the position difference of its two tokens.
 __global__ void begin_step_kernel(DevView v, ActiveIds ids) {
   pdl_wait();
   pdl_launch_dependents();
   const int a = blockIdx.x;
   const int s = ids.id[a];
-  __shared__ int64_t pos0;
+  __shared__ int64_t pos0, qpos0, win;
   if (threadIdx.x == 0) {
     int64_t* st = v.state + static_cast<int64_t>(s) * kStateFields;
     const int64_t n_old = st[F_N];
     const int64_t w = st[F_W];
     const int64_t p0 = st[F_P0];
     int64_t rope_base = st[F_ROPE_BASE];
+    const int64_t ring = w + v.window_slack;  // ring capacity C
     const int64_t n = n_old + v.q_per_step;
-    const int64_t len = n < w ? n : w;
-    const int64_t ev = n - len;
+    // keep every token while they fit in the ring; when this step's would not, evict down to the
+    // last W in one batch (window_slack = 0: exactly enough every step, a plain sliding window)
+    const int64_t ev = n - st[F_EVICTED] > ring ? n - w : st[F_EVICTED];
+    const int64_t len = n - ev;
     int64_t delta = 0;
     if (exact_scheme(v.scheme) && ev - rope_base >= v.rebase_interval) {
       delta = ev - rope_base;
@@ -65,7 +79,7 @@ __global__ void begin_step_kernel(DevView v, ActiveIds ids) {
     st[F_EVICTED] = ev;
     st[F_KV_POS_OFFSET] = p0 + ev;
     st[F_ROPE_BASE] = rope_base;
-    st[F_HEAD_SLOT] = ev % w;
+    st[F_HEAD_SLOT] = ev % ring;
     StepDesc d;
     d.n_old = n_old;
     d.evicted = ev;
@@ -73,22 +87,38 @@ __global__ void begin_step_kernel(DevView v, ActiveIds ids) {
     d.delta = delta;
     d.stream = s;
     d.len = static_cast<int32_t>(len);
-    d.window = static_cast<int32_t>(w);
+    d.ring = static_cast<int32_t>(ring);
     d.pad = 0;
     v.desc[a] = d;
-    // the logical position P0 + j (offset-only), or j - rope_base (exact)
-    pos0 = exact_scheme(v.scheme) ? n_old - rope_base : p0 + n_old;
+    // the logical position P0 + j (offset-only), j - rope_base (exact re-base), or the ring lap's
+    // origin for the queries of the on-read scheme (keys: their slot, below)
+    pos0 = v.scheme == RKV_SCHEME_EXACT_REBASE ? n_old - rope_base : p0 + n_old;
+    qpos0 = n_old - (ev / ring) * ring;
+    win = ring;
   }
   __syncthreads();
   const int half = v.head_dim / 2;
+  const bool on_read = v.scheme == RKV_SCHEME_EXACT_ON_READ;
   for (int idx = threadIdx.x; idx < v.q_per_step * half; idx += blockDim.x) {
     const int t = idx / half, i = idx % half;
+    const int64_t row = ((static_cast<int64_t>(a) * v.q_per_step + t) * half + i) * 2;
     float c, sn;
-    rope_cos_sin(pos0 + t, v.omega[i], &c, &sn);
-    float* dst = v.cs_new + ((static_cast<int64_t>(a) * v.q_per_step + t) * half + i) * 2;
-    dst[0] = c;
-    dst[1] = sn;
+    rope_cos_sin(on_read ? (qpos0 + t) % win : pos0 + t, v.omega[i], &c, &sn);
+    v.cs_new[row] = c;
+    v.cs_new[row + 1] = sn;
+    if (on_read) {
+      rope_cos_sin(qpos0 + t, v.omega[i], &c, &sn);
+      v.cs_q[row] = c;
+      v.cs_q[row + 1] = sn;
+    }
   }
+  if (on_read)
+    for (int i = threadIdx.x; i < half; i += blockDim.x) {
+      float c, sn;
+      rope_cos_sin(-win, v.omega[i], &c, &sn);
+      v.cs_lap[(static_cast<int64_t>(a) * half + i) * 2] = c;
+      v.cs_lap[(static_cast<int64_t>(a) * half + i) * 2 + 1] = sn;
+    }
 }
 
 // One thread: empty stream s (its pages keep stale data, which the ring
@@ -104,7 +134,37 @@ __global__ void reset_stream_kernel(DevView v, int s, int64_t p0) {
   st[F_P0] = p0;  // F_W is kept: the stream's pages fix its window
 }
 
+// One thread per entry of a device-side list: reset stream ids[i] to start offset p0[i] (as
+// reset_stream_kernel); negative ids are skipped, entries out of range are reported.
+__global__ void reset_streams_kernel(DevView v, const int32_t* __restrict__ ids, const int64_t* __restrict__ p0,
+                                     int n) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int s = ids[i];
+  const int64_t start = p0[i];
+  if (s < 0) return;
+  if (s >= v.n_streams || start < 0 || start >= (int64_t(1) << 52)) {
+    record_error(v.status, DEV_BOUNDS, 5, s);
+    return;
+  }
+  int64_t* st = v.state + static_cast<int64_t>(s) * kStateFields;
+  st[F_N] = 0;
+  st[F_LEN] = 0;
+  st[F_EVICTED] = 0;
+  st[F_KV_POS_OFFSET] = start;
+  st[F_ROPE_BASE] = 0;
+  st[F_HEAD_SLOT] = 0;
+  st[F_P0] = start;
+}
+
 }  // namespace
+
+cudaError_t launch_reset_streams(const DevView& v, const int32_t* ids, const int64_t* p0, int n, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  return launch_pdl(reset_streams_kernel, dim3((n + 127) / 128), dim3(128), 0, st, v, ids, p0, n);
+}
 
 cudaError_t launch_reset_stream(const DevView& v, int s, int64_t p0, cudaStream_t st) {
   reset_stream_kernel<<<1, 1, 0, st>>>(v, s, p0);

@@ -39,6 +39,7 @@ class Workload:
     tick_ms: int = 0          # >0: mixed-clock schedule on a tick of this length
     ragged_fill: bool = False
     rebase_interval: int = 1
+    window_slack: int = 0     # ring capacity beyond the window (eviction in batches); 0: every step
     extra: dict = field(default_factory=dict)
 
     @property

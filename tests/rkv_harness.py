@@ -37,8 +37,9 @@ def run_gpu(wl: synth.Workload, n_ticks: int, want: set, streams_of_interest=Non
     whole_step: drive rkv_step (all layers per launch) instead of the
     per-layer calls; the inputs are the same generator draws
     (rkv_gen_next_inputs, every layer of the step in one launch).
-    attn: "regular" (rkv_decode_attn) or "static" (rkv_decode_attn_static) for
-    the per-layer calls.
+    attn: the per-layer calls: "regular" (rkv_append_rope, rkv_decode_attn),
+    "static" (rkv_append_rope, rkv_decode_attn_static) or "fused"
+    (rkv_append_decode_attn).
     """
     import torch
 
@@ -50,7 +51,8 @@ def run_gpu(wl: synth.Workload, n_ticks: int, want: set, streams_of_interest=Non
     h = rkv.RollingKV(windows.tolist(), p0.tolist(), device=dev, n_layers=wl.n_layers, n_streams=wl.n_streams,
                       n_q_heads=wl.n_q_heads, n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim,
                       q_per_step=wl.q_per_step, scheme=wl.scheme, rebase_interval=wl.rebase_interval,
-                      rope_theta=wl.rope_theta, page_size=int(wl.extra.get("page_size", 64)))
+                      rope_theta=wl.rope_theta, page_size=int(wl.extra.get("page_size", 64)),
+                      window_slack=wl.window_slack)
     S, L, Q, hq, hkv, d = wl.n_streams, wl.n_layers, wl.q_per_step, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
     q = torch.empty(S * Q * hq * d, dtype=torch.bfloat16, device=dev)
     k = torch.empty(S * Q * hkv * d, dtype=torch.bfloat16, device=dev)
@@ -60,7 +62,8 @@ def run_gpu(wl: synth.Workload, n_ticks: int, want: set, streams_of_interest=Non
     exact = wl.scheme in (rkv.RKV_SCHEME_EXACT_REBASE, rkv.RKV_SCHEME_EXACT_ON_READ)
     # both exact schemes keep the same bookkeeping; they differ only in what the pool stores
     ring_scheme = rkv.RKV_SCHEME_EXACT_REBASE if exact else rkv.RKV_SCHEME_OFFSET_ONLY
-    rings = {s: StreamRing(int(windows[s]), int(p0[s]), Q, ring_scheme, wl.rebase_interval) for s in range(S)}
+    rings = {s: StreamRing(int(windows[s]), int(p0[s]), Q, ring_scheme, wl.rebase_interval,
+                           capacity=int(windows[s]) + wl.window_slack) for s in range(S)}
     run = Run()
     want_streams = {s for s, _, _ in want}
     if whole_step:
@@ -101,11 +104,14 @@ def run_gpu(wl: synth.Workload, n_ticks: int, want: set, streams_of_interest=Non
             h.gen_step_inputs(wl.seed, layer, wl.input_scale, q, k, v)
             if exact:
                 h.rebase(layer)
-            h.append_rope(layer, k, v)
-            if attn == "static":
-                rkv.rkv_decode_attn_static(h.handle, layer, q, out, lse)
+            if attn == "fused":
+                h.append_decode_attn(layer, q, k, v, out, lse)
             else:
-                h.decode_attn(layer, q, out, lse)
+                h.append_rope(layer, k, v)
+                if attn == "static":
+                    rkv.rkv_decode_attn_static(h.handle, layer, q, out, lse)
+                else:
+                    h.decode_attn(layer, q, out, lse)
             record(active, n_old, layer, out, lse)
 
     # initial fill (ragged), one extra step at a time for the streams still short of it
@@ -126,19 +132,30 @@ def run_gpu(wl: synth.Workload, n_ticks: int, want: set, streams_of_interest=Non
     return run
 
 
-def oracle_step(wl: synth.Workload, stream: int, layer: int, n_old: int):
-    """Oracle outputs of one stream-layer-step, from regenerated inputs."""
+def evicted_after(wl: synth.Workload, stream: int, n_new: int) -> int:
+    """Tokens out of the window once the stream holds n_new tokens (the oracle's ring model)."""
+    w = int(wl.windows()[stream])
+    ring = StreamRing(w, 0, wl.q_per_step, capacity=w + wl.window_slack)
+    while ring.n < n_new:
+        ring.step()
+    return ring.evicted
+
+
+def oracle_step(wl: synth.Workload, stream: int, layer: int, n_old: int, p0: int | None = None):
+    """Oracle outputs of one stream-layer-step, from regenerated inputs (p0: the stream's start
+    offset, by default the workload's)."""
     Q, hq, hkv, d = wl.q_per_step, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
     w = int(wl.windows()[stream])
-    p0 = int(wl.start_offsets()[stream])
+    p0 = int(wl.start_offsets()[stream]) if p0 is None else int(p0)
     n_new = n_old + Q
-    toks = np.arange(max(0, n_new - w), n_new)
+    first = evicted_after(wl, stream, n_new) if wl.window_slack else None
+    toks = np.arange(max(0, n_new - w) if first is None else first, n_new)
     sc = wl.input_scale
     qb = synth.token_tensor(wl.seed, synth.TAG_Q, stream, layer, np.arange(n_old, n_new), hq, d, sc)
     kb = synth.token_tensor(wl.seed, synth.TAG_K, stream, layer, toks, hkv, d, sc)
     vb = synth.token_tensor(wl.seed, synth.TAG_V, stream, layer, toks, hkv, d, sc)
     return attention_step(synth.bf16_bits_to_f64(qb), synth.bf16_bits_to_f64(kb), synth.bf16_bits_to_f64(vb),
-                          toks, n_old, p0, w, 1.0 / math.sqrt(d), wl.rope_theta)
+                          toks, n_old, p0, w, 1.0 / math.sqrt(d), wl.rope_theta, first_key=first)
 
 
 def compare(run: Run, wl: synth.Workload):

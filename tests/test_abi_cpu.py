@@ -72,7 +72,7 @@ def test_required_bytes_closed_form():
                                  dict(n_q_heads=15), dict(head_dim=96), dict(q_per_step=0),
                                  dict(q_per_step=9), dict(n_q_heads=32, n_kv_heads=1), dict(page_size=48),
                                  dict(scheme=3), dict(rebase_interval=0), dict(rope_theta=1.0),
-                                 dict(reserved=1), dict(softmax_scale=-1.0)])
+                                 dict(window_slack=-1), dict(softmax_scale=-1.0)])
 def test_invalid_configs(bad):
     cfg = _cfg(**bad)
     with pytest.raises(rkv.RkvError) as e:
@@ -110,16 +110,17 @@ def test_null_handle_is_rejected():
         assert e.value.code == rkv.RKV_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("scheme,interval,q", [(0, 1, 1), (1, 1, 1), (1, 5, 1), (2, 3, 1), (0, 1, 4)])
-def test_stream_state_check(scheme, interval, q):
+@pytest.mark.parametrize("scheme,interval,q,slack", [(0, 1, 1, 0), (1, 1, 1, 0), (1, 5, 1, 0), (2, 3, 1, 0),
+                                                     (0, 1, 4, 0), (1, 1, 1, 5), (2, 2, 4, 9), (0, 1, 4, 12)])
+def test_stream_state_check(scheme, interval, q, slack):
     """States the integer ring model reaches are accepted; one field off by one is rejected."""
     from oracle.ring import StreamRing
     cfg = _cfg(n_streams=1, scheme=scheme, rebase_interval=interval, q_per_step=q,
-               n_q_heads=4 if q > 1 else 16, n_kv_heads=4 if q > 1 else 2)
+               n_q_heads=4 if q > 1 else 16, n_kv_heads=4 if q > 1 else 2, window_slack=slack)
     w, p0 = 12, 2 ** 40 + 3
-    ring = StreamRing(w, p0, q, 1 if scheme else 0, interval)
+    ring = StreamRing(w, p0, q, 1 if scheme else 0, interval, capacity=w + slack)
     checked = 0
-    for _ in range(40):
+    for _ in range(60):
         st = ring.state()
         rkv.rkv_check_stream_state(cfg, st)
         for i in range(len(st)):
@@ -128,14 +129,15 @@ def test_stream_state_check(scheme, interval, q):
                 bad[i] += dlt
                 if i == 4 and scheme and 0 <= bad[4] <= bad[2] and bad[2] - bad[4] < interval:
                     continue        # rope_base has slack of its own between re-bases
-                if i == 6 and st[0] <= w:
-                    continue        # before the window fills, W is fixed only by the stream's pages
+                if i == 6 and (st[0] <= w or slack):
+                    continue        # W is fixed by the stream's pages (rkv_load_stream checks it); the
+                    #                 state pins it only for a full plain sliding window
                 with pytest.raises(rkv.RkvError) as e:
                     rkv.rkv_check_stream_state(cfg, bad)
                 assert e.value.code == rkv.RKV_ERR_CONFIG
                 checked += 1
         ring.step()
-    assert checked > 400
+    assert checked > 600
     for bad in ([0, 0, 0, -1, 0, 0, w, -1], [0, 0, 0, 2 ** 52, 0, 0, w, 2 ** 52]):   # P0 outside [0, 2^52)
         with pytest.raises(rkv.RkvError):
             rkv.rkv_check_stream_state(cfg, bad)

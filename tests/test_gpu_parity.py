@@ -57,6 +57,37 @@ SMALL = {
     # head_dim 64 with GQA, one query per step
     "d64_gqa4": ("tiny", dict(n_layers=1, n_streams=2, n_q_heads=8, n_kv_heads=2, head_dim=64,
                               extra={"window": 150}), 190),
+    # append fused into the attention launch (rkv_append_decode_attn): every scheme, the 4-query
+    # step whose new tokens straddle stages and wrap the ring, small pages, mixed clocks
+    "tiny_exact_fused": ("tiny", dict(n_layers=2, n_streams=3, extra={"window": 150}), 190, "fused"),
+    "tiny_offset_fused": ("tiny", dict(n_layers=1, n_streams=3, extra={"window": 150}, scheme=0,
+                                       p0_high=2 ** 41), 190, "fused"),
+    "qwen_on_read_fused": ("qwen", dict(n_layers=2, n_streams=3, extra={"window": 100}, scheme=2), 120,
+                           "fused"),
+    "encoder_q4_fused": ("encoder", dict(n_layers=1, n_streams=3, extra={"window": 70}), 30, "fused"),
+    "encoder_q4_on_read_fused": ("encoder", dict(n_layers=1, n_streams=2, extra={"window": 66}, scheme=2), 40,
+                                 "fused"),
+    "tiny_page16_fused": ("tiny", dict(n_layers=1, n_streams=2, extra={"window": 150, "page_size": 16}), 190,
+                          "fused"),
+    "mixed_small_fused": ("mixed", dict(n_layers=1, n_streams=9, extra={}, scheme=2), 60, "fused"),
+    "gqa16_fused": ("tiny", dict(n_layers=1, n_streams=2, n_q_heads=16, n_kv_heads=1, extra={"window": 150}),
+                    190, "fused"),
+    "tiny_w1_fused": ("tiny", dict(n_layers=1, n_streams=2, extra={"window": 1}), 20, "fused"),
+    # eviction in batches: a ring of capacity W + slack, cut back to the last W when a step would
+    # overflow it, so the window length varies in [W, C] (every scheme; C = W + 8 and C = 2W)
+    "tiny_exact_slack8": ("tiny", dict(n_layers=2, n_streams=3, extra={"window": 150}, window_slack=8), 200),
+    "tiny_exact_slack_2w": ("tiny", dict(n_layers=1, n_streams=2, extra={"window": 150}, window_slack=150), 420),
+    "tiny_on_read_slack_2w_fused": ("tiny", dict(n_layers=1, n_streams=2, extra={"window": 150}, scheme=2,
+                                                 window_slack=150), 420, "fused"),
+    "tiny_offset_slack8_fused": ("tiny", dict(n_layers=1, n_streams=3, extra={"window": 150}, scheme=0,
+                                              window_slack=8, p0_high=2 ** 41), 200, "fused"),
+    "encoder_q4_slack8": ("encoder", dict(n_layers=1, n_streams=2, extra={"window": 70}, window_slack=8), 45),
+    "encoder_q4_on_read_slack_2w": ("encoder", dict(n_layers=1, n_streams=2, extra={"window": 70}, scheme=2,
+                                                    window_slack=70), 60),
+    "qwen_whole_step_slack": ("qwen", dict(n_layers=3, n_streams=3, extra={"window": 100}, window_slack=40),
+                              200, True),
+    "mixed_small_slack_on_read": ("mixed", dict(n_layers=1, n_streams=9, extra={}, scheme=2, window_slack=20),
+                                  120, "fused"),
 }
 
 
@@ -74,7 +105,8 @@ def test_small_every_output(case):
         for layer in range(wl.n_layers):
             for n_old in range(int(fill[s]) * wl.q_per_step, int(counts[s]) * wl.q_per_step, wl.q_per_step):
                 want.add((s, layer, n_old))
-    run = run_gpu(wl, ticks, want, whole_step=bool(opt and opt[0]))
+    mode = opt[0] if opt else False
+    run = run_gpu(wl, ticks, want, whole_step=mode is True, attn=mode if isinstance(mode, str) else "regular")
     assert len(run.samples) == len(want)
     e_o, e_l = compare(run, wl)
     print(case, "max out err", e_o, "max lse err", e_l)

@@ -13,6 +13,10 @@ pytestmark = pytest.mark.gpu
     ("tiny", dict(extra={"window": 5}, rebase_interval=3)),
     ("encoder", dict(n_layers=1, n_streams=3, extra={"window": 10})),
     ("mixed", dict(n_layers=1, n_streams=12)),
+    # eviction in batches (ring capacity above the window)
+    ("tiny", dict(extra={"window": 7}, window_slack=5)),
+    ("encoder", dict(n_layers=1, n_streams=3, extra={"window": 10}, window_slack=10)),
+    ("mixed", dict(n_layers=1, n_streams=12, window_slack=3, scheme=2)),
 ])
 def test_state_bit_exact(name, overrides):
     wl = synth.workload(name, **overrides)

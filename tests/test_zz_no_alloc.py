@@ -18,9 +18,16 @@ pytestmark = pytest.mark.gpu
 
 
 def _close_to_rounding(a_out, a_lse, b_out, b_lse):
-    """Outputs within one bf16 rounding step of each other, logsumexps within fp32 merge noise."""
+    """Outputs within one bf16 rounding step of each other plus 1e-4, logsumexps within 1e-5.
+
+    With the same split plan the two calls differ only in the fp32 order of the merge.  With
+    different plans (a long window: 8 splits in a cluster against 32 with the merge kernel) each
+    split also rounds its softmax weights to bf16 against its own running maximum, so the
+    weights differ by up to 2^-9 relative; over the 2000 keys of a window that moves an output of
+    unit-scale values by a few 1e-5 at most (3.1e-5 measured on the B300).
+    """
     a, b = a_out.float(), b_out.float()
-    bound = a.abs().maximum(b.abs()) * 2.0 ** -7 + 1e-6
+    bound = a.abs().maximum(b.abs()) * 2.0 ** -7 + 1e-4
     assert ((a - b).abs() <= bound).all(), (a - b).abs().max().item()
     e_l = ((a_lse - b_lse).abs() / b_lse.abs().clamp(min=1.0)).max().item()
     assert e_l <= 1e-5, e_l
