@@ -30,8 +30,8 @@
 // slots at or above evicted mod C it is rotated to j_q - C * floor(evicted /
 // C), for the slots below (tokens of the ring's next lap) C less, so every
 // score sees the exact position difference of its tokens.  The second query
-// is R(-C) applied to the first, in the registers of the MMA fragments
-// (lap_shift).
+// is R(-C) applied to the first, built once per unit in shared memory
+// (build_next_lap).
 //
 // Splits of one (layer, stream, kv head) form a thread-block cluster and
 // combine their (m, l, O) through distributed shared memory; the scratch
@@ -272,56 +272,35 @@ __device__ __forceinline__ void q_build(const QPrefetch<D>& pf, float scale_log2
 
 // ---------------- exact re-base applied on read: the query of the ring's next lap
 //
-// The query fragments of one k-step hold, per thread, elements 16 ks + 2 tq
-// (+1) and 16 ks + 2 tq + 8 (+1) of query row g; element i < d/2 and its RoPE
-// partner i + d/2 sit in k-steps ks and ks + KSTEPS/2 at the same register,
-// so R(-C) applies to the fragments in place.  Each element is rebuilt in
-// fp32 from its hi + lo parts, rotated with (cos, sin)(-C omega_i), and split
-// into fp16 hi + lo again (a relative error of a few 2^-24, far below the
-// fp16 rounding of the stored key).
+// Built once per unit by the four consumer warps together, from the current lap's tiles: every
+// element pair (i, i + d/2) of every query row is rebuilt in fp32 from its hi + lo parts, rotated
+// with (cos, sin)(-C omega_i) and split into fp16 hi + lo again (a relative error of a few 2^-24,
+// far below the fp16 rounding of a stored key).  Two adjacent frequencies per item.
 template <int D, int NT>
-__device__ __forceinline__ void lap_shift(uint32_t (&qh)[NT][D / 16][2], uint32_t (&ql)[NT][D / 16][2],
-                                          const float* lap, int tq) {
-  constexpr int HK = D / 32;  // k-steps of the first half of the row
-#pragma unroll
-  for (int ks = 0; ks < HK; ++ks)
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      // (cos, sin) of frequencies i, i + 1 with i = 16 ks + 2 tq + 8 r
-      const float4 cs = reinterpret_cast<const float4*>(lap)[(16 * ks + 2 * tq + 8 * r) / 2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const float2 ah = __half22float2(*reinterpret_cast<const __half2*>(&qh[nt][ks][r]));
-        const float2 al = __half22float2(*reinterpret_cast<const __half2*>(&ql[nt][ks][r]));
-        const float2 bh = __half22float2(*reinterpret_cast<const __half2*>(&qh[nt][ks + HK][r]));
-        const float2 bl = __half22float2(*reinterpret_cast<const __half2*>(&ql[nt][ks + HK][r]));
-        const float a0 = ah.x + al.x, a1 = ah.y + al.y, b0 = bh.x + bl.x, b1 = bh.y + bl.y;
-        const float ra0 = a0 * cs.x - b0 * cs.y, rb0 = a0 * cs.y + b0 * cs.x;
-        const float ra1 = a1 * cs.z - b1 * cs.w, rb1 = a1 * cs.w + b1 * cs.z;
-        const __half2 ha = __floats2half2_rn(ra0, ra1), hb = __floats2half2_rn(rb0, rb1);
-        const float2 fa = __half22float2(ha), fb = __half22float2(hb);
-        qh[nt][ks][r] = *reinterpret_cast<const uint32_t*>(&ha);
-        qh[nt][ks + HK][r] = *reinterpret_cast<const uint32_t*>(&hb);
-        ql[nt][ks][r] = pack_f16(ra0 - fa.x, ra1 - fa.y);
-        ql[nt][ks + HK][r] = pack_f16(rb0 - fb.x, rb1 - fb.y);
-      }
-    }
+__device__ __forceinline__ void build_next_lap(const uint16_t* qh_s, const uint16_t* ql_s, uint16_t* bh_s,
+                                               uint16_t* bl_s, const float* lap, int tid) {
+  constexpr int QSTR = D + 8, H = D / 2, ITEMS = 8 * NT * (D / 4);
+  for (int it = tid; it < ITEMS; it += kCW * 32) {
+    const int r = it / (D / 4), i = (it % (D / 4)) * 2;
+    const int oa = r * QSTR + i, ob = oa + H;
+    const float2 ah = __half22float2(*reinterpret_cast<const __half2*>(qh_s + oa));
+    const float2 al = __half22float2(*reinterpret_cast<const __half2*>(ql_s + oa));
+    const float2 bh = __half22float2(*reinterpret_cast<const __half2*>(qh_s + ob));
+    const float2 bl = __half22float2(*reinterpret_cast<const __half2*>(ql_s + ob));
+    const float4 cs = *reinterpret_cast<const float4*>(lap + 2 * i);  // (cos, sin) of i, i + 1
+    const float a0 = ah.x + al.x, a1 = ah.y + al.y, b0 = bh.x + bl.x, b1 = bh.y + bl.y;
+    const float ra0 = a0 * cs.x - b0 * cs.y, rb0 = a0 * cs.y + b0 * cs.x;
+    const float ra1 = a1 * cs.z - b1 * cs.w, rb1 = a1 * cs.w + b1 * cs.z;
+    const __half2 ha = __floats2half2_rn(ra0, ra1), hb = __floats2half2_rn(rb0, rb1);
+    const float2 fa = __half22float2(ha), fb = __half22float2(hb);
+    *reinterpret_cast<__half2*>(bh_s + oa) = ha;
+    *reinterpret_cast<__half2*>(bh_s + ob) = hb;
+    *reinterpret_cast<uint32_t*>(bl_s + oa) = pack_f16(ra0 - fa.x, ra1 - fa.y);
+    *reinterpret_cast<uint32_t*>(bl_s + ob) = pack_f16(rb0 - fb.x, rb1 - fb.y);
+  }
 }
 
-// The order a CTA walks its stages st0 .. st1-1: starting after the stage of the stream's newest
-// ring slot, so that the stage holding the step's new tokens comes last (the producer writes
-// them into the pool just before copying that stage, while the earlier stages stream).
-__device__ __forceinline__ int stage_rot(const StepDesc& d, int nq, int st0, int cnt) {
-  const int newest = static_cast<int>((d.n_old + nq - 1) % d.ring);
-  const int rel = newest / 64 - st0;
-  return rel >= 0 && rel < cnt ? rel + 1 : 0;
-}
-__device__ __forceinline__ int stage_at(int i, int st0, int cnt, int rot) {
-  const int j = i + rot;
-  return st0 + (j >= cnt ? j - cnt : j);
-}
-
-// Fused append (rkv_append_decode_attn, rkv_step): the step's new tokens of (layer, stream, kv
+// Fused append (rkv_append_decode_attn): the step's new tokens of (layer, stream, kv
 // head) that fall in stage `st` are written by the producer warp, as rkv_append_rope would write
 // them (key rotated by its cos/sin row and rounded to fp16, the pre-RoPE key for the materialised
 // re-base, the value as given): into the pool for the steps to come and, unless `kstage` is NULL,
@@ -337,8 +316,35 @@ __device__ __forceinline__ uint64_t new_rows(const StepDesc& dsc, int nq, int st
   return m;
 }
 
+// Pull this lane's inputs of write_new for the unit's new tokens in stages [st0, st0 + cnt) into
+// L1 at the start of the unit, so that write_new (late in the unit's walk) finds them there.
 template <int D>
-__device__ __noinline__ void write_new(const AttnArgs& args, const StepDesc& dsc, const Unit& un, int st,
+__device__ __forceinline__ void prefetch_new(const AttnArgs& args, const StepDesc& dsc, const Unit& un, int st0,
+                                             int cnt, int lane) {
+  const DevView& v = args.v;
+  const int nq = v.q_per_step;
+  constexpr int CP = D / 16, H = D / 2;
+  for (int t = 0; t < nq; ++t) {
+    const int st = static_cast<int>((dsc.n_old + t) % dsc.ring) / 64;
+    if (st < st0 || st >= st0 + cnt) continue;
+    const int64_t row = static_cast<int64_t>(un.a) * nq + t;
+    const int64_t src = un.lz * args.kv_layer_stride + (row * v.n_kv_heads + un.kvh) * D;
+    const void* p0 = nullptr;
+    const void* p1 = nullptr;
+    if (lane < CP) {
+      p0 = args.k_new + src + lane * 8;
+      p1 = v.cs_new + (row * H + lane * 8) * 2;
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(args.k_new + src + H + lane * 8));
+    } else if (lane < CP + D / 8) {
+      p0 = args.v_new + src + (lane - CP) * 8;
+    }
+    if (p0) asm volatile("prefetch.global.L1 [%0];" ::"l"(p0));
+    if (p1) asm volatile("prefetch.global.L1 [%0];" ::"l"(p1));
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void write_new(const AttnArgs& args, const StepDesc& dsc, const Unit& un, int st,
                                        uint16_t* kstage, int lane) {
   const DevView& v = args.v;
   const int nq = v.q_per_step, hkv = v.n_kv_heads, ps = v.page_size;
@@ -486,12 +492,12 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
         const int n_st = (slots_in_use(dsc) + kKS - 1) / kKS;
         const int st0 = split * args.stages_per_split;
         const int cnt = max(0, min(st0 + args.stages_per_split, n_st) - st0);
-        const int rot = stage_rot(dsc, v.q_per_step, st0, cnt);
+        if (FUSE && !stop) prefetch_new<D>(args, dsc, un, st0, cnt, lane);
         const int stream_pages = (dsc.ring + ps - 1) / ps;
         const int32_t* ptab = v.page_table + static_cast<int64_t>(dsc.stream) * v.max_pages;
         int pbase = -64, pt_lane = 0;
         for (int i = 0; i < cnt; ++i, ++k) {
-          const int st = stage_at(i, st0, cnt, rot);
+          const int st = st0 + i;
           const int buf = k % kStages;
           if (!stop && k >= kStages &&
               !__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty_bar[buf]), ((k / kStages) - 1) & 1, v.wait_ns))) {
@@ -594,31 +600,38 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
       const int n_st = (nslots + kKS - 1) / kKS;
       const int st0 = split * args.stages_per_split;
       const int my_st = max(0, min(st0 + args.stages_per_split, n_st) - st0);
-      const int rot = stage_rot(dsc, nq, st0, my_st);
 
       q_build<D, NT>(pf, v.scale_log2, tid, qh_s, ql_s);
       if constexpr (ON_READ) {
         if (tid < D) lap_s[tid] = pf.lap;
       }
       consumer_sync();  // S1: query tiles ready; the previous unit's output pass is over
+      // on read: the next lap's query tiles (R(-C) applied), for the ring slots below evicted mod
+      // C, in the output tiles' space (free until this unit's epilogue)
+      uint16_t* const nh_s = reinterpret_cast<uint16_t*>(obuf);
+      uint16_t* const nl_s = nh_s + ROWS * QSTR;
+      if constexpr (ON_READ) {
+        if (dsc.evicted % W != 0) {  // uniform: some retained tokens are on the next lap
+          build_next_lap<D, NT>(qh_s, ql_s, nh_s, nl_s, lap_s, tid);
+          consumer_sync();  // S1b
+        }
+      }
       uint32_t qh[NT][KSTEPS][2], ql[NT][KSTEPS][2];
-      auto load_q = [&]() {  // the query fragments (B operand) from the tiles
+      auto load_q = [&](const uint16_t* th, const uint16_t* tl) {  // query fragments (B operand)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int ks = 0; ks < KSTEPS; ++ks) {
             const int base = (nt * 8 + g) * QSTR + ks * 16 + 2 * tq;
-            qh[nt][ks][0] = *reinterpret_cast<const uint32_t*>(qh_s + base);
-            qh[nt][ks][1] = *reinterpret_cast<const uint32_t*>(qh_s + base + 8);
-            ql[nt][ks][0] = *reinterpret_cast<const uint32_t*>(ql_s + base);
-            ql[nt][ks][1] = *reinterpret_cast<const uint32_t*>(ql_s + base + 8);
+            qh[nt][ks][0] = *reinterpret_cast<const uint32_t*>(th + base);
+            qh[nt][ks][1] = *reinterpret_cast<const uint32_t*>(th + base + 8);
+            ql[nt][ks][0] = *reinterpret_cast<const uint32_t*>(tl + base);
+            ql[nt][ks][1] = *reinterpret_cast<const uint32_t*>(tl + base + 8);
           }
       };
-      load_q();
-      // on read: whether the fragments hold the next lap's query (R(-C) applied), for the ring
-      // slots below evicted mod C
+      load_q(qh_s, ql_s);
+      // on read: whether the fragments hold the next lap's query
       bool lap_b = false;
-      const float* lap = lap_s;
       if (u + u_step < n_units) {  // the next unit's query and descriptor land during this unit
         const Unit un1 = unit_of(u + u_step, n_active, hkv);
         q_prefetch<D>(args, un1, tid, pf);
@@ -653,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
           aborted = true;
           break;
         }
-        const int slot_base = stage_at(i, st0, my_st, rot) * kKS + wt * 16;
+        const int slot_base = (st0 + i) * kKS + wt * 16;
         const uint32_t kb = smem_u32(kv_s + buf * 2 * STAGE_ELEMS);
         const uint32_t vb = kb + STAGE_ELEMS * 2;
         if (slot_base >= nslots) {  // none of this warp's slots holds a token
@@ -691,11 +704,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
         if constexpr (ON_READ) {
           // warp-uniform: slots [slot_base, slot_base + 16) against ev_mod
           if (slot_base + 16 <= ev_mod) {         // all of the next lap
-            if (!lap_b) lap_shift<D, NT>(qh, ql, lap, tq);
+            if (!lap_b) load_q(nh_s, nl_s);
             lap_b = true;
             qk(sh, sl);
           } else if (slot_base >= ev_mod) {       // all of the current lap
-            if (lap_b) load_q();
+            if (lap_b) load_q(qh_s, ql_s);
             lap_b = false;
             qk(sh, sl);
           } else {                                // the chunk where the two laps meet
@@ -704,9 +717,9 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
               for (int e = 0; e < 4; ++e) bh[nt][e] = bl[nt][e] = 0.f;
-            if (!lap_b) lap_shift<D, NT>(qh, ql, lap, tq);
+            if (!lap_b) load_q(nh_s, nl_s);
             qk(bh, bl);
-            load_q();
+            load_q(qh_s, ql_s);
             lap_b = false;
             qk(sh, sl);
 #pragma unroll
