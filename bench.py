@@ -43,8 +43,16 @@ SCHEMES = {"offset": 0, "exact": 1, "on-read": 2}
 # DRAM traffic (read + write bytes) of one all-layers decode-attention launch, from the committed
 # ncu launch-list summary of the same command, valid only while the attention source's code is the
 # one that was profiled: a different code digest (comments and white space left out) reports null.
-TRAFFIC = [{"workload": "qwen", "layers": 36, "schemes": (0, 1), "attn_code_sha256_16": "b402dd177090064a",
-            "bytes_per_launch": 915.6e6 + 9.0e6}]
+TRAFFIC = [
+    {"workload": "mixed", "layers": 36, "schemes": (0, 1), "attn_code_sha256_16": "803fd1b535bbdbb7",
+     "bytes_per_launch": 1131.05e6 + 13.91e6},   # the tick phase with the most active streams
+    {"workload": "qwen", "layers": 36, "schemes": (0, 1), "attn_code_sha256_16": "803fd1b535bbdbb7",
+     "bytes_per_launch": 915.62e6 + 8.76e6},
+    {"workload": "qwen", "layers": 36, "schemes": (2,), "attn_code_sha256_16": "803fd1b535bbdbb7",
+     "bytes_per_launch": 915.69e6 + 8.89e6},
+    {"workload": "voxtral", "layers": 26, "schemes": (0,), "attn_code_sha256_16": "803fd1b535bbdbb7",
+     "bytes_per_launch": 13962.79e6 + 4.40e6},
+]
 SCHEME_NAMES = {0: "offset-only", 1: "exact re-base", 2: "exact re-base applied on read"}
 
 
@@ -480,49 +488,60 @@ def measure(wl, args, dev, rank, world, timed=True, p0=None, attention=True, per
                free_bytes_delta=torch.cuda.mem_get_info(dev)[0] - free_before)
 
     if per_layer_step:
-        def layer_calls(act, b):
+        def layer_calls(act, b, fused):
             A = len(act)
             h.begin_step(act)
             for layer in range(L):
                 if wl.scheme in (1, 2):
                     h.rebase(layer)
-                h.append_decode_attn(layer, b["q"][layer * A * Q * hq * d:], b["k"][layer * A * Q * hkv * d:],
-                                     b["v"][layer * A * Q * hkv * d:], b["out"][layer * A * Q * hq * d:],
-                                     b["lse"][layer * A * Q * hq:])
-        lgraphs = []
-        with torch.cuda.stream(stream):
-            for r, act in enumerate(plan):
-                if act:
-                    layer_calls(act, sets[r])
-            stream.synchronize()
-            for r, act in enumerate(plan):
-                if not act:
-                    lgraphs.append(None)
-                    continue
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    layer_calls(act, sets[r])
-                lgraphs.append(g)
-        for i in range(args.warmup + R):
-            if lgraphs[i % R] is not None:
-                lgraphs[i % R].replay()
-        barrier()
-        ev0.record(cur)
-        for i in range(args.steps):
-            if lgraphs[i % R] is not None:
-                lgraphs[i % R].replay()
-        ev1.record(cur)
-        torch.cuda.synchronize()
-        lms = ev0.elapsed_time(ev1)
-        h.sync_status()
-        ljob = aggregate(lms, sum(len(plan[i % R]) for i in range(args.steps)), world, dev)
-        per_step_launches = 1 + L * (1 + (1 if wl.scheme == 1 else 0))
-        out["per_layer_step"] = {
-            "value": ljob["value"], "unit": UNIT, "ms_per_step": ljob["ms"] / args.steps,
-            "launches_per_step": per_step_launches,
-            "how": "the same steps as one CUDA graph of per-layer calls each: begin step, then for every layer "
-                   "re-base (materialised exact re-base) and decode attention with the append fused "
-                   "(rkv_append_decode_attn)"}
+                ql, kl, vl = b["q"][layer * A * Q * hq * d:], b["k"][layer * A * Q * hkv * d:], \
+                    b["v"][layer * A * Q * hkv * d:]
+                ol, ll = b["out"][layer * A * Q * hq * d:], b["lse"][layer * A * Q * hq:]
+                if fused:
+                    h.append_decode_attn(layer, ql, kl, vl, ol, ll)
+                else:
+                    h.append_rope(layer, kl, vl)
+                    h.decode_attn(layer, ql, ol, ll)
+
+        for fused in (False, True):
+            lgraphs = []
+            with torch.cuda.stream(stream):
+                for r, act in enumerate(plan):
+                    if act:
+                        layer_calls(act, sets[r], fused)
+                stream.synchronize()
+                for r, act in enumerate(plan):
+                    if not act:
+                        lgraphs.append(None)
+                        continue
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=stream):
+                        layer_calls(act, sets[r], fused)
+                    lgraphs.append(g)
+            for i in range(args.warmup + R):
+                if lgraphs[i % R] is not None:
+                    lgraphs[i % R].replay()
+            barrier()
+            ev0.record(cur)
+            for i in range(args.steps):
+                if lgraphs[i % R] is not None:
+                    lgraphs[i % R].replay()
+            ev1.record(cur)
+            torch.cuda.synchronize()
+            lms = ev0.elapsed_time(ev1)
+            h.sync_status()
+            ljob = aggregate(lms, sum(len(plan[i % R]) for i in range(args.steps)), world, dev)
+            rec = {"value": ljob["value"], "unit": UNIT, "ms_per_step": ljob["ms"] / args.steps,
+                   "launches_per_step": 1 + L * ((1 if fused else 2) + (1 if wl.scheme == 1 else 0))}
+            if fused:
+                rec["how"] = ("the same per-layer calls with RoPE + append fused into the decode-attention "
+                              "launch (rkv_append_decode_attn)")
+                out["per_layer_step"]["fused_append"] = rec
+            else:
+                rec["how"] = ("the same steps as one CUDA graph of per-layer calls each: begin step, then for "
+                              "every layer re-base (materialised exact re-base), RoPE + append and decode "
+                              "attention, as a model that runs other work between its layers calls them")
+                out["per_layer_step"] = rec
     if not attention:
         return out
 
