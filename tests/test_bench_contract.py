@@ -100,6 +100,19 @@ def test_reference_arm_prints_one_line():
     assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "stream-steps/s"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
     # the same workload description as the GPU arm's line, and a per-step time of the steps it ran
-    wl = synth.workload("tiny")
+    import argparse
+    wl, _ = bench.bench_workload(argparse.Namespace(workload="tiny", scheme=None, layers=None))
+    assert wl.scheme == 2        # an exact re-base workload is run with the re-base applied on read
     assert line["config"]["workload"] == bench.describe(wl, bench.SCHEME_NAMES[wl.scheme])
     assert 0 < line["ms_per_step"] * line["steps"] < 600e3
+
+
+def test_rebase_share_with_the_re_base_applied_on_read_as_headline():
+    # the headline runs the re-base on read; the materialised scheme's step comes from `schemes`
+    wl = synth.workload("qwen", scheme=2)
+    m = _fake_measurement(wl, 100, 0.160, 145.0)
+    m["plan"] = [list(range(wl.n_streams))]
+    variants = {"offset-only": {"ms_per_step": 0.154}, "exact re-base": {"ms_per_step": 0.336}}
+    rb = bench.rebase_in_step(wl, m, variants, 100, 6492.7)
+    assert rb["us_per_step"] == pytest.approx(182.0)
+    assert bench.rebase_in_step(wl, m, {"offset-only": {"ms_per_step": 0.154}}, 100, 6492.7) is None
