@@ -50,8 +50,12 @@ TRAFFIC = [
      "bytes_per_launch": 915.62e6 + 8.76e6},
     {"workload": "qwen", "layers": 36, "schemes": (2,), "attn_code_sha256_16": "803fd1b535bbdbb7",
      "bytes_per_launch": 915.69e6 + 8.89e6},
+    {"workload": "mixed", "layers": 36, "schemes": (2,), "attn_code_sha256_16": "803fd1b535bbdbb7",
+     "bytes_per_launch": 1131.23e6 + 13.56e6},   # the tick phase with the most active streams
     {"workload": "voxtral", "layers": 26, "schemes": (0,), "attn_code_sha256_16": "803fd1b535bbdbb7",
      "bytes_per_launch": 13962.79e6 + 4.40e6},
+    {"workload": "encoder", "layers": 32, "schemes": (0,), "attn_code_sha256_16": "803fd1b535bbdbb7",
+     "bytes_per_launch": 4038.26e6 + 10.55e6},
 ]
 SCHEME_NAMES = {0: "offset-only", 1: "exact re-base", 2: "exact re-base applied on read"}
 
@@ -727,7 +731,8 @@ def run_ours(args):
                 "value": cm["value"], "unit": UNIT, "ms_per_step": cm["ms"] / args.steps,
                 "how": "each tick first runs rkv_reset_streams over the next row of a device-side schedule "
                        "(walked by the replayed graphs with a device counter); every 12th row resets one "
-                       "slot to a new start offset, the others list no slot"}
+                       "slot to a new start offset, the others list no slot; a joining stream's window "
+                       "starts empty and refills over its next W steps, so the tick moves fewer bytes"}
 
     def flatness(fw, free_delta):
         # cost per step must not depend on how far the streams are into their logical timelines
