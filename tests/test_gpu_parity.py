@@ -139,6 +139,10 @@ FULL = {
     # mixed clocks: windows of 375 / 250 / 188 filled from ragged starts, then two 12-tick schedule
     # periods more; one stream of each clock and one more 80 ms stream
     "mixed_step": ("mixed", dict(), 510, "schedule", [0, 1, 2, 3], True),
+    # the benchmark's headline: the same ticks with the exact re-base applied on read
+    "mixed_step_on_read": ("mixed", dict(scheme=2), 510, "schedule", [0, 1, 2, 3, 4], True),
+    # the per-layer calls over keys stored at their ring slot
+    "qwen_on_read": ("qwen", dict(scheme=2), 1000, [0, 374, 375, 376, 999], [0, 40, 63]),
     "encoder_step": ("encoder", dict(), 200, [0, 4, 744, 748, 752, 796], [0, 31], True),
 }
 
