@@ -97,6 +97,9 @@ def parse_args():
                    help="skip the Qwen- and voxtral-shaped sub-records of the default run")
     p.add_argument("--no-per-layer", dest="per_layer", action="store_false",
                    help="skip the step made of per-layer calls")
+    p.add_argument("--window-scan", action="store_true",
+                   help="time one-layer decode-attention launches against the window length (Qwen-shaped "
+                        "heads, 64 streams) and print that scan instead of the benchmark line")
     return p.parse_args()
 
 
@@ -843,9 +846,68 @@ def measure_e2e(h, wl, plan, args, dev):
                     "others, overlapping neighbouring steps (double-buffered)"}
 
 
+def window_scan(args):
+    """Per-layer decode-attention launch time against the window length: the intercept of a line
+    through the points is the fixed cost of one launch, the slope the streaming bandwidth."""
+    import torch
+
+    import rolling_kv_sliding_rkv_b300 as rkv
+    dev = torch.device("cuda")
+    S, L, hq, hkv, d = 64, 36, 16, 2, 128
+    points = []
+    for W in (64, 128, 192, 256, 384, 512, 768):
+        h = rkv.RollingKV([W] * S, [0] * S, device=dev, n_layers=L, n_streams=S, n_q_heads=hq, n_kv_heads=hkv,
+                          head_dim=d, q_per_step=1, scheme=0, rope_theta=1e6)
+        act = list(range(S))
+        q = torch.randn(L * S * hq * d, device=dev).mul(0.088).to(torch.bfloat16)
+        k = torch.randn(L * S * hkv * d, device=dev).mul(0.088).to(torch.bfloat16)
+        v = torch.randn(L * S * hkv * d, device=dev).mul(0.088).to(torch.bfloat16)
+        out = torch.empty_like(q)
+        lse = torch.empty(L * S * hq, device=dev)
+        for _ in range(W + 3):
+            h.step(act, q, k, v, out, lse)
+        h.begin_step(act)
+        for layer in range(L):
+            h.append_rope(layer, k[layer * S * hkv * d:], v[layer * S * hkv * d:])
+
+        def body():
+            for layer in range(L):
+                h.decode_attn(layer, q[layer * S * hq * d:], out[layer * S * hq * d:], lse[layer * S * hq:])
+        st = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(st):
+            body()
+            st.synchronize()
+            with torch.cuda.graph(g, stream=st):
+                body()
+        for _ in range(5):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(max(5, args.steps)):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / max(5, args.steps) / L * 1000.0
+        nbytes = S * (2 * W * hkv * d * 2 + hq * d * 2 * 2 + hq * 4)
+        points.append({"window": W, "bytes_per_launch": nbytes, "us_per_launch": us})
+        h.sync_status()
+        h.close()
+    xs = [p["bytes_per_launch"] for p in points]
+    ys = [p["us_per_launch"] for p in points]
+    mx, my = sum(xs) / len(xs), sum(ys) / len(ys)
+    slope = sum((x - mx) * (y - my) for x, y in zip(xs, ys)) / sum((x - mx) ** 2 for x in xs)
+    print(json.dumps({"scan": "one-layer decode attention launch against the window length",
+                      "points": points, "fixed_us_per_launch": my - slope * mx,
+                      "streaming_gbs": 1e-3 / slope}), flush=True)
+
+
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.window_scan:
+        window_scan(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
