@@ -869,6 +869,7 @@ def window_scan(args):
         h.begin_step(act)
         for layer in range(L):
             h.append_rope(layer, k[layer * S * hkv * d:], v[layer * S * hkv * d:])
+        torch.cuda.synchronize()  # the capture stream does not wait for the default stream
 
         def body():
             for layer in range(L):

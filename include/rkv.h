@@ -218,10 +218,11 @@ RKV_API int rkv_rebase(rkv_handle* h, int32_t layer, void* stream);
 RKV_API int rkv_decode_attn(rkv_handle* h, int32_t layer, const rkv_bf16* q, rkv_bf16* out,
                             float* lse, void* stream);
 
-/* rkv_append_rope and rkv_decode_attn of one layer in one launch: the
- * attention kernel writes the step's new keys (rotated as rkv_append_rope
- * rotates them) and values into the pool itself, just before it streams
- * the ring stage that holds them, and attends over them in the same pass.
+/* rkv_append_rope and rkv_decode_attn of one layer in one launch: a warp of
+ * each attention CTA writes the step's new keys (rotated as rkv_append_rope
+ * rotates them) and values into the pool while the CTA streams the window's
+ * older ring stages; the stages that hold new tokens are streamed last,
+ * once those rows are written, and attended over in the same pass.
  * Arguments as the two calls take them (q [A][Q][Hq][d], k and v
  * [A][Q][Hkv][d], out, lse); results as rkv_append_rope followed by
  * rkv_decode_attn.  In the exact schemes rkv_rebase of the layer must come

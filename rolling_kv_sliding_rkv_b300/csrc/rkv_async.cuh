@@ -74,6 +74,37 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 // all committed bulk groups are complete (their global writes done)
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// make this thread's generic-proxy global writes visible to later bulk copies
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// a counter in shared memory published by one warp and read by another of the same CTA
+__device__ __forceinline__ void st_release_smem(int* p, int x) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))),
+               "r"(x)
+               : "memory");
+}
+__device__ __forceinline__ int ld_acquire_smem(const int* p) {
+  int x;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];"
+               : "=r"(x)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p)))
+               : "memory");
+  return x;
+}
+
+// Wait until the counter reaches `want`; false after limit_ns.
+__device__ __forceinline__ bool wait_count(const int* p, int want, unsigned long long limit_ns) {
+  if (ld_acquire_smem(p) >= want) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 32; ++i)
+      if (ld_acquire_smem(p) >= want) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // make this thread's generic-proxy shared-memory writes visible to bulk copies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

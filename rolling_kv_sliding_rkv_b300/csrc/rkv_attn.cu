@@ -50,6 +50,11 @@ namespace {
 
 constexpr int kCW = 4;                    // consumer warps: 16 slots of every stage each
 constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
+// threads of a CTA: with the append fused, a sixth warp writes the step's new tokens
+template <bool FUSE>
+__host__ __device__ constexpr int threads_of() {
+  return FUSE ? kThreads + 32 : kThreads;
+}
 static_assert(kCW == 4, "the epilogue sums warps 0 + 2 and 1 + 3");
 constexpr int kKS = 64;                   // ring slots per stage
 // shared-memory ring per CTA: 96 KB of K/V stages whatever the head dim
@@ -72,9 +77,9 @@ struct AttnArgs {
   // or more launches back), bit 1 the queries (written before the call, rkv_step).  A cleared bit
   // means the data may come from this launch's immediate predecessor and is read after the wait.
   int early;
-  // fused append (rkv_append_decode_attn, rkv_step): the step's new keys and values, pre-RoPE,
-  // [layer][A][Q][Hkv][d], written rotated into the pool by the producer before it copies their
-  // stage; NULL when rkv_append_rope did it
+  // fused append (rkv_append_decode_attn): the step's new keys and values, pre-RoPE,
+  // [layer][A][Q][Hkv][d], written rotated into the pool by the CTA's appender warp before the
+  // producer copies their stage; NULL when rkv_append_rope did it
   const uint16_t* k_new;
   const uint16_t* v_new;
   int64_t kv_layer_stride;
@@ -300,109 +305,82 @@ __device__ __forceinline__ void build_next_lap(const uint16_t* qh_s, const uint1
   }
 }
 
-// Fused append (rkv_append_decode_attn): the step's new tokens of (layer, stream, kv
-// head) that fall in stage `st` are written by the producer warp, as rkv_append_rope would write
-// them (key rotated by its cos/sin row and rounded to fp16, the pre-RoPE key for the materialised
-// re-base, the value as given): into the pool for the steps to come and, unless `kstage` is NULL,
-// into their rows of the stage's shared-memory buffer, which the stage's bulk copies then skip.
-// Lane c < D/16 rotates chunk pair (c, c + D/16) of a key, lanes D/16 .. D/16 + D/8 - 1 copy one
-// 16-byte chunk of a value.  Returns the rows written into the stage (bit r: row r).
-__device__ __forceinline__ uint64_t new_rows(const StepDesc& dsc, int nq, int st) {
-  uint64_t m = 0;
-  for (int t = 0; t < nq; ++t) {
-    const int slot = static_cast<int>((dsc.n_old + t) % dsc.ring);
-    if (slot / 64 == st) m |= uint64_t(1) << (slot % 64);
-  }
-  return m;
+// Fused append (rkv_append_decode_attn): a sixth warp of the CTA, the appender, writes the step's
+// new tokens of every (layer, stream, kv head) the CTA walks into the pool, as rkv_append_rope would
+// write them (key rotated by its cos/sin row and rounded to fp16, the pre-RoPE key for the
+// materialised re-base, the value as given), while the producer streams the window's older stages.
+// The walk of a unit then starts at the stage after the one holding its newest token, so that the
+// stages with new rows come last and their bulk copies, which wait for the appender, find its
+// rows written.  Position i of a unit's walk is stage (rot + i) mod n_st.
+// Ring slot of new token t, from the slot of the step's first (one 64-bit remainder per unit).
+__device__ __forceinline__ int first_new_slot(const StepDesc& dsc) { return static_cast<int>(dsc.n_old % dsc.ring); }
+__device__ __forceinline__ int new_slot(int first, int t, int ring) {
+  const int s = first + t;
+  return s >= ring ? s - ring : s;
 }
 
-// Pull this lane's inputs of write_new for the unit's new tokens in stages [st0, st0 + cnt) into
-// L1 at the start of the unit, so that write_new (late in the unit's walk) finds them there.
-template <int D>
-__device__ __forceinline__ void prefetch_new(const AttnArgs& args, const StepDesc& dsc, const Unit& un, int st0,
-                                             int cnt, int lane) {
-  const DevView& v = args.v;
-  const int nq = v.q_per_step;
-  constexpr int CP = D / 16, H = D / 2;
-  for (int t = 0; t < nq; ++t) {
-    const int st = static_cast<int>((dsc.n_old + t) % dsc.ring) / 64;
-    if (st < st0 || st >= st0 + cnt) continue;
-    const int64_t row = static_cast<int64_t>(un.a) * nq + t;
-    const int64_t src = un.lz * args.kv_layer_stride + (row * v.n_kv_heads + un.kvh) * D;
-    const void* p0 = nullptr;
-    const void* p1 = nullptr;
-    if (lane < CP) {
-      p0 = args.k_new + src + lane * 8;
-      p1 = v.cs_new + (row * H + lane * 8) * 2;
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(args.k_new + src + H + lane * 8));
-    } else if (lane < CP + D / 8) {
-      p0 = args.v_new + src + (lane - CP) * 8;
-    }
-    if (p0) asm volatile("prefetch.global.L1 [%0];" ::"l"(p0));
-    if (p1) asm volatile("prefetch.global.L1 [%0];" ::"l"(p1));
-  }
+__device__ __forceinline__ int walk_rot(int first, int nq, int ring, int n_st) {
+  if (n_st <= 0) return 0;
+  const int last = new_slot(first, nq - 1, ring) / kKS;
+  return last + 1 >= n_st ? 0 : last + 1;
 }
 
+__device__ __forceinline__ bool stage_has_new(int first, int nq, int ring, int st) {
+  for (int t = 0; t < nq; ++t)
+    if (new_slot(first, t, ring) / kKS == st) return true;
+  return false;
+}
+
+// New token t of the unit into the pool: lane c < D/16 rotates chunk pair (c, c + D/16) of its
+// key, lanes D/16 .. D/16 + D/8 - 1 copy one 16-byte chunk of its value.
 template <int D>
-__device__ __forceinline__ void write_new(const AttnArgs& args, const StepDesc& dsc, const Unit& un, int st,
-                                       uint16_t* kstage, int lane) {
+__device__ __forceinline__ void append_token(const AttnArgs& args, const StepDesc& dsc, const Unit& un, int t,
+                                             int slot, int lane) {
   const DevView& v = args.v;
   const int nq = v.q_per_step, hkv = v.n_kv_heads, ps = v.page_size;
   const int layer = args.layer0 + un.lz;
   constexpr int CP = D / 16, H = D / 2;
-  for (int t = 0; t < nq; ++t) {
-    const int slot = static_cast<int>((dsc.n_old + t) % dsc.ring);
-    if (slot / 64 != st) continue;
-    const int rp = slot / ps, off = slot % ps, r = slot % 64;  // r & 7 == off & 7: the same swizzle
-    const int page = rp < v.max_pages ? v.page_table[static_cast<int64_t>(dsc.stream) * v.max_pages + rp] : -1;
-    if (page < 0 || page >= v.n_pages) {
-      if (lane == 0) record_error(v.status, DEV_BOUNDS, 24, page);
-      continue;
-    }
-    const int64_t dst = pool_offset(v, layer, page, un.kvh, off);
-    const int64_t row = static_cast<int64_t>(un.a) * nq + t;
-    const int64_t src = un.lz * args.kv_layer_stride + (row * hkv + un.kvh) * D;
-    if (lane < CP) {
-      const int c = lane;
-      const uint4 ka = *reinterpret_cast<const uint4*>(args.k_new + src + c * 8);
-      const uint4 kb = *reinterpret_cast<const uint4*>(args.k_new + src + H + c * 8);
-      const float4* cs = reinterpret_cast<const float4*>(v.cs_new + (row * H + c * 8) * 2);
-      const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kb.x, kb.y, kb.z, kb.w};
-      uint32_t ya[4], yb[4];
-      bool ok = true;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 rc = cs[j];  // (cos, sin) of elements 2j, 2j + 1 of the chunk
-        const float a0 = __uint_as_float(wa[j] << 16), a1 = __uint_as_float(wa[j] & 0xFFFF0000u);
-        const float b0 = __uint_as_float(wb[j] << 16), b1 = __uint_as_float(wb[j] & 0xFFFF0000u);
-        const float ra0 = a0 * rc.x - b0 * rc.y, rb0 = a0 * rc.y + b0 * rc.x;
-        const float ra1 = a1 * rc.z - b1 * rc.w, rb1 = a1 * rc.w + b1 * rc.z;
-        ok = ok && fits_f16(ra0) && fits_f16(ra1) && fits_f16(rb0) && fits_f16(rb1);
-        ya[j] = pack_f16(ra0, ra1);
-        yb[j] = pack_f16(rb0, rb1);
-      }
-      if (!ok) record_error(v.status, DEV_RANGE, 3, c);
-      const int pa = swizzle_chunk(c, off) * 8, pb = swizzle_chunk(c + CP, off) * 8;
-      const uint4 A = make_uint4(ya[0], ya[1], ya[2], ya[3]), B = make_uint4(yb[0], yb[1], yb[2], yb[3]);
-      *reinterpret_cast<uint4*>(v.k_rot + dst + pa) = A;
-      *reinterpret_cast<uint4*>(v.k_rot + dst + pb) = B;
-      if (v.k_raw) {
-        *reinterpret_cast<uint4*>(v.k_raw + dst + pa) = ka;
-        *reinterpret_cast<uint4*>(v.k_raw + dst + pb) = kb;
-      }
-      if (kstage) {
-        *reinterpret_cast<uint4*>(kstage + r * D + pa) = A;
-        *reinterpret_cast<uint4*>(kstage + r * D + pb) = B;
-      }
-    } else if (lane < CP + D / 8) {
-      const int c = lane - CP;
-      const uint4 x = *reinterpret_cast<const uint4*>(args.v_new + src + c * 8);
-      *reinterpret_cast<uint4*>(v.v + dst + swizzle_chunk(c, off) * 8) = x;
-      if (kstage) *reinterpret_cast<uint4*>(kstage + (64 + r) * D + swizzle_chunk(c, off) * 8) = x;
-    }
+  const int rp = slot / ps, off = slot % ps;
+  const int page = rp < v.max_pages ? v.page_table[static_cast<int64_t>(dsc.stream) * v.max_pages + rp] : -1;
+  if (page < 0 || page >= v.n_pages) {
+    if (lane == 0) record_error(v.status, DEV_BOUNDS, 24, page);
+    return;
   }
-  if (kstage) fence_proxy_async_smem();  // the rows written above precede the buffer's next bulk copies
-  __syncwarp();
+  const int64_t dst = pool_offset(v, layer, page, un.kvh, off);
+  const int64_t row = static_cast<int64_t>(un.a) * nq + t;
+  const int64_t src = un.lz * args.kv_layer_stride + (row * hkv + un.kvh) * D;
+  if (lane < CP) {
+    const int c = lane;
+    const uint4 ka = *reinterpret_cast<const uint4*>(args.k_new + src + c * 8);
+    const uint4 kb = *reinterpret_cast<const uint4*>(args.k_new + src + H + c * 8);
+    const float4* cs = reinterpret_cast<const float4*>(v.cs_new + (row * H + c * 8) * 2);
+    const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kb.x, kb.y, kb.z, kb.w};
+    uint32_t ya[4], yb[4];
+    bool ok = true;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 rc = cs[j];  // (cos, sin) of elements 2j, 2j + 1 of the chunk
+      const float a0 = __uint_as_float(wa[j] << 16), a1 = __uint_as_float(wa[j] & 0xFFFF0000u);
+      const float b0 = __uint_as_float(wb[j] << 16), b1 = __uint_as_float(wb[j] & 0xFFFF0000u);
+      const float ra0 = a0 * rc.x - b0 * rc.y, rb0 = a0 * rc.y + b0 * rc.x;
+      const float ra1 = a1 * rc.z - b1 * rc.w, rb1 = a1 * rc.w + b1 * rc.z;
+      ok = ok && fits_f16(ra0) && fits_f16(ra1) && fits_f16(rb0) && fits_f16(rb1);
+      ya[j] = pack_f16(ra0, ra1);
+      yb[j] = pack_f16(rb0, rb1);
+    }
+    if (!ok) record_error(v.status, DEV_RANGE, 3, c);
+    const int pa = swizzle_chunk(c, off) * 8, pb = swizzle_chunk(c + CP, off) * 8;
+    *reinterpret_cast<uint4*>(v.k_rot + dst + pa) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+    *reinterpret_cast<uint4*>(v.k_rot + dst + pb) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+    if (v.k_raw) {
+      *reinterpret_cast<uint4*>(v.k_raw + dst + pa) = ka;
+      *reinterpret_cast<uint4*>(v.k_raw + dst + pb) = kb;
+    }
+  } else if (lane < CP + D / 8) {
+    const int c = lane - CP;
+    const uint4 x = *reinterpret_cast<const uint4*>(args.v_new + src + c * 8);
+    *reinterpret_cast<uint4*>(v.v + dst + swizzle_chunk(c, off) * 8) = x;
+  }
 }
 
 // Up to two CTAs per SM.  Without a cluster the CTA walks units u = blockIdx.x,
@@ -416,7 +394,7 @@ __device__ __forceinline__ void write_new(const AttnArgs& args, const StepDesc& 
 // into registers and frees the ring slot before the softmax and PV, so the
 // slot refills while the warp computes.
 template <int D, int NT, bool ON_READ, bool FUSE>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const __grid_constant__ AttnArgs args) {
+__global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kernel(const __grid_constant__ AttnArgs args) {
   constexpr int KSTEPS = D / 16;  // k-steps of QK^T, m-tiles of PV
   constexpr int QSTR = D + 8;     // padded fp16 row stride of the query tiles
   constexpr int OSTR = D + 4;     // padded fp32 row stride of the output accumulator
@@ -429,6 +407,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
   uint16_t* ql_s = qh_s + ROWS * QSTR;                 // [ROWS][QSTR] fp16 lo
   float* obuf = reinterpret_cast<float*>(ql_s + ROWS * QSTR);  // [2][ROWS][OSTR] fp32 partial sums
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
+  __shared__ int new_done;  // fused append: units whose new rows the appender has written
   __shared__ float red_m[kCW][ROWS], red_l[kCW][ROWS];
   __shared__ float row_m[ROWS], row_l[ROWS];
   __shared__ int abort_flag, poisoned_s;
@@ -446,11 +425,18 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
   const int u_first = splits > 1 ? static_cast<int>(blockIdx.x / splits) : static_cast<int>(blockIdx.x);
   const int u_step = splits > 1 ? n_units : static_cast<int>(gridDim.x);
 
+  // the producer's lanes touch every 32-byte line of the launch's parameters, so that the reads
+  // after the dependency wait find them in the constant cache
+  if (warp == kCW && lane * 32 < static_cast<int>(sizeof(AttnArgs))) {
+    const uint32_t w = reinterpret_cast<const uint32_t*>(&args)[lane * 8];
+    asm volatile("" ::"r"(w));
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), kCW);
     }
+    new_done = 0;
     abort_flag = 0;
     // after a timed-out wait anywhere, later launches skip their copies (the
     // status word already reports the failure; each CTA ends quickly)
@@ -464,9 +450,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
     // ---------------- producer: the warp walks every stage of every unit in the order the
     // consumers take them; lane 0 issues the bulk copies, the lanes hold 32 page-table
     // entries at a time, the next unit's descriptor is loaded a unit ahead.  With the append
-    // fused, the walk always completes: after a timed-out wait (or in a launch that starts
-    // after one) it still writes every new token into the pool, only the copies stop.
-    if (!poisoned || FUSE) {
+    // fused, the copies of a stage that holds new tokens wait for the appender warp.
+    if (!poisoned) {
       const int ps = v.page_size;
       const uint16_t* kreg = v.k_rot;
       const int copies = ps >= kKS ? 1 : kKS / ps;
@@ -475,16 +460,24 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
       int k = 0;  // stages walked so far (ring position)
       int k_issued = 0;  // stages walked up to the last one whose copies were issued
       bool stop = poisoned;
+      int uj = 0;  // fused append: this CTA's units walked before the current one
       StepDesc dnext;
+      int pbase = -64, pt_lane = 0;  // the lanes' 32-entry window of the unit's page-table row
       // the page table comes from rkv_create; the descriptors from the begin-step kernel, read
-      // before the wait only when it ran two or more launches back (args.early); the pages may
-      // come from the immediate predecessor: the bulk copies start after the wait
+      // before the wait only when it ran two or more launches back (args.early), and then the
+      // first unit's first page-table window with them; the pages may come from the immediate
+      // predecessor: the bulk copies start after the wait
       const bool desc_early = (args.early & kEarlyDesc) != 0;
-      if (u_first < n_units && desc_early && !stop) dnext = v.desc[unit_of(u_first, n_active, hkv).a];
+      if (u_first < n_units && desc_early && !stop) {
+        dnext = v.desc[unit_of(u_first, n_active, hkv).a];
+        pbase = split * args.stages_per_split * kKS / ps;
+        pt_lane = pbase + lane < v.max_pages ? v.page_table[static_cast<int64_t>(dnext.stream) * v.max_pages + pbase + lane]
+                                              : 0;
+      }
       pdl_wait();
       pdl_launch_dependents();
       if (u_first < n_units && !(desc_early && !poisoned)) dnext = v.desc[unit_of(u_first, n_active, hkv).a];
-      for (int u = u_first; u < n_units; u += u_step) {
+      for (int u = u_first; u < n_units; u += u_step, ++uj) {
         const Unit un = unit_of(u, n_active, hkv);
         const StepDesc dsc = dnext;
         if (u + u_step < n_units) dnext = v.desc[unit_of(u + u_step, n_active, hkv).a];  // lands during this unit
@@ -492,12 +485,13 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
         const int n_st = (slots_in_use(dsc) + kKS - 1) / kKS;
         const int st0 = split * args.stages_per_split;
         const int cnt = max(0, min(st0 + args.stages_per_split, n_st) - st0);
-        if (FUSE && !stop) prefetch_new<D>(args, dsc, un, st0, cnt, lane);
+        const int first = FUSE ? first_new_slot(dsc) : 0;
+        const int rot = FUSE ? walk_rot(first, v.q_per_step, dsc.ring, n_st) : 0;
         const int stream_pages = (dsc.ring + ps - 1) / ps;
         const int32_t* ptab = v.page_table + static_cast<int64_t>(dsc.stream) * v.max_pages;
-        int pbase = -64, pt_lane = 0;
+        if (u != u_first) pbase = -64;  // another stream's row
         for (int i = 0; i < cnt; ++i, ++k) {
-          const int st = st0 + i;
+          const int st = FUSE && st0 + i + rot >= n_st ? st0 + i + rot - n_st : st0 + i + rot;
           const int buf = k % kStages;
           if (!stop && k >= kStages &&
               !__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty_bar[buf]), ((k / kStages) - 1) & 1, v.wait_ns))) {
@@ -508,19 +502,22 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
             stop = true;
           }
           if (!stop && __any_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&abort_flag) != 0)) stop = true;
+          // fused append: a stage with new tokens is copied once the appender has written the
+          // unit's rows into the pool
+          if (FUSE && !stop && stage_has_new(first, v.q_per_step, dsc.ring, st) &&
+              !__all_sync(0xffffffffu, wait_count(&new_done, uj + 1, v.wait_ns))) {
+            if (lane == 0) {
+              record_error(v.status, DEV_TIMEOUT, 25, k);
+              atomicExch(&abort_flag, 1);
+            }
+            stop = true;
+          }
           if (!stop) k_issued = k + 1;
-          // fused append: the stage's new rows go into the pool and, when the stage is copied,
-          // into its buffer, which the copies below then skip
-          const uint64_t patched = FUSE ? new_rows(dsc, v.q_per_step, st) : 0;
           // the failure-detection test hook: this stage's copy never starts, so its consumers'
           // bounded wait runs out
-          if (stop || k == v.withhold_stage) {
-            if (FUSE && patched) write_new<D>(args, dsc, un, st, nullptr, lane);
-            continue;
-          }
-          if (FUSE && patched) write_new<D>(args, dsc, un, st, kv_s + buf * 2 * STAGE_ELEMS, lane);
+          if (stop || k == v.withhold_stage) continue;
           const uint32_t fb = smem_u32(&full_bar[buf]);
-          if (lane == 0) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(kKS - __popcll(patched)) * D * 2 * 2);
+          if (lane == 0) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(kKS) * D * 2 * 2);
           for (int c = 0; c < copies; ++c) {
             const int slot = st * kKS + c * rows_per_copy;
             int rp = slot / ps;
@@ -538,24 +535,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
             if (lane == 0) {
               const int64_t src = pool_offset(v, layer, page, un.kvh, off);
               const uint32_t dk = smem_u32(kv_s + buf * 2 * STAGE_ELEMS + c * rows_per_copy * D);
-              const int r0 = c * rows_per_copy;
-              if (!FUSE || ((patched >> r0) & ((uint64_t(2) << (rows_per_copy - 1)) - 1)) == 0) {
-                bulk_copy_g2s(dk, kreg + src, bytes, fb);
-                bulk_copy_g2s(dk + STAGE_ELEMS * 2, v.v + src, bytes, fb);
-              } else {  // runs of rows around the ones written above
-                for (int a = 0; a < rows_per_copy;) {
-                  if ((patched >> (r0 + a)) & 1) {
-                    ++a;
-                    continue;
-                  }
-                  int b = a;
-                  while (b < rows_per_copy && !((patched >> (r0 + b)) & 1)) ++b;
-                  const uint32_t nb = static_cast<uint32_t>(b - a) * D * 2;
-                  bulk_copy_g2s(dk + a * D * 2, kreg + src + a * D, nb, fb);
-                  bulk_copy_g2s(dk + STAGE_ELEMS * 2 + a * D * 2, v.v + src + a * D, nb, fb);
-                  a = b;
-                }
-              }
+              bulk_copy_g2s(dk, kreg + src, bytes, fb);
+              bulk_copy_g2s(dk + STAGE_ELEMS * 2, v.v + src, bytes, fb);
             }
           }
         }
@@ -566,6 +547,29 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
         for (int i = max(0, k_issued - kStages); i < k_issued; ++i)
           if (i != v.withhold_stage && !mbar_wait(smem_u32(&full_bar[i % kStages]), (i / kStages) & 1, v.wait_ns))
             record_error(v.status, DEV_TIMEOUT, 22, i);
+    }
+  } else if (FUSE && warp == kCW + 1) {
+    // ---------------- appender (fused append): after the wait, since the new keys and values may
+    // come from the immediate predecessor, the new tokens of every unit the CTA walks that fall in
+    // its stages, publishing the count of units done after each.  It runs in a launch that skips
+    // its copies too.
+    pdl_wait();
+    int done = 0;
+    for (int u = u_first; u < n_units; u += u_step) {
+      const Unit un = unit_of(u, n_active, hkv);
+      const StepDesc dsc = v.desc[un.a];
+      const int n_st = (slots_in_use(dsc) + kKS - 1) / kKS;
+      const int first = first_new_slot(dsc);
+      const int rot = walk_rot(first, nq, dsc.ring, n_st);
+      const int st0 = split * args.stages_per_split;
+      for (int t = 0; t < nq && n_st > 0; ++t) {
+        const int slot = new_slot(first, t, dsc.ring);
+        const int i = (slot / kKS - rot + n_st) % n_st;
+        if (i >= st0 && i < st0 + args.stages_per_split) append_token<D>(args, dsc, un, t, slot, lane);
+      }
+      fence_proxy_async_global();  // the rows precede the producer's bulk copies
+      __syncwarp();
+      if (lane == 0) st_release_smem(&new_done, ++done);
     }
   } else if (!poisoned) {
     // ---------------- consumers
@@ -600,6 +604,12 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
       const int n_st = (nslots + kKS - 1) / kKS;
       const int st0 = split * args.stages_per_split;
       const int my_st = max(0, min(st0 + args.stages_per_split, n_st) - st0);
+      // fused append: the slot of the walk's current stage, from stage rot + st0 on, wrapping
+      int sb = 0;
+      if (FUSE) {
+        const int st = walk_rot(first_new_slot(dsc), nq, dsc.ring, n_st) + st0;
+        sb = (st >= n_st ? st - n_st : st) * kKS;
+      }
 
       q_build<D, NT>(pf, v.scale_log2, tid, qh_s, ql_s);
       if constexpr (ON_READ) {
@@ -654,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
       const int ev_mod = static_cast<int>(dsc.evicted % W);
       const int first_new = len - nq;  // window index of the step's first new token
       bool aborted = false;
-      for (int i = 0; i < my_st; ++i) {
+      for (int i = 0; i < my_st; ++i, sb = sb + kKS >= nslots ? 0 : sb + kKS) {
         const int k = k0 + i;
         const int buf = k % kStages;
         // warp-uniform decision: every lane leaves together if any lane gave up
@@ -666,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) attn_kernel(const _
           aborted = true;
           break;
         }
-        const int slot_base = (st0 + i) * kKS + wt * 16;
+        const int slot_base = (FUSE ? sb : (st0 + i) * kKS) + wt * 16;
         const uint32_t kb = smem_u32(kv_s + buf * 2 * STAGE_ELEMS);
         const uint32_t vb = kb + STAGE_ELEMS * 2;
         if (slot_base >= nslots) {  // none of this warp's slots holds a token
@@ -996,7 +1006,7 @@ struct Kernel {
       cudaFuncSetAttribute(attn_kernel<D, NT, ON_READ, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem_bytes<D, NT>());
       int o = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, attn_kernel<D, NT, ON_READ, FUSE>, kThreads,
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, attn_kernel<D, NT, ON_READ, FUSE>, threads_of<FUSE>(),
                                                         smem_bytes<D, NT>()) != cudaSuccess)
         o = 1;
       occ[dev] = o < 1 ? 1 : o;
@@ -1007,7 +1017,7 @@ struct Kernel {
     occupancy();
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads_of<FUSE>());
     cfg.dynamicSmemBytes = smem_bytes<D, NT>();
     cfg.stream = st;
     cudaLaunchAttribute attr[2];

@@ -51,6 +51,7 @@ def _handle(rkv, wl):
 @pytest.mark.parametrize("path,withhold", [
     ("per_layer", 0),      # few units: each window split over a cluster of CTAs merged in shared memory
     ("static", 0),         # the scratch form: per-split partials and a merge kernel
+    ("fused", 0),          # the append fused into the launch: the appender warp still writes the tokens
     ("whole_step", 4),     # many units: persistent CTAs, the stage withheld in a CTA's second unit
 ])
 def test_bounded_wait_runs_out_and_the_handle_recovers(path, withhold):
@@ -74,10 +75,13 @@ def test_bounded_wait_runs_out_and_the_handle_recovers(path, withhold):
         for layer in range(L):
             h.gen_step_inputs(wl.seed, layer, wl.input_scale, q[layer], k[layer], v[layer])
             h.rebase(layer)
-            h.append_rope(layer, k[layer], v[layer])
+            if path != "fused":
+                h.append_rope(layer, k[layer], v[layer])
             if layer == fail_layer:
                 rkv.rkv_set_wait_test(h.handle, withhold, WAIT_NS)
-            if path == "static":
+            if path == "fused":
+                h.append_decode_attn(layer, q[layer], k[layer], v[layer], out[layer], lse[layer])
+            elif path == "static":
                 rkv.rkv_decode_attn_static(h.handle, layer, q[layer], out[layer], lse[layer])
             else:
                 h.decode_attn(layer, q[layer], out[layer], lse[layer])

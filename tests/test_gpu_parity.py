@@ -144,6 +144,12 @@ FULL = {
     # the per-layer calls over keys stored at their ring slot
     "qwen_on_read": ("qwen", dict(scheme=2), 1000, [0, 374, 375, 376, 999], [0, 40, 63]),
     "encoder_step": ("encoder", dict(), 200, [0, 4, 744, 748, 752, 796], [0, 31], True),
+    # the append fused into the per-layer attention launch (rkv_append_decode_attn): one unit per
+    # CTA at the Qwen shape and on the mixed schedule; several units per CTA at 1024 streams
+    "qwen_fused": ("qwen", dict(), 1000, [0, 374, 375, 376, 999], [0, 17, 40, 63], "fused"),
+    "mixed_fused_on_read": ("mixed", dict(scheme=2), 510, "schedule", [0, 1, 2, 3, 4], "fused"),
+    "max_streams_fused": ("qwen", dict(n_layers=1, n_streams=1024, extra={"window": 40}, scheme=2), 50,
+                          [0, 39, 40, 49], [0, 511, 1023], "fused"),
 }
 
 
@@ -151,7 +157,8 @@ FULL = {
 @pytest.mark.parametrize("case", sorted(FULL))
 def test_full_size_sampled(case):
     name, over, ticks, steps, streams, *opt = FULL[case]
-    whole_step = bool(opt and opt[0])
+    whole_step = bool(opt and opt[0] is True)
+    attn = opt[0] if opt and isinstance(opt[0], str) else "regular"
     wl = synth.workload(name, **over)
     layers = sorted({0, wl.n_layers // 2, wl.n_layers - 1})
     final = final_counts(wl, ticks)
@@ -172,7 +179,7 @@ def test_full_size_sampled(case):
                     want.add((s, layer, n_old))
     if steps == "schedule":
         assert all(final[s] >= w[s] + 2 for s in streams)   # every chosen window filled and rolled
-    run = run_gpu(wl, ticks, want, streams_of_interest=streams, whole_step=whole_step)
+    run = run_gpu(wl, ticks, want, streams_of_interest=streams, whole_step=whole_step, attn=attn)
     assert set(run.samples) == want
     e_o, e_l = compare(run, wl)
     for s in streams:
