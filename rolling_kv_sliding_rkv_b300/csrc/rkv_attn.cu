@@ -474,6 +474,58 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
         pt_lane = pbase + lane < v.max_pages ? v.page_table[static_cast<int64_t>(dnext.stream) * v.max_pages + pbase + lane]
                                               : 0;
       }
+      // the bulk copies of stage st of (layer, kv head) into ring buffer buf
+      auto issue = [&](int st, int buf, int layer, int kvh, int stream_pages, const int32_t* ptab) {
+        const uint32_t fb = smem_u32(&full_bar[buf]);
+        if (lane == 0) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(kKS) * D * 2 * 2);
+        for (int c = 0; c < copies; ++c) {
+          const int slot = st * kKS + c * rows_per_copy;
+          int rp = slot / ps;
+          const int off = slot % ps;
+          if (rp >= stream_pages) rp = 0;  // past the window: any finite page (masked)
+          if (rp < pbase || rp >= pbase + 32) {  // warp-uniform: refill the lanes' page-table window
+            pbase = rp;
+            pt_lane = pbase + lane < v.max_pages ? ptab[pbase + lane] : 0;
+          }
+          int page = __shfl_sync(0xffffffffu, pt_lane, rp - pbase);
+          if (page < 0 || page >= v.n_pages) {
+            if (lane == 0) record_error(v.status, DEV_BOUNDS, 21, page);
+            page = 0;
+          }
+          if (lane == 0) {
+            const int64_t src = pool_offset(v, layer, page, kvh, off);
+            const uint32_t dk = smem_u32(kv_s + buf * 2 * STAGE_ELEMS + c * rows_per_copy * D);
+            bulk_copy_g2s(dk, kreg + src, bytes, fb);
+            bulk_copy_g2s(dk + STAGE_ELEMS * 2, v.v + src, bytes, fb);
+          }
+        }
+      };
+      // Fused append over keys that no launch of the step rewrites (offset-only, re-base applied
+      // on read): the first unit's first stages hold none of the step's new rows (they are walked
+      // last) and only pages that earlier steps wrote, so their copies start before the wait,
+      // under the tail of the preceding launch.  A CTA with several units (its slot freed only as
+      // the preceding launch's CTAs leave) takes a whole ring early; a CTA with one unit, which
+      // may start while the preceding launch still streams, one stage (measured: a whole ring
+      // there competes with that stream and costs more than it saves).
+      int n_early = 0;
+      const int early_cap = u_first + u_step < n_units ? kStages : 1;
+      if (FUSE && u_first < n_units && desc_early && !stop && v.scheme != RKV_SCHEME_EXACT_REBASE &&
+          v.withhold_stage < 0) {
+        const Unit un = unit_of(u_first, n_active, hkv);
+        const StepDesc& dsc = dnext;
+        const int n_st = (slots_in_use(dsc) + kKS - 1) / kKS;
+        const int st0 = split * args.stages_per_split;
+        const int cnt = max(0, min(st0 + args.stages_per_split, n_st) - st0);
+        const int first = first_new_slot(dsc);
+        const int rot = walk_rot(first, v.q_per_step, dsc.ring, n_st);
+        const int32_t* ptab = v.page_table + static_cast<int64_t>(dsc.stream) * v.max_pages;
+        for (; n_early < early_cap && n_early < cnt; ++n_early) {
+          const int st = st0 + n_early + rot >= n_st ? st0 + n_early + rot - n_st : st0 + n_early + rot;
+          if (stage_has_new(first, v.q_per_step, dsc.ring, st)) break;
+          issue(st, n_early, args.layer0 + un.lz, un.kvh, (dsc.ring + ps - 1) / ps, ptab);
+        }
+        k = k_issued = n_early;
+      }
       pdl_wait();
       pdl_launch_dependents();
       if (u_first < n_units && !(desc_early && !poisoned)) dnext = v.desc[unit_of(u_first, n_active, hkv).a];
@@ -490,7 +542,7 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
         const int stream_pages = (dsc.ring + ps - 1) / ps;
         const int32_t* ptab = v.page_table + static_cast<int64_t>(dsc.stream) * v.max_pages;
         if (u != u_first) pbase = -64;  // another stream's row
-        for (int i = 0; i < cnt; ++i, ++k) {
+        for (int i = u == u_first ? n_early : 0; i < cnt; ++i, ++k) {
           const int st = FUSE && st0 + i + rot >= n_st ? st0 + i + rot - n_st : st0 + i + rot;
           const int buf = k % kStages;
           if (!stop && k >= kStages &&
@@ -516,29 +568,7 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
           // the failure-detection test hook: this stage's copy never starts, so its consumers'
           // bounded wait runs out
           if (stop || k == v.withhold_stage) continue;
-          const uint32_t fb = smem_u32(&full_bar[buf]);
-          if (lane == 0) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(kKS) * D * 2 * 2);
-          for (int c = 0; c < copies; ++c) {
-            const int slot = st * kKS + c * rows_per_copy;
-            int rp = slot / ps;
-            const int off = slot % ps;
-            if (rp >= stream_pages) rp = 0;  // past the window: any finite page (masked)
-            if (rp < pbase || rp >= pbase + 32) {  // warp-uniform: refill the lanes' page-table window
-              pbase = rp;
-              pt_lane = pbase + lane < v.max_pages ? ptab[pbase + lane] : 0;
-            }
-            int page = __shfl_sync(0xffffffffu, pt_lane, rp - pbase);
-            if (page < 0 || page >= v.n_pages) {
-              if (lane == 0) record_error(v.status, DEV_BOUNDS, 21, page);
-              page = 0;
-            }
-            if (lane == 0) {
-              const int64_t src = pool_offset(v, layer, page, un.kvh, off);
-              const uint32_t dk = smem_u32(kv_s + buf * 2 * STAGE_ELEMS + c * rows_per_copy * D);
-              bulk_copy_g2s(dk, kreg + src, bytes, fb);
-              bulk_copy_g2s(dk + STAGE_ELEMS * 2, v.v + src, bytes, fb);
-            }
-          }
+          issue(st, buf, layer, un.kvh, stream_pages, ptab);
         }
       }
       // never leave with copies in flight (only reachable on an aborted run): the last kStages
