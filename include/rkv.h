@@ -94,6 +94,18 @@ typedef enum {
                                 * no bytes) */
 } rkv_scheme;
 
+/* How the pool stores keys and values. */
+typedef enum {
+  RKV_KV_F16 = 0,  /* rotated keys as fp16, values as the bf16 given (the default) */
+  RKV_KV_E4M3 = 1  /* keys (rotated) and values as fp8 e4m3 (round to nearest even), each row of d
+                    * elements (one token, one kv head) with its own power-of-two scale 2^e, e the
+                    * smallest for which max|x| / 2^e <= 448; half the bytes per token, read back
+                    * exactly as code * 2^e.  Offset-only and the re-base applied on read only
+                    * (a materialised re-base would round every retained key again each roll), and
+                    * (n_q_heads / n_kv_heads) * q_per_step <= 8.  No page prescribes it: an
+                    * optional store for more streams per GPU at lower precision. */
+} rkv_kv_format;
+
 /* Shape and policy of one handle.  All layers share it. */
 typedef struct {
   int32_t n_layers;        /* L >= 1 */
@@ -110,6 +122,8 @@ typedef struct {
                             * evicts down to the last W_s in one batch (the oldest batch leaves
                             * together); 0 evicts exactly enough on every step (a plain sliding
                             * window of W_s) */
+  int32_t kv_format;       /* rkv_kv_format; 0 (zero-initialised configs) is the fp16 store */
+  int32_t reserved;        /* must be 0 */
   double rope_theta;       /* RoPE base theta > 1 (1e6 for the Qwen2.5 decoder) */
   double softmax_scale;    /* score scale; 0 selects 1/sqrt(head_dim) */
 } rkv_config;

@@ -120,4 +120,45 @@ class RingSlotKeyCache:
         return o, lse
 
 
-__all__ = ["StoredKeyCache", "RingSlotKeyCache", "SCHEME_OFFSET_ONLY", "SCHEME_EXACT_REBASE"]
+def stored_key_attention_step(q_new, k_tok, v_tok, key_tokens, n: int, window: int, scale: float,
+                              theta: float, stored_pos, quantize=None, first_key: int | None = None):
+    """One step's outputs over keys as a store holds them, without the store's state.
+
+    Key token j is stored rotated by R(s_j), s_j = stored_pos(j) (P0 + j offset-only; j mod C
+    with the exact re-base applied on read), then passed through ``quantize`` (rows of d, e.g.
+    ``oracle.fp8.quantize_rows``); values through the same.  Query token t meets key j rotated
+    by R(t - j + s_j), so every score is <R(t - j) q, k_j> up to the store's rounding: with no
+    quantisation this is the definition (``oracle.attention.attention_step``) exactly, and the
+    fp8 store's error is modelled by quantising what the store would hold.
+    Arguments as ``attention_step`` (q_new [Q][Hq][d] raw, k_tok / v_tok [T][Hkv][d] raw)."""
+    from .attention import visible_keys
+    q_new = np.asarray(q_new, dtype=np.float64)
+    k_tok = np.asarray(k_tok, dtype=np.float64)
+    v_tok = np.asarray(v_tok, dtype=np.float64)
+    key_tokens = [int(j) for j in key_tokens]
+    row = {j: r for r, j in enumerate(key_tokens)}
+    spos = [int(stored_pos(j)) for j in key_tokens]
+    k_st = np.stack([rotate(k_tok[r][None], [spos[r]], theta)[0] for r in range(len(key_tokens))])
+    v_st = v_tok
+    if quantize is not None:
+        k_st, v_st = quantize(k_st), quantize(v_st)
+    n_q, hq, d = q_new.shape
+    group = hq // k_tok.shape[1]
+    o = np.zeros((n_q, hq, d))
+    lse = np.zeros((n_q, hq))
+    for i, (lo, hi) in enumerate(visible_keys(n, n_q, window, first_key=first_key)):
+        t = n + i
+        rows = [row[j] for j in range(lo, hi + 1)]
+        qpos = [t - key_tokens[r] + spos[r] for r in rows]
+        q_rot = {p: rotate(q_new[i][None], [p], theta)[0] for p in set(qpos)}
+        for h in range(hq):
+            s = np.array([k_st[r, h // group] @ q_rot[p][h] for r, p in zip(rows, qpos)]) * scale
+            m = s.max()
+            e = np.exp(s - m)
+            o[i, h] = e @ v_st[rows, h // group] / e.sum()
+            lse[i, h] = m + math.log(e.sum())
+    return o, lse
+
+
+__all__ = ["StoredKeyCache", "RingSlotKeyCache", "stored_key_attention_step", "SCHEME_OFFSET_ONLY",
+           "SCHEME_EXACT_REBASE"]

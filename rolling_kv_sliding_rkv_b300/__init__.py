@@ -11,7 +11,7 @@ from __future__ import annotations
 from . import _abi
 from ._abi import (  # noqa: F401
     RKV_ERR_CAPACITY, RKV_ERR_CONFIG, RKV_ERR_CUDA, RKV_ERR_DEVICE_BOUNDS, RKV_ERR_DEVICE_RANGE, RKV_ERR_INVALID_ARG,
-    RKV_ERR_STATE, RKV_ERR_TIMEOUT, RKV_OK, RKV_SCHEME_EXACT_ON_READ, RKV_SCHEME_EXACT_REBASE, RKV_SCHEME_OFFSET_ONLY,
+    RKV_ERR_STATE, RKV_ERR_TIMEOUT, RKV_KV_E4M3, RKV_KV_F16, RKV_OK, RKV_SCHEME_EXACT_ON_READ, RKV_SCHEME_EXACT_REBASE, RKV_SCHEME_OFFSET_ONLY,
     STATE_FIELDS, RkvError, make_config, rkv_append_decode_attn, rkv_append_rope, rkv_begin_step, rkv_check_stream_state, rkv_clock_resolve,
     rkv_create, rkv_decode_attn, rkv_decode_attn_layers, rkv_decode_attn_static, rkv_destroy, rkv_gen_next_inputs, rkv_gen_step_inputs, rkv_gen_tokens,
     rkv_get_stream_state, rkv_last_error, rkv_load_stream, rkv_rebase, rkv_required_bytes, rkv_reset_stream, rkv_reset_streams,

@@ -22,6 +22,8 @@ RKV_ERR_TIMEOUT = -5
 RKV_ERR_STATE = -6
 RKV_ERR_DEVICE_BOUNDS = -7
 RKV_ERR_DEVICE_RANGE = -8
+RKV_KV_F16 = 0
+RKV_KV_E4M3 = 1
 RKV_SCHEME_OFFSET_ONLY = 0
 RKV_SCHEME_EXACT_REBASE = 1
 RKV_SCHEME_EXACT_ON_READ = 2
@@ -40,7 +42,8 @@ class rkv_config(C.Structure):
     _fields_ = [("n_layers", C.c_int32), ("n_streams", C.c_int32), ("n_q_heads", C.c_int32),
                 ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("q_per_step", C.c_int32),
                 ("page_size", C.c_int32), ("scheme", C.c_int32), ("rebase_interval", C.c_int32),
-                ("window_slack", C.c_int32), ("rope_theta", C.c_double), ("softmax_scale", C.c_double)]
+                ("window_slack", C.c_int32), ("kv_format", C.c_int32), ("reserved", C.c_int32),
+                ("rope_theta", C.c_double), ("softmax_scale", C.c_double)]
 
 
 class rkv_clock(C.Structure):

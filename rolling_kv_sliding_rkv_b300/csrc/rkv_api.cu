@@ -31,9 +31,9 @@ struct rkv_handle {
   int32_t n_active = 0;
   std::vector<uint8_t> appended, rebased;
   std::vector<int32_t> first_page, n_pages_of;  // per stream: its contiguous run of pages
-  int32_t regions = 0;
-  uint16_t* pool = nullptr;
-  size_t region_elems = 0;
+  int32_t regions = 0;           // planes of the pool: K, V (, pre-RoPE K | row scales)
+  char* pool = nullptr;
+  size_t region_elems = 0;       // elements (rows x d) of one plane
   std::string last_error;
 };
 
@@ -57,7 +57,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Layout {
   size_t state, page_table, desc, cs_new, cs_q, cs_lap, omega, rope_table, status, total;
-  size_t pool_region_elems;  // elements of one pool region (all layers)
+  size_t pool_region_elems;  // elements (rows x d) of one pool plane (all layers)
+  size_t pool_bytes;
   int32_t max_pages, n_pages, t_rows, w_max, regions;
 };
 
@@ -78,6 +79,12 @@ bool validate_config(const rkv_config* c, std::string* why) {
   if (c->scheme != RKV_SCHEME_OFFSET_ONLY && !rkv::exact_scheme(c->scheme)) return bad("unknown scheme");
   if (c->rebase_interval < 1) return bad("rebase_interval must be >= 1");
   if (c->window_slack < 0 || c->window_slack > RKV_MAX_WINDOW) return bad("window_slack must be in [0, RKV_MAX_WINDOW]");
+  if (c->kv_format != RKV_KV_F16 && c->kv_format != RKV_KV_E4M3) return bad("unknown kv_format");
+  if (c->reserved != 0) return bad("reserved must be 0");
+  if (c->kv_format == RKV_KV_E4M3 && c->scheme == RKV_SCHEME_EXACT_REBASE)
+    return bad("the fp8 store takes offset-only or the re-base applied on read, not the materialised re-base");
+  if (c->kv_format == RKV_KV_E4M3 && c->n_q_heads / c->n_kv_heads * c->q_per_step > 8)
+    return bad("the fp8 store needs (n_q_heads / n_kv_heads) * q_per_step <= 8");
   if (!(c->rope_theta > 1.0) || !std::isfinite(c->rope_theta)) return bad("rope_theta must be finite and > 1");
   if (!(c->softmax_scale >= 0.0) || !std::isfinite(c->softmax_scale)) return bad("softmax_scale must be finite and >= 0");
   (void)buf;
@@ -141,6 +148,13 @@ bool compute_layout(const rkv_config* c, const int32_t* window, Layout* L, std::
   L->status = take(4 * sizeof(int32_t));
   L->total = off;
   L->pool_region_elems = static_cast<size_t>(c->n_layers) * n_pages * c->n_kv_heads * c->page_size * c->head_dim;
+  if (c->kv_format == RKV_KV_E4M3) {
+    // planes: fp8 keys, fp8 values (one byte per element), and a (key, value) scale pair per row
+    L->regions = 3;
+    L->pool_bytes = 2 * L->pool_region_elems + L->pool_region_elems / c->head_dim * 2 * sizeof(float);
+  } else {
+    L->pool_bytes = L->pool_region_elems * L->regions * sizeof(uint16_t);
+  }
   return true;
 }
 
@@ -198,7 +212,7 @@ int rkv_required_bytes(const rkv_config* cfg, const int32_t* window, size_t* poo
   Layout L;
   std::string why;
   if (!compute_layout(cfg, window, &L, &why)) return fail(nullptr, cfg && window ? RKV_ERR_CONFIG : RKV_ERR_INVALID_ARG, why);
-  *pool_bytes = L.pool_region_elems * L.regions * sizeof(uint16_t);
+  *pool_bytes = L.pool_bytes;
   *state_bytes = L.total;
   return RKV_OK;
 }
@@ -217,7 +231,7 @@ int rkv_create(const rkv_config* cfg, const int32_t* window, const int64_t* star
   if (!pool_dev || !state_dev) return fail(nullptr, RKV_ERR_INVALID_ARG, "pool_dev or state_dev is NULL");
   if ((reinterpret_cast<uintptr_t>(pool_dev) | reinterpret_cast<uintptr_t>(state_dev)) & (kAlign - 1))
     return fail(nullptr, RKV_ERR_INVALID_ARG, "device buffers must be 256-byte aligned");
-  const size_t need_pool = L.pool_region_elems * L.regions * sizeof(uint16_t);
+  const size_t need_pool = L.pool_bytes;
   if (pool_bytes < need_pool || state_bytes < L.total)
     return fail(nullptr, RKV_ERR_CAPACITY, "pool or state buffer smaller than rkv_required_bytes");
 
@@ -246,10 +260,13 @@ int rkv_create(const rkv_config* cfg, const int32_t* window, const int64_t* star
   v.part_ml = nullptr;  // split-K partials: only the scratch form of decode attention has them
   v.part_o = nullptr;
   v.status = reinterpret_cast<int32_t*>(sb + L.status);
-  uint16_t* pool = static_cast<uint16_t*>(pool_dev);
-  v.k_rot = pool;
-  v.v = pool + L.pool_region_elems;
-  v.k_raw = L.regions == 3 ? pool + 2 * L.pool_region_elems : nullptr;
+  char* pool = static_cast<char*>(pool_dev);
+  const bool kv8 = cfg->kv_format == RKV_KV_E4M3;
+  const size_t plane_bytes = L.pool_region_elems * (kv8 ? 1 : sizeof(uint16_t));
+  v.k_rot = reinterpret_cast<uint16_t*>(pool);  // fp8: the same plane read as bytes
+  v.v = reinterpret_cast<uint16_t*>(pool + plane_bytes);
+  v.k_raw = !kv8 && L.regions == 3 ? reinterpret_cast<uint16_t*>(pool + 2 * plane_bytes) : nullptr;
+  v.kv_scale = kv8 ? reinterpret_cast<float2*>(pool + 2 * plane_bytes) : nullptr;
   v.layer_stride = static_cast<int64_t>(L.n_pages) * cfg->n_kv_heads * cfg->page_size * cfg->head_dim;
   v.n_streams = cfg->n_streams;
   v.n_layers = cfg->n_layers;
@@ -505,27 +522,40 @@ void snap_header(const rkv_handle* h, int32_t s, int64_t* hdr) {
   const rkv_config& c = h->cfg;
   const int64_t fields[kSnapHeader] = {kSnapMagic, 1, c.n_layers, c.n_kv_heads, c.head_dim, c.page_size,
                                        c.scheme, c.q_per_step, c.rebase_interval,
-                                       static_cast<int64_t>(h->n_pages_of[s]), h->regions, c.window_slack, 0, 0, 0, 0};
+                                       static_cast<int64_t>(h->n_pages_of[s]), h->regions, c.window_slack,
+                                       c.kv_format, 0, 0, 0};
   std::memcpy(hdr, fields, sizeof fields);
 }
 
-// elements of one (region, layer) run of a stream's pages
-size_t snap_run_elems(const rkv_handle* h, int32_t s) {
+// Bytes per row (one token, one kv head) of plane r: d 16-bit elements; with the fp8 store d
+// bytes of keys or values, and the row's two float scales.
+size_t plane_row_bytes(const rkv_handle* h, int r) {
   const rkv_config& c = h->cfg;
-  return static_cast<size_t>(h->n_pages_of[s]) * c.n_kv_heads * c.page_size * c.head_dim;
+  if (c.kv_format != RKV_KV_E4M3) return static_cast<size_t>(c.head_dim) * sizeof(uint16_t);
+  return r < 2 ? static_cast<size_t>(c.head_dim) : 2 * sizeof(float);
+}
+
+// bytes of one (plane, layer) run of a stream's pages
+size_t snap_run_bytes(const rkv_handle* h, int32_t s, int r) {
+  const rkv_config& c = h->cfg;
+  return static_cast<size_t>(h->n_pages_of[s]) * c.n_kv_heads * c.page_size * plane_row_bytes(h, r);
 }
 
 size_t snap_bytes(const rkv_handle* h, int32_t s) {
-  return (kSnapHeader + kSnapState) * sizeof(int64_t) +
-         static_cast<size_t>(h->regions) * h->cfg.n_layers * snap_run_elems(h, s) * sizeof(uint16_t);
+  size_t b = (kSnapHeader + kSnapState) * sizeof(int64_t);
+  for (int r = 0; r < h->regions; ++r) b += static_cast<size_t>(h->cfg.n_layers) * snap_run_bytes(h, s, r);
+  return b;
 }
 
-
-// pointer to (region r, layer l) of stream s's pages
-uint16_t* snap_run(const rkv_handle* h, int32_t s, int r, int l) {
+// pointer to (plane r, layer l) of stream s's pages
+char* snap_run(const rkv_handle* h, int32_t s, int r, int l) {
   const rkv_config& c = h->cfg;
-  return h->pool + static_cast<size_t>(r) * h->region_elems + static_cast<size_t>(l) * h->view.layer_stride +
-         static_cast<size_t>(h->first_page[s]) * c.n_kv_heads * c.page_size * c.head_dim;
+  const size_t rows_per_plane = h->region_elems / c.head_dim, rows_per_layer = h->view.layer_stride / c.head_dim;
+  size_t base = 0;
+  for (int p = 0; p < r; ++p) base += rows_per_plane * plane_row_bytes(h, p);
+  return h->pool + base +
+         (static_cast<size_t>(l) * rows_per_layer + static_cast<size_t>(h->first_page[s]) * c.n_kv_heads * c.page_size) *
+             plane_row_bytes(h, r);
 }
 
 }  // namespace
@@ -552,10 +582,11 @@ int rkv_save_stream(rkv_handle* h, int32_t stream_id, void* dst, size_t bytes, v
     e = cudaMemcpyAsync(d + sizeof hdr, h->view.state + static_cast<int64_t>(stream_id) * rkv::kStateFields,
                         kSnapState * sizeof(int64_t), cudaMemcpyDefault, st);
   size_t off = (kSnapHeader + kSnapState) * sizeof(int64_t);
-  const size_t run = snap_run_elems(h, stream_id) * sizeof(uint16_t);
-  for (int r = 0; r < h->regions && e == cudaSuccess; ++r)
+  for (int r = 0; r < h->regions && e == cudaSuccess; ++r) {
+    const size_t run = snap_run_bytes(h, stream_id, r);
     for (int l = 0; l < h->cfg.n_layers && e == cudaSuccess; ++l, off += run)
       e = cudaMemcpyAsync(d + off, snap_run(h, stream_id, r, l), run, cudaMemcpyDefault, st);
+  }
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   return e == cudaSuccess ? RKV_OK : cuda_fail(h, e, "saving a stream");
 }
@@ -588,10 +619,11 @@ int rkv_load_stream(rkv_handle* h, int32_t stream_id, const void* src, size_t by
   e = cudaMemcpyAsync(h->view.state + static_cast<int64_t>(stream_id) * rkv::kStateFields, sp + sizeof hdr,
                       kSnapState * sizeof(int64_t), cudaMemcpyDefault, st);
   size_t off = (kSnapHeader + kSnapState) * sizeof(int64_t);
-  const size_t run = snap_run_elems(h, stream_id) * sizeof(uint16_t);
-  for (int r = 0; r < h->regions && e == cudaSuccess; ++r)
+  for (int r = 0; r < h->regions && e == cudaSuccess; ++r) {
+    const size_t run = snap_run_bytes(h, stream_id, r);
     for (int l = 0; l < h->cfg.n_layers && e == cudaSuccess; ++l, off += run)
       e = cudaMemcpyAsync(snap_run(h, stream_id, r, l), sp + off, run, cudaMemcpyDefault, st);
+  }
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   return e == cudaSuccess ? RKV_OK : cuda_fail(h, e, "loading a stream");
 }

@@ -46,6 +46,9 @@ struct DevView {
   uint16_t* k_rot;       // pool: [L][n_pages][Hkv][ps][d] rotated keys, fp16 bits
   uint16_t* v;           // pool: values (bf16 bits), same layout
   uint16_t* k_raw;       // pool: pre-RoPE keys (bf16 bits; materialised exact re-base only), same layout
+  // fp8 store (kv_format e4m3): k_rot and v point at planes of d bytes per row instead, and
+  // kv_scale at the rows' (key, value) scales 2^e, [L][n_pages][Hkv][ps]; NULL otherwise
+  float2* kv_scale;
   int64_t layer_stride;  // elements of one layer in one pool region
   int32_t n_streams, n_layers, n_q_heads, n_kv_heads, head_dim, q_per_step;
   int32_t page_size, n_pages, max_pages, t_rows;

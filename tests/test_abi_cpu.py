@@ -66,13 +66,20 @@ def test_required_bytes_closed_form():
     pool_l1, _ = rkv.rkv_required_bytes(_cfg(n_layers=1), [375] * 64)
     assert pool_l1 * 36 == pool
     assert state < 8 << 20
+    # fp8 store: one byte per key and value element, plus a (key, value) pair of float scales per row
+    rows = 36 * 64 * 6 * 2 * 64
+    for scheme in (0, 2):
+        pool8, _ = rkv.rkv_required_bytes(_cfg(scheme=scheme, kv_format=rkv.RKV_KV_E4M3), [375] * 64)
+        assert pool8 == rows * 128 * 2 + rows * 8
 
 
 @pytest.mark.parametrize("bad", [dict(n_layers=0), dict(n_streams=0), dict(n_streams=2000),
                                  dict(n_q_heads=15), dict(head_dim=96), dict(q_per_step=0),
                                  dict(q_per_step=9), dict(n_q_heads=32, n_kv_heads=1), dict(page_size=48),
                                  dict(scheme=3), dict(rebase_interval=0), dict(rope_theta=1.0),
-                                 dict(window_slack=-1), dict(softmax_scale=-1.0)])
+                                 dict(window_slack=-1), dict(softmax_scale=-1.0), dict(kv_format=2),
+                                 dict(reserved=1), dict(kv_format=1, scheme=1),
+                                 dict(kv_format=1, scheme=2, n_q_heads=16, n_kv_heads=1)])
 def test_invalid_configs(bad):
     cfg = _cfg(**bad)
     with pytest.raises(rkv.RkvError) as e:
