@@ -13,6 +13,11 @@ prescribes a format, so the plainest common one is taken:
   zeros takes e = 0.
 * A key is quantised after its rotation, at the position the scheme stores it at; the
   attention reads code * 2^e, which is exactly what it would read back from the store.
+* The code an element rounds to is an integer decision taken from a floating-point value, so
+  it is taken in the precision the store computes in: the rotation in fp32, each product and
+  sum rounded on its own, from the fp32 roundings of the exactly reduced cos and sin
+  (``rotate_fp32``).  In fp64 the rotated value can fall on the other side of a rounding
+  boundary, and one code a whole e4m3 step apart moves a score by a few 1e-3.
 """
 from __future__ import annotations
 
@@ -54,14 +59,15 @@ def e4m3_round(x) -> np.ndarray:
 
 
 def row_exponent(amax: float) -> int:
-    """The smallest e with amax / 2^e <= 448 (0 for amax = 0).
+    """The smallest e with amax / 2^e <= 448 (0 for amax = 0), kept >= -126 so that 2^e is a
+    normal fp32 number (rows that small round to zero codes either way).
 
     With amax = f * 2^E, f in [0.5, 1): 448 * 2^(E - 9) = 0.875 * 2^E, so e = E - 9 when
     f <= 0.875 and E - 8 otherwise."""
     if amax == 0.0:
         return 0
     f, big_e = math.frexp(amax)
-    return big_e - 9 if f <= 0.875 else big_e - 8
+    return max(-126, big_e - 9 if f <= 0.875 else big_e - 8)
 
 
 def quantize_row(x) -> tuple:
@@ -69,6 +75,23 @@ def quantize_row(x) -> tuple:
     x = np.asarray(x, dtype=np.float64)
     e = row_exponent(float(np.max(np.abs(x))) if x.size else 0.0)
     return e4m3_round(np.ldexp(x, -e)) * 2.0 ** e, e
+
+
+def rotate_fp32(x, positions, theta: float) -> np.ndarray:
+    """R(p) x as the store computes it: x [T][H][d] (bf16 inputs, exact in fp32), one position
+    per T row, pairs (a, b) = (x_i, x_{i+d/2}) -> (a c - b s, a s + b c) with c, s the fp32
+    roundings of the exact cos and sin, every product and difference or sum rounded to fp32."""
+    from .rope import cos_sin
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    c, s = cos_sin(positions, d, theta)
+    c = c.astype(np.float32)[:, None, :]
+    s = s.astype(np.float32)[:, None, :]
+    a = x[..., : d // 2].astype(np.float32)
+    b = x[..., d // 2:].astype(np.float32)
+    ra = (a * c) - (b * s)          # numpy float32: each operation rounds to fp32
+    rb = (a * s) + (b * c)
+    return np.concatenate([ra, rb], axis=-1).astype(np.float64)
 
 
 def quantize_rows(x) -> np.ndarray:
@@ -79,4 +102,4 @@ def quantize_rows(x) -> np.ndarray:
     return out.reshape(x.shape)
 
 
-__all__ = ["E4M3_MAX", "e4m3_grid", "e4m3_round", "row_exponent", "quantize_row", "quantize_rows"]
+__all__ = ["E4M3_MAX", "e4m3_grid", "e4m3_round", "row_exponent", "quantize_row", "quantize_rows", "rotate_fp32"]

@@ -121,7 +121,8 @@ class RingSlotKeyCache:
 
 
 def stored_key_attention_step(q_new, k_tok, v_tok, key_tokens, n: int, window: int, scale: float,
-                              theta: float, stored_pos, quantize=None, first_key: int | None = None):
+                              theta: float, stored_pos, quantize=None, first_key: int | None = None,
+                              rotate_keys=None):
     """One step's outputs over keys as a store holds them, without the store's state.
 
     Key token j is stored rotated by R(s_j), s_j = stored_pos(j) (P0 + j offset-only; j mod C
@@ -129,7 +130,9 @@ def stored_key_attention_step(q_new, k_tok, v_tok, key_tokens, n: int, window: i
     ``oracle.fp8.quantize_rows``); values through the same.  Query token t meets key j rotated
     by R(t - j + s_j), so every score is <R(t - j) q, k_j> up to the store's rounding: with no
     quantisation this is the definition (``oracle.attention.attention_step``) exactly, and the
-    fp8 store's error is modelled by quantising what the store would hold.
+    fp8 store's error is modelled by quantising what the store would hold.  ``rotate_keys(k,
+    positions)`` replaces the fp64 rotation of the stored keys (``oracle.fp8.rotate_fp32``: the
+    store's own fp32 arithmetic, in which its quantisation decisions are taken).
     Arguments as ``attention_step`` (q_new [Q][Hq][d] raw, k_tok / v_tok [T][Hkv][d] raw)."""
     from .attention import visible_keys
     q_new = np.asarray(q_new, dtype=np.float64)
@@ -138,7 +141,10 @@ def stored_key_attention_step(q_new, k_tok, v_tok, key_tokens, n: int, window: i
     key_tokens = [int(j) for j in key_tokens]
     row = {j: r for r, j in enumerate(key_tokens)}
     spos = [int(stored_pos(j)) for j in key_tokens]
-    k_st = np.stack([rotate(k_tok[r][None], [spos[r]], theta)[0] for r in range(len(key_tokens))])
+    if rotate_keys is None:
+        k_st = np.stack([rotate(k_tok[r][None], [spos[r]], theta)[0] for r in range(len(key_tokens))])
+    else:
+        k_st = rotate_keys(k_tok, spos)
     v_st = v_tok
     if quantize is not None:
         k_st, v_st = quantize(k_st), quantize(v_st)

@@ -100,6 +100,84 @@ __global__ void __launch_bounds__(128) append_rope_kernel(DevView v, int layer0,
   *reinterpret_cast<uint4*>(v.k_rot + dst + pb) = yb;
 }
 
+// The fp8 store (kv_format e4m3): the same threads (one per chunk pair of a (row, kv head); the
+// d/16 threads of a row are consecutive lanes), each rotating its 16 key elements in fp32 as above
+// but with every product and sum rounded on its own, so that the code each element rounds to is a
+// function of fp32 arithmetic that a reference can repeat exactly;
+// the row's largest magnitude, of the rotated key and of the value separately, comes from a
+// butterfly over those lanes, fixes the row's scale 2^e, and each element is stored as the e4m3
+// code of x / 2^e (bytes, unswizzled: element i at byte i of the row) with the scales beside.
+// Threads past the last row take part in the butterfly with zeros and store nothing.
+__global__ void __launch_bounds__(128) append_rope_e4m3_kernel(DevView v, int layer0, int n_rows,
+                                                               const uint16_t* __restrict__ k,
+                                                               const uint16_t* __restrict__ val, int64_t kv_layer_stride) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int d = v.head_dim, half = d / 2, cpairs = d / 16, hkv = v.n_kv_heads;
+  const int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  const int64_t per_layer = static_cast<int64_t>(n_rows) * hkv * cpairs;
+  const int lz = blockIdx.y;
+  bool live = idx < per_layer;
+  const int64_t id = live ? idx : 0;
+  const int cp = static_cast<int>(id % cpairs);
+  const int kvh = static_cast<int>((id / cpairs) % hkv);
+  const int row = static_cast<int>(id / (static_cast<int64_t>(cpairs) * hkv));  // a * Q + t
+  const int layer = layer0 + lz;
+  const int a = row / v.q_per_step, t = row % v.q_per_step;
+  const StepDesc dsc = v.desc[a];
+  const int slot = static_cast<int>((dsc.n_old + t) % dsc.ring);
+  const int ring_page = slot / v.page_size;
+  int page = -1;
+  if (live && ring_page >= v.max_pages) {
+    record_error(v.status, DEV_BOUNDS, 1, ring_page);
+    live = false;
+  }
+  if (live) {
+    page = v.page_table[static_cast<int64_t>(dsc.stream) * v.max_pages + ring_page];
+    if (page < 0 || page >= v.n_pages) {
+      record_error(v.status, DEV_BOUNDS, 2, page);
+      live = false;
+    }
+  }
+  float ra[8], rb[8], va[8], vb[8];
+  float km = 0.f, vm = 0.f;
+  bool ok = true;
+  const int64_t src = lz * kv_layer_stride + (static_cast<int64_t>(row) * hkv + kvh) * d;
+  if (live) {
+    float xa[8], xb[8];
+    unpack8(*reinterpret_cast<const uint4*>(k + src + cp * 8), xa);
+    unpack8(*reinterpret_cast<const uint4*>(k + src + half + cp * 8), xb);
+    unpack8(*reinterpret_cast<const uint4*>(val + src + cp * 8), va);
+    unpack8(*reinterpret_cast<const uint4*>(val + src + half + cp * 8), vb);
+    const float* cs = v.cs_new + (static_cast<int64_t>(row) * half + cp * 8) * 2;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // each product and sum rounded to fp32 (no fused multiply-add)
+      const float c = cs[2 * j], sn = cs[2 * j + 1];
+      ra[j] = __fsub_rn(__fmul_rn(xa[j], c), __fmul_rn(xb[j], sn));
+      rb[j] = __fadd_rn(__fmul_rn(xa[j], sn), __fmul_rn(xb[j], c));
+      ok = ok && fits_f16(ra[j]) && fits_f16(rb[j]);
+      km = fmaxf(km, fmaxf(fabsf(ra[j]), fabsf(rb[j])));
+      vm = fmaxf(vm, fmaxf(fabsf(va[j]), fabsf(vb[j])));
+    }
+  }
+  for (int o = 1; o < cpairs; o <<= 1) {
+    km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, o));
+    vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+  }
+  if (!live) return;
+  if (!ok) record_error(v.status, DEV_RANGE, 1, cp);
+  const int ek = e4m3_row_exponent(km), ev = e4m3_row_exponent(vm);
+  const int off = slot % v.page_size;
+  const int64_t dst = pool_offset(v, layer, page, kvh, off);  // = row index * d: a byte offset here
+  uint8_t* k8 = reinterpret_cast<uint8_t*>(v.k_rot);
+  uint8_t* v8 = reinterpret_cast<uint8_t*>(v.v);
+  *reinterpret_cast<uint2*>(k8 + dst + cp * 8) = quantize8(ra, exp2_int(-ek));
+  *reinterpret_cast<uint2*>(k8 + dst + half + cp * 8) = quantize8(rb, exp2_int(-ek));
+  *reinterpret_cast<uint2*>(v8 + dst + cp * 8) = quantize8(va, exp2_int(-ev));
+  *reinterpret_cast<uint2*>(v8 + dst + half + cp * 8) = quantize8(vb, exp2_int(-ev));
+  if (cp == 0) v.kv_scale[dst / d] = make_float2(exp2_int(ek), exp2_int(ev));
+}
+
 // A thread re-bases one chunk pair (elements 8c .. 8c+7 and their partners
 // + d/2) of one kv head for a run of kRebaseRun consecutive ring slots of one
 // stream and layer.  Consecutive slots hold consecutive window positions
@@ -228,6 +306,8 @@ cudaError_t launch_append_rope(const DevView& v, int n_active, int layer0, int n
   const int n_rows = n_active * v.q_per_step;
   const int64_t per_layer = static_cast<int64_t>(n_rows) * v.n_kv_heads * (v.head_dim / 16);
   dim3 grid(static_cast<unsigned>((per_layer + 127) / 128), n_layers);
+  if (v.kv_scale)
+    return launch_pdl(append_rope_e4m3_kernel, grid, dim3(128), 0, st, v, layer0, n_rows, k, vv, kv_layer_stride);
   return launch_pdl(append_rope_kernel, grid, dim3(128), 0, st, v, layer0, n_rows, k, vv, kv_layer_stride);
 }
 

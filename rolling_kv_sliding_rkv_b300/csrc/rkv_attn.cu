@@ -175,6 +175,26 @@ __host__ __device__ constexpr int smem_bytes() {
   // stages (K | V), query tiles hi + lo, two fp32 output tiles
   return stages_for<D>() * 2 * kKS * D * 2 + 2 * (8 * NT) * (D + 8) * 2 + 2 * (8 * NT) * (D + 4) * 4;
 }
+
+// fp8 store: a stage is 64 rows of fp8 keys, 64 of fp8 values and 64 (key, value) scale pairs;
+// ~66 KB of stages (as many tokens in flight as 132 KB of fp16 ones), then one expanded stage
+// (K | V as 16-bit codes, the fp16 stage layout) that the consumer warps fill from each stage
+template <int D>
+__host__ __device__ constexpr int stage8_bytes() {
+  return 2 * kKS * D + kKS * 8;
+}
+template <int D>
+__host__ __device__ constexpr int stages8_for() {
+  return D == 128 ? 4 : 8;
+}
+template <int D, int NT, bool KV8>
+__host__ __device__ constexpr int smem_bytes_for() {
+  return KV8 ? stages8_for<D>() * stage8_bytes<D>() + 2 * kKS * D * 2 + 2 * (8 * NT) * (D + 8) * 2 +
+                   2 * (8 * NT) * (D + 4) * 4
+             : smem_bytes<D, NT>();
+}
+static_assert(smem_bytes_for<128, 1, true>() <= 112 * 1024 && smem_bytes_for<64, 1, true>() <= 112 * 1024,
+              "two fp8-store CTAs per SM");
 static_assert(smem_bytes<128, 2>() <= 227 * 1024, "shared memory budget");
 
 __device__ __forceinline__ float4 ld_dsmem_f32x4(const void* local, uint32_t rank) {
@@ -383,6 +403,81 @@ __device__ __forceinline__ void append_token(const AttnArgs& args, const StepDes
   }
 }
 
+// The same token into the fp8 store: key lanes c < D/16 rotate chunk pair (c, c + D/16), value
+// lanes VB .. VB + D/8 - 1 hold one chunk of 8 values (VB = D/8, so that each group is an aligned
+// run of lanes); butterflies give each group its row's largest magnitude, and the codes of x / 2^e
+// go to the row's bytes, the scales beside.  Every lane of the warp calls it.
+template <int D>
+__device__ __forceinline__ void append_token_e4m3(const AttnArgs& args, const StepDesc& dsc, const Unit& un, int t,
+                                                  int slot, int lane) {
+  const DevView& v = args.v;
+  const int nq = v.q_per_step, hkv = v.n_kv_heads, ps = v.page_size;
+  const int layer = args.layer0 + un.lz;
+  constexpr int CP = D / 16, H = D / 2, VB = D / 8;
+  const int rp = slot / ps, off = slot % ps;
+  const int page = rp < v.max_pages ? v.page_table[static_cast<int64_t>(dsc.stream) * v.max_pages + rp] : -1;
+  if (page < 0 || page >= v.n_pages) {
+    if (lane == 0) record_error(v.status, DEV_BOUNDS, 24, page);
+    return;
+  }
+  const int64_t dst = pool_offset(v, layer, page, un.kvh, off);  // row index * D: a byte offset here
+  const int64_t row = static_cast<int64_t>(un.a) * nq + t;
+  const int64_t src = un.lz * args.kv_layer_stride + (row * hkv + un.kvh) * D;
+  float ra[8], rb[8];
+  float km = 0.f, vm = 0.f;
+  if (lane < CP) {
+    const uint4 ka = *reinterpret_cast<const uint4*>(args.k_new + src + lane * 8);
+    const uint4 kb = *reinterpret_cast<const uint4*>(args.k_new + src + H + lane * 8);
+    const float4* cs = reinterpret_cast<const float4*>(v.cs_new + (row * H + lane * 8) * 2);
+    const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kb.x, kb.y, kb.z, kb.w};
+    bool ok = true;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 rc = cs[j];
+      const float a0 = __uint_as_float(wa[j] << 16), a1 = __uint_as_float(wa[j] & 0xFFFF0000u);
+      const float b0 = __uint_as_float(wb[j] << 16), b1 = __uint_as_float(wb[j] & 0xFFFF0000u);
+      // every product and sum rounded to fp32 on its own, as the append kernel does
+      ra[2 * j] = __fsub_rn(__fmul_rn(a0, rc.x), __fmul_rn(b0, rc.y));
+      rb[2 * j] = __fadd_rn(__fmul_rn(a0, rc.y), __fmul_rn(b0, rc.x));
+      ra[2 * j + 1] = __fsub_rn(__fmul_rn(a1, rc.z), __fmul_rn(b1, rc.w));
+      rb[2 * j + 1] = __fadd_rn(__fmul_rn(a1, rc.w), __fmul_rn(b1, rc.z));
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      ok = ok && fits_f16(ra[j]) && fits_f16(rb[j]);
+      km = fmaxf(km, fmaxf(fabsf(ra[j]), fabsf(rb[j])));
+    }
+    if (!ok) record_error(v.status, DEV_RANGE, 3, lane);
+  } else if (lane >= VB && lane < VB + D / 8) {
+    const uint4 x = *reinterpret_cast<const uint4*>(args.v_new + src + (lane - VB) * 8);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      ra[2 * j] = __uint_as_float(w[j] << 16);
+      ra[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) vm = fmaxf(vm, fabsf(ra[j]));
+  }
+#pragma unroll
+  for (int o = 1; o < D / 8; o <<= 1) {  // key groups of CP lanes and value groups of D/8, aligned
+    const float pk = __shfl_xor_sync(0xffffffffu, km, o), pv = __shfl_xor_sync(0xffffffffu, vm, o);
+    if (o < CP) km = fmaxf(km, pk);
+    vm = fmaxf(vm, pv);
+  }
+  const int ek = e4m3_row_exponent(__shfl_sync(0xffffffffu, km, 0));
+  const int ev = e4m3_row_exponent(__shfl_sync(0xffffffffu, vm, VB));
+  uint8_t* k8 = reinterpret_cast<uint8_t*>(v.k_rot);
+  uint8_t* v8 = reinterpret_cast<uint8_t*>(v.v);
+  if (lane < CP) {
+    *reinterpret_cast<uint2*>(k8 + dst + lane * 8) = quantize8(ra, exp2_int(-ek));
+    *reinterpret_cast<uint2*>(k8 + dst + H + lane * 8) = quantize8(rb, exp2_int(-ek));
+    if (lane == 0) v.kv_scale[dst / D] = make_float2(exp2_int(ek), exp2_int(ev));
+  } else if (lane >= VB && lane < VB + D / 8) {
+    *reinterpret_cast<uint2*>(v8 + dst + (lane - VB) * 8) = quantize8(ra, exp2_int(-ev));
+  }
+}
+
 // Up to two CTAs per SM.  Without a cluster the CTA walks units u = blockIdx.x,
 // blockIdx.x + gridDim.x, ... (whole windows, no split), its producer warp
 // streaming the next unit's pages while the consumers finish the current
@@ -393,17 +488,20 @@ __device__ __forceinline__ void append_token(const AttnArgs& args, const StepDes
 // moves its K fragments into registers, runs QK^T, moves its V fragments
 // into registers and frees the ring slot before the softmax and PV, so the
 // slot refills while the warp computes.
-template <int D, int NT, bool ON_READ, bool FUSE>
+template <int D, int NT, bool ON_READ, bool FUSE, bool KV8>
 __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kernel(const __grid_constant__ AttnArgs args) {
   constexpr int KSTEPS = D / 16;  // k-steps of QK^T, m-tiles of PV
   constexpr int QSTR = D + 8;     // padded fp16 row stride of the query tiles
   constexpr int OSTR = D + 4;     // padded fp32 row stride of the output accumulator
   constexpr int ROWS = 8 * NT;
   constexpr int STAGE_ELEMS = kKS * D;
-  constexpr int kStages = stages_for<D>();
+  constexpr int kStages = KV8 ? stages8_for<D>() : stages_for<D>();
+  constexpr int STAGE_BYTES = KV8 ? stage8_bytes<D>() : 2 * STAGE_ELEMS * 2;
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint16_t* kv_s = reinterpret_cast<uint16_t*>(smem);  // [stage][K | V][64][D]
-  uint16_t* qh_s = kv_s + kStages * 2 * STAGE_ELEMS;   // [ROWS][QSTR] fp16 hi
+  uint16_t* kv_s = reinterpret_cast<uint16_t*>(smem);  // [stage][K | V][64][D] (fp8 store: bytes, + scales)
+  // fp8 store: the expanded stage the consumers read, [K | V][64][D] 16-bit codes
+  uint16_t* exp_s = reinterpret_cast<uint16_t*>(smem + kStages * STAGE_BYTES);
+  uint16_t* qh_s = reinterpret_cast<uint16_t*>(smem + kStages * STAGE_BYTES + (KV8 ? 2 * STAGE_ELEMS * 2 : 0));  // [ROWS][QSTR] fp16 hi
   uint16_t* ql_s = qh_s + ROWS * QSTR;                 // [ROWS][QSTR] fp16 lo
   float* obuf = reinterpret_cast<float*>(ql_s + ROWS * QSTR);  // [2][ROWS][OSTR] fp32 partial sums
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
@@ -456,7 +554,7 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
       const uint16_t* kreg = v.k_rot;
       const int copies = ps >= kKS ? 1 : kKS / ps;
       const int rows_per_copy = ps >= kKS ? kKS : ps;
-      const uint32_t bytes = static_cast<uint32_t>(rows_per_copy) * D * 2;
+      const uint32_t bytes = static_cast<uint32_t>(rows_per_copy) * D * (KV8 ? 1 : 2);
       int k = 0;  // stages walked so far (ring position)
       int k_issued = 0;  // stages walked up to the last one whose copies were issued
       bool stop = poisoned;
@@ -477,7 +575,7 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
       // the bulk copies of stage st of (layer, kv head) into ring buffer buf
       auto issue = [&](int st, int buf, int layer, int kvh, int stream_pages, const int32_t* ptab) {
         const uint32_t fb = smem_u32(&full_bar[buf]);
-        if (lane == 0) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(kKS) * D * 2 * 2);
+        if (lane == 0) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(STAGE_BYTES));
         for (int c = 0; c < copies; ++c) {
           const int slot = st * kKS + c * rows_per_copy;
           int rp = slot / ps;
@@ -494,9 +592,17 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
           }
           if (lane == 0) {
             const int64_t src = pool_offset(v, layer, page, kvh, off);
-            const uint32_t dk = smem_u32(kv_s + buf * 2 * STAGE_ELEMS + c * rows_per_copy * D);
-            bulk_copy_g2s(dk, kreg + src, bytes, fb);
-            bulk_copy_g2s(dk + STAGE_ELEMS * 2, v.v + src, bytes, fb);
+            if constexpr (KV8) {  // fp8 keys, fp8 values (one byte per element) and the rows' scales
+              const uint32_t dk = smem_u32(smem + buf * STAGE_BYTES + c * rows_per_copy * D);
+              bulk_copy_g2s(dk, reinterpret_cast<const uint8_t*>(kreg) + src, bytes, fb);
+              bulk_copy_g2s(dk + STAGE_ELEMS, reinterpret_cast<const uint8_t*>(v.v) + src, bytes, fb);
+              bulk_copy_g2s(smem_u32(smem + buf * STAGE_BYTES + 2 * STAGE_ELEMS + c * rows_per_copy * 8),
+                            v.kv_scale + src / D, static_cast<uint32_t>(rows_per_copy) * 8, fb);
+            } else {
+              const uint32_t dk = smem_u32(kv_s + buf * 2 * STAGE_ELEMS + c * rows_per_copy * D);
+              bulk_copy_g2s(dk, kreg + src, bytes, fb);
+              bulk_copy_g2s(dk + STAGE_ELEMS * 2, v.v + src, bytes, fb);
+            }
           }
         }
       };
@@ -595,7 +701,12 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
       for (int t = 0; t < nq && n_st > 0; ++t) {
         const int slot = new_slot(first, t, dsc.ring);
         const int i = (slot / kKS - rot + n_st) % n_st;
-        if (i >= st0 && i < st0 + args.stages_per_split) append_token<D>(args, dsc, un, t, slot, lane);
+        if (i >= st0 && i < st0 + args.stages_per_split) {
+          if constexpr (KV8)
+            append_token_e4m3<D>(args, dsc, un, t, slot, lane);
+          else
+            append_token<D>(args, dsc, un, t, slot, lane);
+        }
       }
       fence_proxy_async_global();  // the rows precede the producer's bulk copies
       __syncwarp();
@@ -707,12 +818,48 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
           break;
         }
         const int slot_base = (FUSE ? sb : (st0 + i) * kKS) + wt * 16;
-        const uint32_t kb = smem_u32(kv_s + buf * 2 * STAGE_ELEMS);
+        const uint32_t kb = smem_u32(KV8 ? exp_s : kv_s + buf * 2 * STAGE_ELEMS);
         const uint32_t vb = kb + STAGE_ELEMS * 2;
         if (slot_base >= nslots) {  // none of this warp's slots holds a token
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&empty_bar[buf]));
           continue;
+        }
+        // fp8 store: the warp expands its 16 rows of codes into the 16-bit stage (keys as fp16,
+        // values as bf16, both exact; two lanes a row), takes its two keys' scales, and frees the
+        // ring slot at once.  Scores are scaled by the key's 2^e, softmax weights by the value's.
+        float sk[2] = {1.f, 1.f}, sv[2] = {1.f, 1.f};
+        if constexpr (KV8) {
+          const uint8_t* st8 = smem + buf * STAGE_BYTES;
+          constexpr int PER = D / 32;  // 16-byte chunks of codes per lane
+          const int r = wt * 16 + (lane >> 1);
+          __syncwarp();  // the previous stage's fragment loads of these rows are done
+#pragma unroll
+          for (int j = 0; j < PER; ++j) {
+            const int c = (lane & 1) * PER + j;  // codes 16c .. 16c + 15 = 16-bit chunks 2c, 2c + 1
+            const uint4 kq = *reinterpret_cast<const uint4*>(st8 + r * D + c * 16);
+            const uint4 vq = *reinterpret_cast<const uint4*>(st8 + STAGE_ELEMS + r * D + c * 16);
+            const uint4 k0 = make_uint4(e4m3x2_to_f16x2(kq.x & 0xFFFFu), e4m3x2_to_f16x2(kq.x >> 16),
+                                        e4m3x2_to_f16x2(kq.y & 0xFFFFu), e4m3x2_to_f16x2(kq.y >> 16));
+            const uint4 k1 = make_uint4(e4m3x2_to_f16x2(kq.z & 0xFFFFu), e4m3x2_to_f16x2(kq.z >> 16),
+                                        e4m3x2_to_f16x2(kq.w & 0xFFFFu), e4m3x2_to_f16x2(kq.w >> 16));
+            const uint4 v0 = make_uint4(e4m3x2_to_bf16x2(vq.x & 0xFFFFu), e4m3x2_to_bf16x2(vq.x >> 16),
+                                        e4m3x2_to_bf16x2(vq.y & 0xFFFFu), e4m3x2_to_bf16x2(vq.y >> 16));
+            const uint4 v1 = make_uint4(e4m3x2_to_bf16x2(vq.z & 0xFFFFu), e4m3x2_to_bf16x2(vq.z >> 16),
+                                        e4m3x2_to_bf16x2(vq.w & 0xFFFFu), e4m3x2_to_bf16x2(vq.w >> 16));
+            *reinterpret_cast<uint4*>(exp_s + r * D + swizzle_chunk(2 * c, r) * 8) = k0;
+            *reinterpret_cast<uint4*>(exp_s + r * D + swizzle_chunk(2 * c + 1, r) * 8) = k1;
+            *reinterpret_cast<uint4*>(exp_s + STAGE_ELEMS + r * D + swizzle_chunk(2 * c, r) * 8) = v0;
+            *reinterpret_cast<uint4*>(exp_s + STAGE_ELEMS + r * D + swizzle_chunk(2 * c + 1, r) * 8) = v1;
+          }
+          const float2* sc = reinterpret_cast<const float2*>(st8 + 2 * STAGE_ELEMS);
+          const float2 s0 = sc[wt * 16 + g], s1 = sc[wt * 16 + g + 8];
+          sk[0] = s0.x;
+          sv[0] = s0.y;
+          sk[1] = s1.x;
+          sv[1] = s1.y;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&empty_bar[buf]));
         }
         // window index (token - evicted) of this thread's two keys; -1 = empty slot
         int widx[2];
@@ -778,8 +925,10 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
         uint32_t vf[KSTEPS][4];
 #pragma unroll
         for (int mt = 0; mt < KSTEPS; ++mt) ldsm_x4_t(vb + vrow * D * 2 + (swizzle_chunk(2 * mt + vchunk, ri) << 4), vf[mt]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty_bar[buf]));
+        if constexpr (!KV8) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&empty_bar[buf]));
+        }
         // online softmax; C layout: e = 0,1 key g rows 2tq, 2tq+1; e = 2,3 key g+8.  A chunk
         // whose slots all hold tokens that every query of the step sees needs no mask (one query
         // and every written slot in the window: no test needed).
@@ -797,7 +946,7 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
             const int row = nt * 8 + 2 * tq + (e & 1);
             // causal inside the step: query t sees window index <= first_new + t
             const bool ok = full_chunk || (wi >= 0 && wi <= first_new + min(row / group, nq - 1));
-            s[e] = ok ? sh[nt][e] + sl[nt][e] : -CUDART_INF_F;
+            s[e] = ok ? (sh[nt][e] + sl[nt][e]) * sk[e >> 1] : -CUDART_INF_F;
           }
           float p[4];
 #pragma unroll
@@ -814,8 +963,8 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
             l_run[nt][c] = l_run[nt][c] * alpha[nt][c] + p[c] + p[c + 2];
             m_run[nt][c] = m_new;
           }
-          pb[nt][0] = movmatrix_t(pack_bf16(p[0], p[1]));
-          pb[nt][1] = movmatrix_t(pack_bf16(p[2], p[3]));
+          pb[nt][0] = movmatrix_t(pack_bf16(p[0] * sv[0], p[1] * sv[0]));
+          pb[nt][1] = movmatrix_t(pack_bf16(p[2] * sv[1], p[3] * sv[1]));
         }
         // rescale the accumulators only when some row's running max moved in this warp
         bool moved = false;
@@ -1021,8 +1170,9 @@ __global__ void __launch_bounds__(128) merge_kernel(DevView v, int splits, uint1
   if (lse && threadIdx.x == 0) lse[blockIdx.x] = (mx + log2f(lsum)) * 0.69314718055994531f;
 }
 
-template <int D, int NT, bool ON_READ, bool FUSE>
+template <int D, int NT, bool ON_READ, bool FUSE, bool KV8>
 struct Kernel {
+  static constexpr int kSmem = smem_bytes_for<D, NT, KV8>();
   // The dynamic shared-memory opt-in is per device, so it and the occupancy it gives are
   // set up once for every device the process uses.
   static int occupancy() {
@@ -1033,11 +1183,10 @@ struct Kernel {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
     std::lock_guard<std::mutex> lock(mu);
     if (occ[dev] == 0) {
-      cudaFuncSetAttribute(attn_kernel<D, NT, ON_READ, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           smem_bytes<D, NT>());
+      cudaFuncSetAttribute(attn_kernel<D, NT, ON_READ, FUSE, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
       int o = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, attn_kernel<D, NT, ON_READ, FUSE>, threads_of<FUSE>(),
-                                                        smem_bytes<D, NT>()) != cudaSuccess)
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, attn_kernel<D, NT, ON_READ, FUSE, KV8>, threads_of<FUSE>(),
+                                                        kSmem) != cudaSuccess)
         o = 1;
       occ[dev] = o < 1 ? 1 : o;
     }
@@ -1048,7 +1197,7 @@ struct Kernel {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(threads_of<FUSE>());
-    cfg.dynamicSmemBytes = smem_bytes<D, NT>();
+    cfg.dynamicSmemBytes = kSmem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     cfg.attrs = attr;
@@ -1062,28 +1211,43 @@ struct Kernel {
       attr[1].val.clusterDim.z = 1;
       cfg.numAttrs = 2;
     }
-    return cudaLaunchKernelEx(&cfg, attn_kernel<D, NT, ON_READ, FUSE>, args);
+    return cudaLaunchKernelEx(&cfg, attn_kernel<D, NT, ON_READ, FUSE, KV8>, args);
   }
 };
 
 template <int D, int NT>
-int occupancy_of(bool on_read) {
-  return on_read ? Kernel<D, NT, true, false>::occupancy() : Kernel<D, NT, false, false>::occupancy();
+int occupancy_of(bool on_read, bool kv8) {
+  if constexpr (NT == 1) {
+    if (kv8) return on_read ? Kernel<D, 1, true, false, true>::occupancy() : Kernel<D, 1, false, false, true>::occupancy();
+  }
+  return on_read ? Kernel<D, NT, true, false, false>::occupancy() : Kernel<D, NT, false, false, false>::occupancy();
 }
 
 int occupancy_for(const DevView& v) {
   const bool two = v.n_q_heads / v.n_kv_heads * v.q_per_step > 8;
-  const bool on_read = v.scheme == RKV_SCHEME_EXACT_ON_READ;
-  if (v.head_dim == 128) return two ? occupancy_of<128, 2>(on_read) : occupancy_of<128, 1>(on_read);
-  return two ? occupancy_of<64, 2>(on_read) : occupancy_of<64, 1>(on_read);
+  const bool on_read = v.scheme == RKV_SCHEME_EXACT_ON_READ, kv8 = v.kv_scale != nullptr;
+  if (v.head_dim == 128) return two ? occupancy_of<128, 2>(on_read, kv8) : occupancy_of<128, 1>(on_read, kv8);
+  return two ? occupancy_of<64, 2>(on_read, kv8) : occupancy_of<64, 1>(on_read, kv8);
+}
+
+template <int D, int NT, bool KV8>
+cudaError_t dispatch_fused(const AttnArgs& args, int grid, cudaStream_t st) {
+  const bool fuse = args.k_new != nullptr;
+  if (args.v.scheme == RKV_SCHEME_EXACT_ON_READ)
+    return fuse ? Kernel<D, NT, true, true, KV8>::launch(args, grid, st)
+                : Kernel<D, NT, true, false, KV8>::launch(args, grid, st);
+  return fuse ? Kernel<D, NT, false, true, KV8>::launch(args, grid, st)
+              : Kernel<D, NT, false, false, KV8>::launch(args, grid, st);
 }
 
 template <int D, int NT>
 cudaError_t dispatch_on_read(const AttnArgs& args, int grid, cudaStream_t st) {
-  const bool fuse = args.k_new != nullptr;
-  if (args.v.scheme == RKV_SCHEME_EXACT_ON_READ)
-    return fuse ? Kernel<D, NT, true, true>::launch(args, grid, st) : Kernel<D, NT, true, false>::launch(args, grid, st);
-  return fuse ? Kernel<D, NT, false, true>::launch(args, grid, st) : Kernel<D, NT, false, false>::launch(args, grid, st);
+  if constexpr (NT == 1) {
+    if (args.v.kv_scale) return dispatch_fused<D, 1, true>(args, grid, st);
+  } else {
+    if (args.v.kv_scale) return cudaErrorInvalidValue;  // the fp8 store takes up to 8 query rows a kv head
+  }
+  return dispatch_fused<D, NT, false>(args, grid, st);
 }
 
 cudaError_t dispatch(const AttnArgs& args, int grid, cudaStream_t st) {

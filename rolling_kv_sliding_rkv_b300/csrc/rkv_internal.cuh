@@ -158,6 +158,47 @@ __device__ __forceinline__ float f16_to_f32(uint16_t b) { return __half2float(__
 // largest finite fp16 value after rounding: |x| >= 65520 rounds to infinity
 __device__ __forceinline__ bool fits_f16(float x) { return fabsf(x) < 65520.0f; }
 
+// ---- fp8 store (kv_format e4m3): rows of d elements, each with a power-of-two scale 2^e, e the
+// smallest integer for which max|x| / 2^e <= 448 (the largest finite e4m3 magnitude, 1.75 * 2^8):
+// with max|x| = f * 2^E, f in [0.5, 1), that is E - 9 when f <= 0.875 and E - 8 otherwise.  A row
+// of zeros takes e = 0; e stays >= -126 so that 2^e is a normal float.
+__device__ __forceinline__ int e4m3_row_exponent(float amax) {
+  if (!(amax > 0.f)) return 0;
+  int big_e;
+  const float f = frexpf(amax, &big_e);
+  const int e = f <= 0.875f ? big_e - 9 : big_e - 8;
+  return e < -126 ? -126 : e;
+}
+__device__ __forceinline__ float exp2_int(int e) { return __int_as_float((e + 127) << 23); }  // e in [-126, 127]
+
+// two fp32 (already divided by the row's 2^e, so within +-448) to e4m3, nearest even: x0 in the
+// low byte, x1 in the high byte
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float x0, float x1) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(x1), "f"(x0));
+  return r;
+}
+// two e4m3 (low byte first) to fp16x2 (low half first), exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t b) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(b));
+  return r;
+}
+// two e4m3 to bf16x2, exact (every e4m3 value is a bf16 value)
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t b) {
+  const uint32_t h = e4m3x2_to_f16x2(b);
+  const float lo = __half2float(__ushort_as_half(static_cast<uint16_t>(h & 0xFFFFu)));
+  const float hi = __half2float(__ushort_as_half(static_cast<uint16_t>(h >> 16)));
+  return (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
+}
+// eight fp32 divided by 2^e to eight e4m3 bytes (element 0 in the lowest byte)
+__device__ __forceinline__ uint2 quantize8(const float (&x)[8], float inv_scale) {
+  uint32_t w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) w[j] = f32x2_to_e4m3x2(x[2 * j] * inv_scale, x[2 * j + 1] * inv_scale);
+  return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+}
+
 // element offset of (layer, physical page, kv head, offset in page) in a pool region
 __device__ __forceinline__ int64_t pool_offset(const DevView& v, int layer, int page, int kvh, int off) {
   return static_cast<int64_t>(layer) * v.layer_stride +

@@ -40,6 +40,7 @@ class Workload:
     ragged_fill: bool = False
     rebase_interval: int = 1
     window_slack: int = 0     # ring capacity beyond the window (eviction in batches); 0: every step
+    kv_format: int = 0        # 0: fp16 keys / bf16 values; 1: the fp8 (e4m3) store
     extra: dict = field(default_factory=dict)
 
     @property

@@ -13,7 +13,9 @@ import numpy as np
 
 import synth
 from oracle.attention import attention_step
+from oracle.fp8 import quantize_rows, rotate_fp32
 from oracle.ring import StreamRing
+from oracle.schemes import stored_key_attention_step
 
 OUT_TOL = 2e-2
 LSE_TOL = 1e-3
@@ -52,7 +54,7 @@ def run_gpu(wl: synth.Workload, n_ticks: int, want: set, streams_of_interest=Non
                       n_q_heads=wl.n_q_heads, n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim,
                       q_per_step=wl.q_per_step, scheme=wl.scheme, rebase_interval=wl.rebase_interval,
                       rope_theta=wl.rope_theta, page_size=int(wl.extra.get("page_size", 64)),
-                      window_slack=wl.window_slack)
+                      window_slack=wl.window_slack, kv_format=wl.kv_format)
     S, L, Q, hq, hkv, d = wl.n_streams, wl.n_layers, wl.q_per_step, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
     q = torch.empty(S * Q * hq * d, dtype=torch.bfloat16, device=dev)
     k = torch.empty(S * Q * hkv * d, dtype=torch.bfloat16, device=dev)
@@ -154,8 +156,16 @@ def oracle_step(wl: synth.Workload, stream: int, layer: int, n_old: int, p0: int
     qb = synth.token_tensor(wl.seed, synth.TAG_Q, stream, layer, np.arange(n_old, n_new), hq, d, sc)
     kb = synth.token_tensor(wl.seed, synth.TAG_K, stream, layer, toks, hkv, d, sc)
     vb = synth.token_tensor(wl.seed, synth.TAG_V, stream, layer, toks, hkv, d, sc)
-    return attention_step(synth.bf16_bits_to_f64(qb), synth.bf16_bits_to_f64(kb), synth.bf16_bits_to_f64(vb),
-                          toks, n_old, p0, w, 1.0 / math.sqrt(d), wl.rope_theta, first_key=first)
+    q, k, v = synth.bf16_bits_to_f64(qb), synth.bf16_bits_to_f64(kb), synth.bf16_bits_to_f64(vb)
+    if wl.kv_format == 1:
+        # the fp8 store: keys rotated at the position the scheme stores them at (P0 + j offset-only,
+        # the ring slot j mod C on read), then quantised, as are the values
+        C = w + wl.window_slack
+        spos = (lambda j: j % C) if wl.scheme == 2 else (lambda j: p0 + j)
+        return stored_key_attention_step(q, k, v, toks, n_old, w, 1.0 / math.sqrt(d), wl.rope_theta, spos,
+                                         quantize=quantize_rows, first_key=first,
+                                         rotate_keys=lambda kk, pos: rotate_fp32(kk, pos, wl.rope_theta))
+    return attention_step(q, k, v, toks, n_old, p0, w, 1.0 / math.sqrt(d), wl.rope_theta, first_key=first)
 
 
 def compare(run: Run, wl: synth.Workload):

@@ -112,9 +112,11 @@ def _drive(h, wl, steps, q, k, v, out, lse, record_stream=None):
     return rec
 
 
-@pytest.mark.parametrize("scheme,where", [(1, "device"), (2, "host"), (0, "device")])
-def test_snapshot_resumes_a_stream_exactly(scheme, where):
-    """A stream saved from one handle and loaded into another continues bit for bit."""
+@pytest.mark.parametrize("scheme,where,kv_format", [(1, "device", 0), (2, "host", 0), (0, "device", 0),
+                                                   (2, "device", 1), (0, "host", 1)])
+def test_snapshot_resumes_a_stream_exactly(scheme, where, kv_format):
+    """A stream saved from one handle and loaded into another continues bit for bit (also from
+    the fp8 store: its key, value and scale planes)."""
     import torch
 
     import rolling_kv_sliding_rkv_b300 as rkv
@@ -125,7 +127,7 @@ def test_snapshot_resumes_a_stream_exactly(scheme, where):
     def handle():
         return rkv.RollingKV(wl.windows().tolist(), wl.start_offsets().tolist(), n_layers=L, n_streams=S,
                              n_q_heads=hq, n_kv_heads=hkv, head_dim=d, q_per_step=1, scheme=scheme,
-                             rope_theta=wl.rope_theta)
+                             rope_theta=wl.rope_theta, kv_format=kv_format)
 
     q = torch.empty(S, 1, hq, d, dtype=torch.bfloat16, device="cuda")
     k = torch.empty(S, 1, hkv, d, dtype=torch.bfloat16, device="cuda")
@@ -153,7 +155,8 @@ def test_snapshot_resumes_a_stream_exactly(scheme, where):
 
     # a slot with another window cannot take the snapshot
     c = rkv.RollingKV([100, 90, 100], wl.start_offsets().tolist(), n_layers=L, n_streams=S, n_q_heads=hq,
-                      n_kv_heads=hkv, head_dim=d, q_per_step=1, scheme=scheme, rope_theta=wl.rope_theta)
+                      n_kv_heads=hkv, head_dim=d, q_per_step=1, scheme=scheme, rope_theta=wl.rope_theta,
+                      kv_format=kv_format)
     with pytest.raises(rkv.RkvError) as e:
         c.load_stream(1, snap)
     assert e.value.code == rkv.RKV_ERR_CONFIG

@@ -88,6 +88,27 @@ SMALL = {
                               200, True),
     "mixed_small_slack_on_read": ("mixed", dict(n_layers=1, n_streams=9, extra={}, scheme=2, window_slack=20),
                                   120, "fused"),
+    # the fp8 (e4m3) store, against the oracle's model of it: keys quantised after their rotation at
+    # the stored position, values quantised, power-of-two row scales
+    "tiny_offset_fp8": ("tiny", dict(n_layers=1, n_streams=3, extra={"window": 150}, scheme=0, kv_format=1,
+                                     p0_high=2 ** 41), 190),
+    "tiny_on_read_fp8": ("tiny", dict(n_layers=2, n_streams=3, extra={"window": 150}, scheme=2, kv_format=1), 190),
+    "tiny_on_read_fp8_fused": ("tiny", dict(n_layers=1, n_streams=3, extra={"window": 150}, scheme=2,
+                                            kv_format=1), 190, "fused"),
+    "tiny_offset_fp8_static": ("tiny", dict(n_layers=1, n_streams=3, extra={"window": 150}, scheme=0,
+                                            kv_format=1), 190, "static"),
+    "qwen_on_read_fp8_whole_step": ("qwen", dict(n_layers=2, n_streams=3, extra={"window": 100}, scheme=2,
+                                                 kv_format=1), 120, True),
+    "encoder_q4_fp8": ("encoder", dict(n_layers=1, n_streams=3, extra={"window": 70}, kv_format=1), 30),
+    "encoder_q4_on_read_fp8_fused": ("encoder", dict(n_layers=1, n_streams=2, extra={"window": 66}, scheme=2,
+                                                     kv_format=1), 40, "fused"),
+    "tiny_page16_fp8": ("tiny", dict(n_layers=1, n_streams=2, extra={"window": 150, "page_size": 16}, scheme=2,
+                                     kv_format=1), 190),
+    "tiny_on_read_slack_fp8": ("tiny", dict(n_layers=1, n_streams=2, extra={"window": 150}, scheme=2,
+                                            window_slack=40, kv_format=1), 230, "fused"),
+    "mixed_whole_step_fp8": ("mixed", dict(n_layers=2, n_streams=9, extra={}, scheme=2, kv_format=1), 60, True),
+    "d64_gqa4_fp8": ("tiny", dict(n_layers=1, n_streams=2, n_q_heads=8, n_kv_heads=2, head_dim=64,
+                                  extra={"window": 150}, scheme=0, kv_format=1), 190),
 }
 
 
@@ -144,6 +165,9 @@ FULL = {
     # the per-layer calls over keys stored at their ring slot
     "qwen_on_read": ("qwen", dict(scheme=2), 1000, [0, 374, 375, 376, 999], [0, 40, 63]),
     "encoder_step": ("encoder", dict(), 200, [0, 4, 744, 748, 752, 796], [0, 31], True),
+    # the fp8 store at the benchmark's shape, through rkv_step
+    "qwen_step_on_read_fp8": ("qwen", dict(scheme=2, kv_format=1), 1000, [0, 374, 375, 376, 999], [0, 17, 63],
+                              True),
     # the append fused into the per-layer attention launch (rkv_append_decode_attn): one unit per
     # CTA at the Qwen shape and on the mixed schedule; several units per CTA at 1024 streams
     "qwen_fused": ("qwen", dict(), 1000, [0, 374, 375, 376, 999], [0, 17, 40, 63], "fused"),
