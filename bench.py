@@ -68,6 +68,8 @@ def bench_workload(args, **extra):
     over = dict(extra)
     if args.scheme:
         over["scheme"] = SCHEMES[args.scheme]
+    if getattr(args, "kv_format", "f16") == "e4m3":
+        over["kv_format"] = 1
     if args.layers:
         over["n_layers"] = args.layers
     wl = synth.workload(args.workload, **over)
@@ -83,6 +85,9 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--workload", default="mixed", choices=["tiny", "qwen", "voxtral", "encoder", "mixed"])
     p.add_argument("--scheme", default=None, choices=[None, "offset", "exact", "on-read"])
+    p.add_argument("--kv-format", default="f16", choices=["f16", "e4m3"],
+                   help="key/value store: fp16 keys and bf16 values, or the optional fp8 (e4m3) store "
+                        "(lower precision: profiling and comparison runs, never the headline)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
     p.add_argument("--no-e2e", action="store_true")
@@ -118,9 +123,11 @@ def describe(wl, scheme_name):
 
 
 def algorithmic_attn_bytes(wl, lens):
-    """Bytes decode attention must move for one layer: K+V of the window, q in, out, lse."""
+    """Bytes decode attention must move for one layer: K+V of the window, q in, out, lse (the fp8
+    store: one byte per key and value element and a pair of float scales per token and kv head)."""
     Q, hq, hkv, d = wl.q_per_step, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
-    kv = sum(2 * int(n) * hkv * d * 2 for n in lens)
+    per_token = 2 * d + 8 if wl.kv_format == 1 else 2 * d * 2
+    kv = sum(int(n) * hkv * per_token for n in lens)
     return kv + len(lens) * (Q * hq * d * 2 * 2 + Q * hq * 4)
 
 
@@ -406,7 +413,7 @@ def measure(wl, args, dev, rank, world, timed=True, p0=None, attention=True, per
     starts = wl.start_offsets().tolist() if p0 is None else [int(p0)] * S
     h = rkv.RollingKV(windows.tolist(), starts, device=dev, n_layers=L, n_streams=S,
                       n_q_heads=hq, n_kv_heads=hkv, head_dim=d, q_per_step=Q, scheme=wl.scheme,
-                      rebase_interval=wl.rebase_interval, rope_theta=wl.rope_theta)
+                      rebase_interval=wl.rebase_interval, rope_theta=wl.rope_theta, kv_format=wl.kv_format)
     phases = [ph for ph in step_phases(wl)]
     # one resident input set (and one CUDA graph of a whole step) per phase; a single-phase
     # workload cycles through `--inputs` sets
@@ -716,6 +723,10 @@ def run_ours(args):
         todo = [(SCHEME_NAMES[sch], dict(over, scheme=sch)) for sch in SCHEMES.values() if sch != wl.scheme]
         if wl.scheme in (1, 2):   # chunked re-base: the materialised scheme re-basing once every 8 rolls
             todo.append(("exact re-base every 8 rolls", dict(over, scheme=1, rebase_interval=8)))
+        if wl.scheme in (0, 2) and wl.n_q_heads // wl.n_kv_heads * wl.q_per_step <= 8:
+            # the optional fp8 (e4m3) store: lower precision, so never the headline
+            todo.append((f"{SCHEME_NAMES[wl.scheme]}, fp8 (e4m3) key/value store",
+                         dict(over, scheme=wl.scheme, kv_format=1)))
         for label, vover in todo:
             vw = synth.workload(args.workload, **vover)
             vm = measure(vw, args, dev, rank, 1, timed=False, per_layer_step=args.per_layer)

@@ -80,7 +80,8 @@ typedef enum {
   RKV_ERR_TIMEOUT = -5,      /* a bounded device-side wait gave up */
   RKV_ERR_STATE = -6,        /* call out of order (see "Per-step order" above) */
   RKV_ERR_DEVICE_BOUNDS = -7, /* a kernel found an index outside its table */
-  RKV_ERR_DEVICE_RANGE = -8   /* a rotated key did not fit fp16 (|k| >= 65520) */
+  RKV_ERR_DEVICE_RANGE = -8   /* a rotated key did not fit fp16 (|k| >= 65520), or, in the fp8
+                               * store, a value row reached |v| >= 61440 (read back in fp16) */
 } rkv_status;
 
 typedef enum {

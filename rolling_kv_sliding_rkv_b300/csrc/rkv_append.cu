@@ -166,6 +166,8 @@ __global__ void __launch_bounds__(128) append_rope_e4m3_kernel(DevView v, int la
   }
   if (!live) return;
   if (!ok) record_error(v.status, DEV_RANGE, 1, cp);
+  // values are read back as fp16 code * 2^e: a row must stay clear of the fp16 limit after rounding
+  if (!(vm < 61440.f)) record_error(v.status, DEV_RANGE, 2, cp);
   const int ek = e4m3_row_exponent(km), ev = e4m3_row_exponent(vm);
   const int off = slot % v.page_size;
   const int64_t dst = pool_offset(v, layer, page, kvh, off);  // = row index * d: a byte offset here

@@ -177,15 +177,16 @@ __host__ __device__ constexpr int smem_bytes() {
 }
 
 // fp8 store: a stage is 64 rows of fp8 keys, 64 of fp8 values and 64 (key, value) scale pairs;
-// ~66 KB of stages (as many tokens in flight as 132 KB of fp16 ones), then one expanded stage
-// (K | V as 16-bit codes, the fp16 stage layout) that the consumer warps fill from each stage
+// ~50 KB of stages (as many tokens in flight as 100 KB of fp16 ones), then one expanded stage
+// (K | V in 16 bits, the fp16 stage layout) that the consumer warps fill from each stage; two
+// CTAs still fit an SM
 template <int D>
 __host__ __device__ constexpr int stage8_bytes() {
   return 2 * kKS * D + kKS * 8;
 }
 template <int D>
 __host__ __device__ constexpr int stages8_for() {
-  return D == 128 ? 4 : 8;
+  return D == 128 ? 3 : 6;
 }
 template <int D, int NT, bool KV8>
 __host__ __device__ constexpr int smem_bytes_for() {
@@ -193,7 +194,7 @@ __host__ __device__ constexpr int smem_bytes_for() {
                    2 * (8 * NT) * (D + 4) * 4
              : smem_bytes<D, NT>();
 }
-static_assert(smem_bytes_for<128, 1, true>() <= 112 * 1024 && smem_bytes_for<64, 1, true>() <= 112 * 1024,
+static_assert(smem_bytes_for<128, 1, true>() <= 100 * 1024 && smem_bytes_for<64, 1, true>() <= 100 * 1024,
               "two fp8-store CTAs per SM");
 static_assert(smem_bytes<128, 2>() <= 227 * 1024, "shared memory budget");
 
@@ -458,6 +459,8 @@ __device__ __forceinline__ void append_token_e4m3(const AttnArgs& args, const St
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) vm = fmaxf(vm, fabsf(ra[j]));
+    // read back as fp16 code * 2^e: a row must stay clear of the fp16 limit after rounding up a code
+    if (!(vm < 61440.f)) record_error(v.status, DEV_RANGE, 4, lane);
   }
 #pragma unroll
   for (int o = 1; o < D / 8; o <<= 1) {  // key groups of CP lanes and value groups of D/8, aligned
@@ -776,8 +779,10 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
             const int base = (nt * 8 + g) * QSTR + ks * 16 + 2 * tq;
             qh[nt][ks][0] = *reinterpret_cast<const uint32_t*>(th + base);
             qh[nt][ks][1] = *reinterpret_cast<const uint32_t*>(th + base + 8);
-            ql[nt][ks][0] = *reinterpret_cast<const uint32_t*>(tl + base);
-            ql[nt][ks][1] = *reinterpret_cast<const uint32_t*>(tl + base + 8);
+            if constexpr (!KV8) {
+              ql[nt][ks][0] = *reinterpret_cast<const uint32_t*>(tl + base);
+              ql[nt][ks][1] = *reinterpret_cast<const uint32_t*>(tl + base + 8);
+            }
           }
       };
       load_q(qh_s, ql_s);
@@ -825,39 +830,46 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
           if (lane == 0) mbar_arrive(smem_u32(&empty_bar[buf]));
           continue;
         }
-        // fp8 store: the warp expands its 16 rows of codes into the 16-bit stage (keys as fp16,
-        // values as bf16, both exact; two lanes a row), takes its two keys' scales, and frees the
-        // ring slot at once.  Scores are scaled by the key's 2^e, softmax weights by the value's.
-        float sk[2] = {1.f, 1.f}, sv[2] = {1.f, 1.f};
+        // fp8 store: the warp expands its 16 rows into the 16-bit stage (two lanes a row): key codes
+        // as fp16 (exact), values as fp16 code * 2^e (exact unless a row's scale is below 2^-15,
+        // where the smallest codes lose bits below 2^-24), takes its two keys' scales and frees the
+        // ring slot at once.  Scores are scaled by the key's 2^e; the values then need an fp16
+        // product with the softmax weights.
+        float sk[2] = {1.f, 1.f};
         if constexpr (KV8) {
           const uint8_t* st8 = smem + buf * STAGE_BYTES;
-          constexpr int PER = D / 32;  // 16-byte chunks of codes per lane
-          const int r = wt * 16 + (lane >> 1);
+          constexpr int C8 = D / 16;       // 16-byte chunks of codes per row
+          constexpr int RPP = 32 / C8;     // rows per pass: C8 lanes read a row's codes side by side
+          const int c = lane % C8;         // codes 16c .. 16c + 15 = 16-bit chunks 2c, 2c + 1
           __syncwarp();  // the previous stage's fragment loads of these rows are done
-#pragma unroll
-          for (int j = 0; j < PER; ++j) {
-            const int c = (lane & 1) * PER + j;  // codes 16c .. 16c + 15 = 16-bit chunks 2c, 2c + 1
+#pragma unroll 1
+          for (int j = 0; j < 16 / RPP; ++j) {  // one pass at a time: the consumers sit at the register limit
+            const int r = wt * 16 + j * RPP + lane / C8;
+            const __half2 vs2 = __float2half2_rn(reinterpret_cast<const float2*>(st8 + 2 * STAGE_ELEMS)[r].y);
+            const uint32_t vsc = *reinterpret_cast<const uint32_t*>(&vs2);
+            auto vscale = [&](uint32_t h2) {  // fp16x2 codes times the row's value scale
+              uint32_t y;
+              asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(y) : "r"(h2), "r"(vsc));
+              return y;
+            };
             const uint4 kq = *reinterpret_cast<const uint4*>(st8 + r * D + c * 16);
             const uint4 vq = *reinterpret_cast<const uint4*>(st8 + STAGE_ELEMS + r * D + c * 16);
             const uint4 k0 = make_uint4(e4m3x2_to_f16x2(kq.x & 0xFFFFu), e4m3x2_to_f16x2(kq.x >> 16),
                                         e4m3x2_to_f16x2(kq.y & 0xFFFFu), e4m3x2_to_f16x2(kq.y >> 16));
             const uint4 k1 = make_uint4(e4m3x2_to_f16x2(kq.z & 0xFFFFu), e4m3x2_to_f16x2(kq.z >> 16),
                                         e4m3x2_to_f16x2(kq.w & 0xFFFFu), e4m3x2_to_f16x2(kq.w >> 16));
-            const uint4 v0 = make_uint4(e4m3x2_to_bf16x2(vq.x & 0xFFFFu), e4m3x2_to_bf16x2(vq.x >> 16),
-                                        e4m3x2_to_bf16x2(vq.y & 0xFFFFu), e4m3x2_to_bf16x2(vq.y >> 16));
-            const uint4 v1 = make_uint4(e4m3x2_to_bf16x2(vq.z & 0xFFFFu), e4m3x2_to_bf16x2(vq.z >> 16),
-                                        e4m3x2_to_bf16x2(vq.w & 0xFFFFu), e4m3x2_to_bf16x2(vq.w >> 16));
+            const uint4 v0 = make_uint4(vscale(e4m3x2_to_f16x2(vq.x & 0xFFFFu)), vscale(e4m3x2_to_f16x2(vq.x >> 16)),
+                                        vscale(e4m3x2_to_f16x2(vq.y & 0xFFFFu)), vscale(e4m3x2_to_f16x2(vq.y >> 16)));
+            const uint4 v1 = make_uint4(vscale(e4m3x2_to_f16x2(vq.z & 0xFFFFu)), vscale(e4m3x2_to_f16x2(vq.z >> 16)),
+                                        vscale(e4m3x2_to_f16x2(vq.w & 0xFFFFu)), vscale(e4m3x2_to_f16x2(vq.w >> 16)));
             *reinterpret_cast<uint4*>(exp_s + r * D + swizzle_chunk(2 * c, r) * 8) = k0;
             *reinterpret_cast<uint4*>(exp_s + r * D + swizzle_chunk(2 * c + 1, r) * 8) = k1;
             *reinterpret_cast<uint4*>(exp_s + STAGE_ELEMS + r * D + swizzle_chunk(2 * c, r) * 8) = v0;
             *reinterpret_cast<uint4*>(exp_s + STAGE_ELEMS + r * D + swizzle_chunk(2 * c + 1, r) * 8) = v1;
           }
           const float2* sc = reinterpret_cast<const float2*>(st8 + 2 * STAGE_ELEMS);
-          const float2 s0 = sc[wt * 16 + g], s1 = sc[wt * 16 + g + 8];
-          sk[0] = s0.x;
-          sv[0] = s0.y;
-          sk[1] = s1.x;
-          sv[1] = s1.y;
+          sk[0] = sc[wt * 16 + g].x;
+          sk[1] = sc[wt * 16 + g + 8].x;
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&empty_bar[buf]));
         }
@@ -885,7 +897,9 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               mma_f16(ah[nt], kf[ks], qh[nt][ks][0], qh[nt][ks][1]);
-              mma_f16(al[nt], kf[ks], ql[nt][ks][0], ql[nt][ks][1]);
+              // the query's low part: fp32 accuracy against fp16 keys; the fp8 store's keys carry
+              // 2^-4 relative error, where the fp16 query alone (2^-11) is already far below it
+              if constexpr (!KV8) mma_f16(al[nt], kf[ks], ql[nt][ks][0], ql[nt][ks][1]);
             }
         };
         if constexpr (ON_READ) {
@@ -963,8 +977,13 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
             l_run[nt][c] = l_run[nt][c] * alpha[nt][c] + p[c] + p[c + 2];
             m_run[nt][c] = m_new;
           }
-          pb[nt][0] = movmatrix_t(pack_bf16(p[0] * sv[0], p[1] * sv[0]));
-          pb[nt][1] = movmatrix_t(pack_bf16(p[2] * sv[1], p[3] * sv[1]));
+          if constexpr (KV8) {  // fp16 weights against the fp16 values
+            pb[nt][0] = movmatrix_t(pack_f16(p[0], p[1]));
+            pb[nt][1] = movmatrix_t(pack_f16(p[2], p[3]));
+          } else {
+            pb[nt][0] = movmatrix_t(pack_bf16(p[0], p[1]));
+            pb[nt][1] = movmatrix_t(pack_bf16(p[2], p[3]));
+          }
         }
         // rescale the accumulators only when some row's running max moved in this warp
         bool moved = false;
@@ -984,7 +1003,12 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
 #pragma unroll
         for (int mt = 0; mt < KSTEPS; ++mt)
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_bf16(o_acc[mt][nt], vf[mt], pb[nt][0], pb[nt][1]);
+          for (int nt = 0; nt < NT; ++nt) {
+            if constexpr (KV8)
+              mma_f16(o_acc[mt][nt], vf[mt], pb[nt][0], pb[nt][1]);
+            else
+              mma_bf16(o_acc[mt][nt], vf[mt], pb[nt][0], pb[nt][1]);
+          }
       }
       k0 += my_st;
 
