@@ -44,18 +44,18 @@ SCHEMES = {"offset": 0, "exact": 1, "on-read": 2}
 # ncu launch-list summary of the same command, valid only while the attention source's code is the
 # one that was profiled: a different code digest (comments and white space left out) reports null.
 TRAFFIC = [
-    {"workload": "mixed", "layers": 36, "schemes": (0, 1), "attn_code_sha256_16": "6cc26d3203835adb",
-     "bytes_per_launch": 1131.08e6 + 13.66e6},   # the tick phase with the most active streams
-    {"workload": "mixed", "layers": 36, "schemes": (2,), "attn_code_sha256_16": "6cc26d3203835adb",
-     "bytes_per_launch": 1131.17e6 + 13.65e6},   # the tick phase with the most active streams
-    {"workload": "qwen", "layers": 36, "schemes": (0, 1), "attn_code_sha256_16": "6cc26d3203835adb",
-     "bytes_per_launch": 915.61e6 + 8.78e6},
-    {"workload": "qwen", "layers": 36, "schemes": (2,), "attn_code_sha256_16": "6cc26d3203835adb",
-     "bytes_per_launch": 915.69e6 + 8.83e6},
-    {"workload": "voxtral", "layers": 26, "schemes": (0,), "attn_code_sha256_16": "6cc26d3203835adb",
-     "bytes_per_launch": 13963.02e6 + 4.51e6},
-    {"workload": "encoder", "layers": 32, "schemes": (0,), "attn_code_sha256_16": "6cc26d3203835adb",
-     "bytes_per_launch": 4037.84e6 + 10.52e6},
+    {"workload": "mixed", "layers": 36, "schemes": (0, 1), "attn_code_sha256_16": "0081f47d3a673c9e",
+     "bytes_per_launch": 1131.04e6 + 13.56e6},   # the tick phase with the most active streams
+    {"workload": "mixed", "layers": 36, "schemes": (2,), "attn_code_sha256_16": "0081f47d3a673c9e",
+     "bytes_per_launch": 1131.23e6 + 13.60e6},   # the tick phase with the most active streams
+    {"workload": "qwen", "layers": 36, "schemes": (0, 1), "attn_code_sha256_16": "0081f47d3a673c9e",
+     "bytes_per_launch": 915.62e6 + 8.79e6},
+    {"workload": "qwen", "layers": 36, "schemes": (2,), "attn_code_sha256_16": "0081f47d3a673c9e",
+     "bytes_per_launch": 915.70e6 + 9.08e6},
+    {"workload": "voxtral", "layers": 26, "schemes": (0,), "attn_code_sha256_16": "0081f47d3a673c9e",
+     "bytes_per_launch": 13962.82e6 + 4.41e6},
+    {"workload": "encoder", "layers": 32, "schemes": (0,), "attn_code_sha256_16": "0081f47d3a673c9e",
+     "bytes_per_launch": 4037.85e6 + 10.54e6},
 ]
 SCHEME_NAMES = {0: "offset-only", 1: "exact re-base", 2: "exact re-base applied on read"}
 
