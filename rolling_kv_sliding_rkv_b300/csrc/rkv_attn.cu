@@ -37,6 +37,12 @@
 // combine their (m, l, O) through distributed shared memory; the scratch
 // form writes per-split partials to global memory for a separate merge.
 // Every sum runs in a fixed order, so outputs are reproducible run to run.
+//
+// With the append fused (rkv_append_decode_attn), a sixth warp writes the
+// step's new keys and values into the pool while the others stream the
+// window's older stages, which a unit's walk takes first.  With the optional
+// fp8 store, stages hold e4m3 codes and their rows' scales; each consumer
+// warp expands its 16 rows into a 16-bit stage before the fragment loads.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
