@@ -148,3 +148,27 @@ def test_stream_state_check(scheme, interval, q, slack):
     for bad in ([0, 0, 0, -1, 0, 0, w, -1], [0, 0, 0, 2 ** 52, 0, 0, w, 2 ** 52]):   # P0 outside [0, 2^52)
         with pytest.raises(rkv.RkvError):
             rkv.rkv_check_stream_state(cfg, bad)
+
+
+@pytest.mark.parametrize("struct", ["rkv_config", "rkv_clock"])
+def test_struct_layout_matches_the_header(tmp_path, struct):
+    """The ctypes mirrors of the ABI's structs have the C structs' sizes and field offsets (gcc)."""
+    import ctypes
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    cls = getattr(rkv._abi, struct)
+    fields = [f for f, _ in cls._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "rkv.h"\nint main(void) {\n'
+                   f'  printf("%zu\\n", sizeof({struct}));\n' +
+                   "".join(f'  printf("%zu\\n", offsetof({struct}, {f}));\n' for f in fields) +
+                   "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([gcc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(cls)
+    assert got[1:] == [getattr(cls, f).offset for f in fields]
