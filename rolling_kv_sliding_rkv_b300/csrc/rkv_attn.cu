@@ -237,16 +237,25 @@ __device__ __forceinline__ Unit unit_of(int u, int n_active, int hkv) {
 // capacity above the window (window_slack > 0) some of them hold evicted tokens: masked.
 __device__ __forceinline__ int slots_in_use(const StepDesc& d) { return d.evicted > 0 ? d.ring : d.len; }
 
-// Query prefetch of one consumer thread: pair cp of row r (chunks cp and cp + D/16).
+// Query prefetch of one consumer thread, pair cp of row r (chunks cp and cp + D/16), and, on
+// read, element tid of the unit's (cos, sin)(-C omega) row.  The cos/sin of the pair's eight
+// frequencies go to registers.  The raw bf16 chunks and the lap element go either to registers
+// too, or (STAGED) by cp.async into the thread's own slots of the CTA's raw-query rows and into
+// lap_dst, so that those registers are not tied up while the current unit streams: the consumers
+// sit at the register limit of two CTAs per SM, and the re-base applied on read, whose lap switch
+// needs the most, runs faster staged (the other kernels measured faster without).  The issuing
+// thread reads its chunks back after cp_async_wait_all; other threads read the lap row after the
+// next barrier.
 template <int D>
 struct QPrefetch {
-  uint4 xa, xb;
+  uint4 xa, xb;  // register form only
   float4 cs[4];
-  float lap;  // on read: element tid of the unit's (cos, sin)(-C omega) row
+  float lap;     // register form only
 };
 
-template <int D>
-__device__ __forceinline__ void q_prefetch(const AttnArgs& args, const Unit& un, int tid, QPrefetch<D>& pf) {
+template <int D, bool STAGED>
+__device__ __forceinline__ void q_prefetch(const AttnArgs& args, const Unit& un, int tid, QPrefetch<D>& pf,
+                                           uint16_t* qraw_s, float* lap_dst) {
   constexpr int CP = D / 16, H = D / 2;
   const DevView& v = args.v;
   const int r = tid / CP, cp = tid % CP;
@@ -255,27 +264,46 @@ __device__ __forceinline__ void q_prefetch(const AttnArgs& args, const Unit& un,
     const int t = r / group, h = un.kvh * group + r % group;
     const uint16_t* x =
         args.q + un.lz * args.q_layer_stride + ((static_cast<int64_t>(un.a) * nq + t) * v.n_q_heads + h) * D;
-    pf.xa = *reinterpret_cast<const uint4*>(x + cp * 8);
-    pf.xb = *reinterpret_cast<const uint4*>(x + H + cp * 8);
+    if constexpr (STAGED) {
+      cp_async16(qraw_s + r * D + cp * 8, x + cp * 8);
+      cp_async16(qraw_s + r * D + H + cp * 8, x + H + cp * 8);
+    } else {
+      pf.xa = *reinterpret_cast<const uint4*>(x + cp * 8);
+      pf.xb = *reinterpret_cast<const uint4*>(x + H + cp * 8);
+    }
     const float4* cs = reinterpret_cast<const float4*>(v.cs_q + ((static_cast<int64_t>(un.a) * nq + t) * H + cp * 8) * 2);
 #pragma unroll
     for (int j = 0; j < 4; ++j) pf.cs[j] = cs[j];
   } else {
-    pf.xa = pf.xb = make_uint4(0, 0, 0, 0);
+    if constexpr (!STAGED) pf.xa = pf.xb = make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int j = 0; j < 4; ++j) pf.cs[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  pf.lap = v.cs_lap && tid < D ? v.cs_lap[static_cast<int64_t>(un.a) * D + tid] : 0.f;
+  if constexpr (STAGED) {
+    if (lap_dst && tid < D) cp_async4(lap_dst + tid, v.cs_lap + static_cast<int64_t>(un.a) * D + tid);
+  } else {
+    pf.lap = v.cs_lap && tid < D ? v.cs_lap[static_cast<int64_t>(un.a) * D + tid] : 0.f;
+  }
 }
 
-// Rotate, scale to log2 units and split into fp16 hi + lo; write the tiles.
-template <int D, int NT>
+// Rotate, scale to log2 units and split into fp16 hi + lo; write the tiles (rows from rows_live
+// on are zero).  STAGED: the caller has waited for its own cp.async copies.
+template <int D, int NT, bool STAGED>
 __device__ __forceinline__ void q_build(const QPrefetch<D>& pf, float scale_log2, int tid, uint16_t* qh_s,
-                                        uint16_t* ql_s) {
+                                        uint16_t* ql_s, const uint16_t* qraw_s, int rows_live) {
   constexpr int CP = D / 16, H = D / 2, QSTR = D + 8;
   const int r = tid / CP, cp = tid % CP;
   if (r >= 8 * NT) return;
-  const uint32_t wa[4] = {pf.xa.x, pf.xa.y, pf.xa.z, pf.xa.w}, wb[4] = {pf.xb.x, pf.xb.y, pf.xb.z, pf.xb.w};
+  uint4 xa, xb;
+  if constexpr (STAGED) {
+    const bool live = r < rows_live;
+    xa = live ? *reinterpret_cast<const uint4*>(qraw_s + r * D + cp * 8) : make_uint4(0, 0, 0, 0);
+    xb = live ? *reinterpret_cast<const uint4*>(qraw_s + r * D + H + cp * 8) : make_uint4(0, 0, 0, 0);
+  } else {
+    xa = pf.xa;
+    xb = pf.xb;
+  }
+  const uint32_t wa[4] = {xa.x, xa.y, xa.z, xa.w}, wb[4] = {xb.x, xb.y, xb.z, xb.w};
   const float* cs = reinterpret_cast<const float*>(pf.cs);
   uint32_t ha[4], hb[4], la[4], lb[4];
 #pragma unroll
@@ -519,6 +547,9 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
   __shared__ float row_m[ROWS], row_l[ROWS];
   __shared__ int abort_flag, poisoned_s;
   __shared__ __align__(16) float lap_s[ON_READ ? D : 4];  // (cos, sin)(-C omega_i) of the unit's stream
+  // the raw query of the next unit lands in shared memory (cp.async) on read, in registers otherwise
+  constexpr bool STAGED = ON_READ && !FUSE;
+  __shared__ __align__(16) uint16_t qraw_s[STAGED ? 8 * NT * D : 8];  // the unit's query rows as given
 
   const DevView& v = args.v;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -737,13 +768,13 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
     if (u_first < n_units) {
       const Unit un0 = unit_of(u_first, n_active, hkv);
       if (desc_early) dnext = v.desc[un0.a];
-      if (desc_early && q_early) q_prefetch<D>(args, un0, tid, pf);
+      if (desc_early && q_early) q_prefetch<D, STAGED>(args, un0, tid, pf, qraw_s, ON_READ ? lap_s : nullptr);
     }
     pdl_wait();
     if (u_first < n_units) {
       const Unit un0 = unit_of(u_first, n_active, hkv);
       if (!desc_early) dnext = v.desc[un0.a];
-      if (!(desc_early && q_early)) q_prefetch<D>(args, un0, tid, pf);
+      if (!(desc_early && q_early)) q_prefetch<D, STAGED>(args, un0, tid, pf, qraw_s, ON_READ ? lap_s : nullptr);
     }
     int k0 = 0;  // ring position of the unit's first stage
     for (int u = u_first; u < n_units; u += u_step) {
@@ -761,8 +792,9 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
         sb = (st >= n_st ? st - n_st : st) * kKS;
       }
 
-      q_build<D, NT>(pf, v.scale_log2, tid, qh_s, ql_s);
-      if constexpr (ON_READ) {
+      if constexpr (STAGED) cp_async_wait_all();  // own raw query chunks, lap element (S1 publishes it)
+      q_build<D, NT, STAGED>(pf, v.scale_log2, tid, qh_s, ql_s, qraw_s, rows);
+      if constexpr (ON_READ && !STAGED) {
         if (tid < D) lap_s[tid] = pf.lap;
       }
       consumer_sync();  // S1: query tiles ready; the previous unit's output pass is over
@@ -796,7 +828,8 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
       bool lap_b = false;
       if (u + u_step < n_units) {  // the next unit's query and descriptor land during this unit
         const Unit un1 = unit_of(u + u_step, n_active, hkv);
-        q_prefetch<D>(args, un1, tid, pf);
+        // lap_s is free: this unit's next-lap tile is built (S1b), or was not needed
+        q_prefetch<D, STAGED>(args, un1, tid, pf, qraw_s, ON_READ ? lap_s : nullptr);
         dnext = v.desc[un1.a];
       }
 
