@@ -1148,6 +1148,8 @@ __global__ void __launch_bounds__(threads_of<FUSE>(), NT == 1 ? 2 : 1) attn_kern
         }
       }
     }
+    // a unit loop left early (a wait gave up) may leave the next unit's staged copies in flight
+    if constexpr (STAGED) cp_async_wait_all();
   }
 
   if (args.mode == 1) {
