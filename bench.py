@@ -44,18 +44,18 @@ SCHEMES = {"offset": 0, "exact": 1, "on-read": 2}
 # ncu launch-list summary of the same command, valid only while the attention source's code is the
 # one that was profiled: a different code digest (comments and white space left out) reports null.
 TRAFFIC = [
-    {"workload": "mixed", "layers": 36, "schemes": (0, 1), "attn_code_sha256_16": "1c6ff75ea20c51d1",
-     "bytes_per_launch": 1131.04e6 + 13.58e6},   # the tick phase with the most active streams
-    {"workload": "mixed", "layers": 36, "schemes": (2,), "attn_code_sha256_16": "1c6ff75ea20c51d1",
-     "bytes_per_launch": 1131.27e6 + 13.31e6},   # the tick phase with the most active streams
-    {"workload": "qwen", "layers": 36, "schemes": (0, 1), "attn_code_sha256_16": "1c6ff75ea20c51d1",
-     "bytes_per_launch": 915.61e6 + 8.49e6},
-    {"workload": "qwen", "layers": 36, "schemes": (2,), "attn_code_sha256_16": "1c6ff75ea20c51d1",
-     "bytes_per_launch": 915.74e6 + 8.30e6},
-    {"workload": "voxtral", "layers": 26, "schemes": (0,), "attn_code_sha256_16": "1c6ff75ea20c51d1",
-     "bytes_per_launch": 13963.00e6 + 4.12e6},
-    {"workload": "encoder", "layers": 32, "schemes": (0,), "attn_code_sha256_16": "1c6ff75ea20c51d1",
-     "bytes_per_launch": 4037.88e6 + 10.52e6},
+    {"workload": "mixed", "layers": 36, "schemes": (0, 1), "attn_code_sha256_16": "d10556389b5bee13",
+     "bytes_per_launch": 1131.00e6 + 13.58e6},   # the tick phase with the most active streams
+    {"workload": "mixed", "layers": 36, "schemes": (2,), "attn_code_sha256_16": "d10556389b5bee13",
+     "bytes_per_launch": 1131.25e6 + 13.41e6},   # the tick phase with the most active streams
+    {"workload": "qwen", "layers": 36, "schemes": (0, 1), "attn_code_sha256_16": "d10556389b5bee13",
+     "bytes_per_launch": 915.69e6 + 8.37e6},
+    {"workload": "qwen", "layers": 36, "schemes": (2,), "attn_code_sha256_16": "d10556389b5bee13",
+     "bytes_per_launch": 915.77e6 + 8.11e6},
+    {"workload": "voxtral", "layers": 26, "schemes": (0,), "attn_code_sha256_16": "d10556389b5bee13",
+     "bytes_per_launch": 13962.88e6 + 3.72e6},
+    {"workload": "encoder", "layers": 32, "schemes": (0,), "attn_code_sha256_16": "d10556389b5bee13",
+     "bytes_per_launch": 4037.93e6 + 10.59e6},
 ]
 SCHEME_NAMES = {0: "offset-only", 1: "exact re-base", 2: "exact re-base applied on read"}
 
