@@ -53,21 +53,24 @@ def _handle(rkv, wl):
     ("static", 0),         # the scratch form: per-split partials and a merge kernel
     ("fused", 0),          # the append fused into the launch: the appender warp still writes the tokens
     ("whole_step", 4),     # many units: persistent CTAs, the stage withheld in a CTA's second unit
+    ("whole_step_on_read", 4),  # the same over keys at their ring slot (next unit's query staged)
 ])
 def test_bounded_wait_runs_out_and_the_handle_recovers(path, withhold):
     import torch
 
     import rolling_kv_sliding_rkv_b300 as rkv
 
-    n_streams = 64 if path == "whole_step" else 3
-    wl = synth.workload("tiny", n_layers=3, n_streams=n_streams, extra={"window": 150}, scheme=1)
+    whole = path.startswith("whole_step")
+    n_streams = 64 if whole else 3
+    wl = synth.workload("tiny", n_layers=3, n_streams=n_streams, extra={"window": 150},
+                        scheme=2 if path.endswith("on_read") else 1)
     S, L = wl.n_streams, wl.n_layers
     h = _handle(rkv, wl)
     q, k, v, out, lse = _bufs(wl, L)
     active = list(range(S))
 
     def step(n_old, fail_layer=None):
-        if path == "whole_step":
+        if whole:
             h.gen_next_inputs(wl.seed, active, wl.input_scale, q, k, v)
             h.step(active, q, k, v, out, lse)
             return
@@ -99,7 +102,7 @@ def test_bounded_wait_runs_out_and_the_handle_recovers(path, withhold):
     torch.cuda.synchronize()
 
     t0 = time.perf_counter()
-    if path == "whole_step":
+    if whole:
         rkv.rkv_set_wait_test(h.handle, withhold, WAIT_NS)
         step(n)
         rkv.rkv_set_wait_test(h.handle, -1, 0)
