@@ -774,6 +774,14 @@ def run_ours(args):
             subs[name]["free_bytes_delta_over_timed_steps"] = sm["free_bytes_delta"]
             if name == "qwen" and args.flatness:
                 subs[name]["flatness"] = flatness(sw, sm["free_bytes_delta"])
+        # the mixed-clock batch read the other way: every one of the 256 streams steps on every call
+        # (no scheduler tick), 2.56 GB of windows per step
+        import dataclasses
+        sw = dataclasses.replace(wl, name="mixed_all_streams", tick_ms=0)
+        sm = measure(sw, args, dev, rank, 1, timed=False, per_layer_step=args.per_layer)
+        sm.pop("h").close()
+        subs["mixed_all_streams"] = workload_figures(sw, SCHEME_NAMES[sw.scheme], sm, peak, peak_kind, args.steps, 1)
+        subs["mixed_all_streams"]["free_bytes_delta_over_timed_steps"] = sm["free_bytes_delta"]
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

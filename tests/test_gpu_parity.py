@@ -162,6 +162,8 @@ FULL = {
     "mixed_step": ("mixed", dict(), 510, "schedule", [0, 1, 2, 3], True),
     # the benchmark's headline: the same ticks with the exact re-base applied on read
     "mixed_step_on_read": ("mixed", dict(scheme=2), 510, "schedule", [0, 1, 2, 3, 4], True),
+    # the same batch read the other way: all 256 streams step on every call (no scheduler tick)
+    "mixed_all_streams_step_on_read": ("mixed", dict(scheme=2, tick_ms=0), 400, "schedule", [0, 1, 2, 3], True),
     # the per-layer calls over keys stored at their ring slot
     "qwen_on_read": ("qwen", dict(scheme=2), 1000, [0, 374, 375, 376, 999], [0, 40, 63]),
     "encoder_step": ("encoder", dict(), 200, [0, 4, 744, 748, 752, 796], [0, 31], True),
