@@ -92,6 +92,19 @@ def test_code_digest_ignores_comments_and_layout_only(tmp_path):
     assert bench.profiled_traffic(wl) is None
 
 
+def test_traffic_table_is_for_the_current_attention_source():
+    """The committed DRAM-traffic figures are those of the attention source as it stands: a change
+    to its code must come with a new launch-list capture (else the bench line reports null)."""
+    digest = bench.code_digest(os.path.join(ROOT, "rolling_kv_sliding_rkv_b300", "csrc", "rkv_attn.cu"))
+    assert {t["attn_code_sha256_16"] for t in bench.TRAFFIC} == {digest}
+    for name, scheme in (("mixed", 2), ("qwen", 2), ("qwen", 1), ("voxtral", 0), ("encoder", 0)):
+        t = bench.profiled_traffic(synth.workload(name, scheme=scheme))
+        lens = [int(w) for w in synth.workload(name).windows()]
+        algo = bench.algorithmic_attn_bytes(synth.workload(name), lens) * synth.workload(name).n_layers
+        if name != "mixed":   # every stream active: within a few % above the algorithmic bytes
+            assert algo <= t <= 1.05 * algo, (name, t, algo)
+
+
 def test_reference_arm_prints_one_line():
     out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--steps", "1",
                           "--warmup", "0"], cwd=ROOT, capture_output=True, text=True, timeout=600)
