@@ -663,7 +663,7 @@ def workload_figures(wl, scheme_name, m, peak, peak_kind, steps, world):
 
 def bench_line(wl, scheme_name, args, world, m, peak, peak_kind, variants=None, flat=None, e2e=None, cpu=None,
                subs=None):
-    """The one JSON line of a run: the driver's contract keys plus the roofline of the dominant kernel."""
+    """The one JSON line of a run: the keys of the benchmark contract plus the roofline of the dominant kernel."""
     fig = workload_figures(wl, scheme_name, m, peak, peak_kind, args.steps, world)
     line = {"metric": METRIC, "value": fig["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": fig["ms_per_step"], "higher_is_better": True,

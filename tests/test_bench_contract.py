@@ -1,4 +1,4 @@
-"""bench.py's JSON line: the keys and arithmetic the benchmark driver relies on (no GPU needed)."""
+"""bench.py's JSON line: the contract keys and the roofline arithmetic (no GPU needed)."""
 import json
 import os
 import subprocess
