@@ -46,12 +46,15 @@
  *
  * Memory in HBM (pool_dev).  Regions of [L][pages][Hkv][page_size][d]
  * 16-bit elements: rotated keys (fp16), values (bf16), and in
- * RKV_SCHEME_EXACT_REBASE pre-RoPE keys (bf16).  Stream s
- * owns ceil(W_s / page_size) pages; token j lives in ring slot j mod W_s, so
- * eviction moves no data.  Within a row of d elements the 16-byte chunk c
- * sits at chunk position c ^ (row offset in the page & 7), which makes a
- * page copied verbatim into shared memory bank-conflict-free for 8x8 matrix
- * loads.  rkv_create zeroes the pool.
+ * RKV_SCHEME_EXACT_REBASE pre-RoPE keys (bf16); with the fp8 store
+ * (RKV_KV_E4M3) byte planes of key codes and value codes of the same shape
+ * and a (key, value) pair of float scales per row.  Stream s owns
+ * ceil(C_s / page_size) pages, C_s = W_s + window_slack the capacity of its
+ * ring; token j lives in ring slot j mod C_s, so eviction moves no data.
+ * Within a row of d 16-bit elements the 16-byte chunk c sits at chunk
+ * position c ^ (row offset in the page & 7), which makes a page copied
+ * verbatim into shared memory bank-conflict-free for 8x8 matrix loads.
+ * rkv_create zeroes the pool.
  */
 #ifndef RKV_H_
 #define RKV_H_
@@ -89,8 +92,8 @@ typedef enum {
   RKV_SCHEME_EXACT_REBASE = 1, /* K kept at window-relative positions, re-based on every roll */
   RKV_SCHEME_EXACT_ON_READ = 2 /* the same exact positions and re-base bookkeeping, but the re-base is
                                 * applied as attention reads: a key is stored once, rotated by its
-                                * ring slot index j mod W (positions stay below W however long the
-                                * stream runs), and the query is rotated by its offset from the ring
+                                * ring slot index j mod C (C = W + window_slack; positions stay below C
+                                * however long the stream runs), and the query is rotated by its offset from the ring
                                 * lap of each key, so no stored key is ever re-rotated (re-base moves
                                 * no bytes) */
 } rkv_scheme;
