@@ -179,8 +179,10 @@ RKV_API int rkv_create(const rkv_config* cfg, const int32_t* window, const int64
 
 /* Open a step for the streams in active_ids (host [n_active], distinct ids in
  * [0, S), 1 <= n_active <= S).  On the device, for each active stream:
- * n += Q; len = min(n, W); evicted = n - len; kv_pos_offset = P0 + evicted;
- * head_slot = evicted mod W; in the exact scheme, if evicted - rope_base >=
+ * n += Q; len = min(n, W) (with window_slack > 0: len grows to C = W +
+ * window_slack, then drops back to W in one batch); evicted = n - len;
+ * kv_pos_offset = P0 + evicted; head_slot = evicted mod C; in the exact
+ * schemes, if evicted - rope_base >=
  * rebase_interval, the step re-bases by delta = evicted - rope_base and
  * rope_base = evicted.  Then cos/sin of the new tokens' RoPE positions are
  * computed once for all layers (fp64 with error-free range reduction).
@@ -194,13 +196,14 @@ RKV_API int rkv_begin_step(rkv_handle* h, const int32_t* active_ids, int32_t n_a
  *      n_active, rows in active_ids order)
  *   v  device [A][Q][Hkv][d] bf16
  * Writes the key rotated to its position (logical P0 + j; j - rope_base in
- * RKV_SCHEME_EXACT_REBASE; its ring slot j mod W in RKV_SCHEME_EXACT_ON_READ)
- * into ring slot (token mod W) of each stream, stored as fp16 (round to
+ * RKV_SCHEME_EXACT_REBASE; its ring slot j mod C in RKV_SCHEME_EXACT_ON_READ)
+ * into ring slot (token mod C) of each stream, stored as fp16 (round to
  * nearest even; eleven significant bits, so a stored key adds ~2e-4 to a
  * unit-scale score, where bf16 would add ~1.6e-3), and v as given (bf16),
- * plus the pre-RoPE k in RKV_SCHEME_EXACT_REBASE.  A rotated key of
- * magnitude >= 65520 is reported as RKV_ERR_DEVICE_RANGE by rkv_sync_status.
- * Once per layer per step. */
+ * plus the pre-RoPE k in RKV_SCHEME_EXACT_REBASE.  With the fp8 store the
+ * rotated key and the value are written as e4m3 codes with their rows'
+ * scales (rkv_kv_format).  A rotated key of magnitude >= 65520 is reported
+ * as RKV_ERR_DEVICE_RANGE by rkv_sync_status.  Once per layer per step. */
 RKV_API int rkv_append_rope(rkv_handle* h, int32_t layer, const rkv_bf16* k, const rkv_bf16* v,
                             void* stream);
 
@@ -338,8 +341,9 @@ RKV_API int rkv_load_stream(rkv_handle* h, int32_t stream_id, const void* src, s
 /* Check a stream state record (RKV_STATE_FIELDS int64, the order of
  * rkv_get_stream_state) against the rules every step keeps under `cfg`:
  * W_s in [q_per_step, RKV_MAX_WINDOW], 0 <= P0 < 2^52, n >= 0 a multiple of
- * q_per_step with P0 + n < 2^52, len = min(n, W), evicted = n - len,
- * kv_pos_offset = P0 + evicted, head_slot = evicted mod W, and rope_base in
+ * q_per_step with P0 + n < 2^52, len = min(n, W) (with window_slack > 0:
+ * the batched rule of rkv_begin_step), evicted = n - len,
+ * kv_pos_offset = P0 + evicted, head_slot = evicted mod C, and rope_base in
  * (evicted - rebase_interval, evicted] for the exact schemes, 0 otherwise.
  * rkv_load_stream applies it to a snapshot before restoring it.  Host only:
  * RKV_OK, else RKV_ERR_CONFIG with the broken rule in rkv_last_error(NULL). */
