@@ -126,3 +126,24 @@ def test_rotate_fp32_is_the_fp64_rotation_rounded_per_operation():
     a, b = np.float32(k[3, 1, 2]), np.float32(k[3, 1, 6])
     assert got[3, 1, 2] == float(np.float32(np.float32(a * c32) - np.float32(b * s32)))
     assert got[3, 1, 6] == float(np.float32(np.float32(a * s32) + np.float32(b * c32)))
+
+
+def test_code_decisions_depend_on_the_rotation_precision():
+    """Why the store model rotates in fp32: over many bf16 rows near a rounding tie (small angles
+    keep a rotated bf16 value close to its 8-bit grid), rounding the fp64 rotation instead picks a
+    different code for a few elements (one e4m3 step apart, never more), so a model that skipped
+    the fp32 arithmetic would disagree with the store now and then by a whole code."""
+    torch = pytest.importorskip("torch")
+    from oracle.fp8 import rotate_fp32
+    from oracle.rope import rotate
+    rng = np.random.default_rng(21)
+    k = torch.tensor(rng.normal(size=(8000, 1, 64)), dtype=torch.float32).to(torch.bfloat16)
+    k = k.to(torch.float64).numpy()
+    pos = rng.integers(0, 64, size=8000).tolist()
+    a = quantize_rows(rotate(k, pos, 1e6))
+    b = quantize_rows(rotate_fp32(k, pos, 1e6))
+    diff = a != b
+    assert diff.any()                                   # the precision decides some codes
+    assert diff.mean() < 1e-4                           # but only a few
+    step = np.abs(b[diff]) * 2.0 ** -3                  # one code step at that magnitude, or less
+    assert np.all(np.abs(a[diff] - b[diff]) <= step + 1e-30)
